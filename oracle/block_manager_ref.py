@@ -1,0 +1,103 @@
+"""Naive block allocator: the oracle for the host-side block manager.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  Plain Python lists and
+dicts, one operation at a time, written from the pages:
+
+* Ultralytics glossary "PagedAttention", section "How paging works": a request
+  of n tokens takes ceil(n / block_size) blocks popped from the front of the
+  free list; a new block is taken only when the last one is full.
+* OptiVerse "Paged KV cache", section "Block table and non-contiguous
+  allocation": the table maps logical block i (tokens 16 i .. 16 i + 15) to a
+  physical block; the token after a 41-token prompt goes to offset 9 (the
+  10th position) of the third block; all blocks return to the pool when the
+  request ends.
+* iThome "how to store the KV cache", sections "Physical Block sharing" and
+  "Copy-on-Write": forked samples point at the same blocks with a reference
+  count; a writer into a shared, partly filled last block gets a fresh block
+  holding a copy, and the old block's count drops by one; full shared blocks
+  stay shared with unchanged counts.
+
+Readings where the pages are silent: freed blocks go to the back of the free
+list; writers are processed one at a time in call order, and a writer copies
+only while the block's count is above 1, so the last holder writes in place.
+"""
+from __future__ import annotations
+
+
+class OutOfBlocks(RuntimeError):
+    pass
+
+
+class RefBlockManager:
+    def __init__(self, num_blocks: int, block_size: int, free_list=None):
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        self.free = list(range(num_blocks)) if free_list is None else [int(b) for b in free_list]
+        self.ref = [0] * num_blocks
+        self.tables: dict[int, list[int]] = {}
+        self.lens: dict[int, int] = {}
+
+    def _take(self) -> int:
+        if not self.free:
+            raise OutOfBlocks("no free block")
+        b = self.free.pop(0)
+        self.ref[b] = 1
+        return b
+
+    def add_sequence(self, seq: int, num_tokens: int) -> list[int]:
+        """Give a new request ceil(num_tokens / bs) blocks (its prompt)."""
+        assert seq not in self.tables
+        need = -(-num_tokens // self.block_size)
+        if need > len(self.free):
+            raise OutOfBlocks(f"need {need} blocks, {len(self.free)} free")
+        self.tables[seq] = [self._take() for _ in range(need)]
+        self.lens[seq] = num_tokens
+        return list(self.tables[seq])
+
+    def append_slot(self, seq: int):
+        """Reserve the slot of the next token; return (slot, cow_pair or None)."""
+        table = self.tables[seq]
+        pos = self.lens[seq]
+        bs = self.block_size
+        cow = None
+        if pos % bs == 0:
+            table.append(self._take())
+        else:
+            last = table[pos // bs]
+            if self.ref[last] > 1:
+                new = self._take()
+                cow = (last, new)
+                self.ref[last] -= 1
+                table[pos // bs] = new
+        self.lens[seq] = pos + 1
+        return table[pos // bs] * bs + pos % bs, cow
+
+    def fork(self, parent: int, child: int) -> None:
+        """The child shares every block of the parent (counts + 1)."""
+        assert child not in self.tables
+        self.tables[child] = list(self.tables[parent])
+        self.lens[child] = self.lens[parent]
+        for b in self.tables[child]:
+            self.ref[b] += 1
+
+    def free_sequence(self, seq: int) -> None:
+        """Release a finished request: counts - 1, blocks at 0 go back to the pool."""
+        for b in self.tables.pop(seq):
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free.append(b)
+        del self.lens[seq]
+
+    def unused_slots(self, seq: int) -> int:
+        """Slots allocated to the request but not yet written."""
+        return len(self.tables[seq]) * self.block_size - self.lens[seq]
+
+
+def reserved_unused_slots(num_tokens: int, reservation: int) -> int:
+    """Slots left empty by a contiguous reservation of ``reservation`` tokens."""
+    return reservation - num_tokens
+
+
+def kv_bytes_per_sequence(layers: int, heads: int, head_dim: int, tokens: int, elem_bytes: int) -> int:
+    """K and V bytes of one sequence across all layers."""
+    return layers * heads * head_dim * 2 * elem_bytes * tokens
