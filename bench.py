@@ -1,0 +1,445 @@
+"""Benchmark: one paged decode step (KV append + paged attention) per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama7b] [--impl native|reference]
+
+A step is one pass of the hot path over one batch: the slot-mapped append of
+every sequence's new token (copy-on-write copies first when there are any),
+then paged decode attention over all context tokens (split-K partitions and
+their merge when a context spans several partitions).  The step is repeated on
+the same batch (each step rewrites the same slots), so every step does the
+same work.  Inputs are synthetic N(0,1), resident in HBM when the timed region
+starts, and larger than L2 (the K/V read per step is ~1.2 GB for llama7b).
+
+Prints one JSON line.  `value` is algorithmic bytes per step (K/V read through
+the tables, table entries, queries, outputs, the appended K/V) / device step
+time, in GB/s; `seq_steps_per_s` = sequences x steps / time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention achieved HBM GB/s (% of GB300 peak); seq-steps/sec"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+ELEM = {"f16": 2, "bf16": 2, "e4m3": 1}
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """Raw element bits of a tensor (uint16 or uint8 numpy array) for the oracle."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return t.view(torch.uint8).numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def algorithmic_bytes(wl, lens: np.ndarray):
+    """Bytes the method must move for one step (decode part, append part)."""
+    e = ELEM[wl.cache_dtype]
+    ea = ELEM[wl.act_dtype]
+    L = lens.astype(np.int64)
+    B = len(L)
+    kv = int(L.sum()) * 2 * wl.num_kv_heads * wl.head_dim * e
+    tables = int(np.sum(-(-L // wl.block_size))) * 4 + B * 4
+    qo = 2 * B * wl.num_q_heads * wl.head_dim * ea
+    decode = kv + tables + qo
+    append = B * wl.num_kv_heads * wl.head_dim * 2 * (ea + e) + B * 8
+    return decode, append
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.time(), parts))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t0, t1):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:
+            self.proc.kill()
+        rows = [r for t, r in self.rows if t0 - 0.25 <= t <= t1 + 0.25] or [r for _, r in self.rows]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return dist, dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+def _traffic(workload: str):
+    """dram bytes per decode launch from a committed ncu summary, if it still matches the kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        src = open(os.path.join(ROOT, "paged_kv_cache_102_gb300", "csrc", "decode.cuh"), "rb").read()
+        if t.get("decode_cuh_sha256") != hashlib.sha256(src).hexdigest() or t.get("workload") != workload:
+            return None
+        return float(t["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def setup(pkv, W, workload: str, seed: int, dev):
+    d = W.draw(workload, seed)
+    wl = d.workload
+    vals = W.make_values(d, device=dev)
+    B = len(d.context_lens)
+    ids = np.arange(B)
+    bm = pkv.BlockManager(d.num_blocks, wl.block_size, free_list=d.free_list)
+    for i, c in enumerate(d.context_lens):
+        bm.add_sequence(i, int(c))
+    slots, pairs = bm.append_slots(ids)
+    tables, lens = bm.tables(ids)
+    st = dict(d=d, wl=wl, vals=vals, bm=bm, ids=ids, slots_h=slots, tables_h=tables, lens_h=lens,
+              slots=torch.from_numpy(slots).to(dev), pairs=torch.from_numpy(pairs).to(dev),
+              tables=torch.from_numpy(tables).to(dev), lens=torch.from_numpy(lens).to(dev))
+    st["out"] = torch.empty_like(vals["q"])
+    return st
+
+
+def run_native(args):
+    import paged_kv_cache_102_gb300 as pkv
+    from paged_kv_cache_102_gb300 import workloads as W
+
+    dist, rank, world, local = _dist()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.load()
+    st = setup(pkv, W, args.workload, args.seed + rank, dev)
+    wl, vals = st["wl"], st["vals"]
+    B = len(st["ids"])
+    ps = args.partition_size
+    need = pkv.workspace_size(B, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, st["tables_h"].shape[1],
+                              wl.block_size, ps)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    max_parts = math.ceil(st["tables_h"].shape[1] * wl.block_size /
+                          pkv.resolve_partition_size(B, wl.num_kv_heads, st["tables_h"].shape[1], wl.block_size, ps))
+    ks, vs = vals.get("k_scale"), vals.get("v_scale")
+    stream = torch.cuda.current_stream(dev)
+    npairs = st["pairs"].shape[0]
+
+    def step(ev_mid=None):
+        if npairs:
+            pkv.paged_block_copy(vals["k_cache"], vals["v_cache"], st["pairs"])
+        pkv.paged_kv_append(vals["k_new"], vals["v_new"], st["slots"], vals["k_cache"], vals["v_cache"], ks, vs)
+        if ev_mid is not None:
+            ev_mid.record(stream)
+        pkv.paged_attention_decode(vals["q"], vals["k_cache"], vals["v_cache"], st["tables"], st["lens"], wl.scale,
+                                   out=st["out"], k_scale=ks, v_scale=vs, partition_size=ps, workspace=ws)
+
+    launches_per_step = (1 if npairs else 0) + 1 + 1 + (1 if max_parts > 1 else 0)
+    dec_bytes, app_bytes = algorithmic_bytes(wl, st["lens_h"])
+    step_bytes = dec_bytes + app_bytes
+
+    sampler = ClockSampler(dev.index if not os.environ.get("CUDA_VISIBLE_DEVICES") else
+                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    # keep the GPU busy long enough for the clock sampler to see it under load
+    t_soak = time.time()
+    while time.time() - t_soak < 0.6:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_start.record(stream)
+    for i in range(args.steps):
+        step(mids[i])
+        ends[i].record(stream)
+    ev_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    t1 = time.time()
+    ms_total = ev_start.elapsed_time(ev_end)
+    dec_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    clocks = sampler.stop(t_soak, t1)
+    if dist:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    ms_step = ms_total / args.steps
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    peak, peak_src = _peaks()
+    dec_avg_ms = statistics.mean(dec_ms)
+    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
+    traffic = _traffic(args.workload)
+
+    # end to end through the public API: pinned host inputs -> device, step, output -> host
+    e2e = None
+    if not args.no_e2e:
+        host = {k: vals[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
+        host["slots"] = st["slots"].cpu().pin_memory()
+        t_pin = torch.empty(st["tables_h"].shape, dtype=torch.int32).pin_memory()
+        l_pin = torch.empty(st["lens_h"].shape, dtype=torch.int32).pin_memory()
+        out_h = torch.empty(st["out"].shape, dtype=st["out"].dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(vals["q"]), torch.empty_like(vals["k_new"]), torch.empty_like(vals["v_new"])
+        dslots, dtab, dlens = torch.empty_like(st["slots"]), torch.empty_like(st["tables"]), torch.empty_like(st["lens"])
+        h2d = sum(t.numel() * t.element_size() for t in (*host.values(), t_pin, l_pin))
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            tab, lens = st["bm"].tables(st["ids"], st["tables_h"].shape[1])  # host block manager (C++)
+            t_pin.numpy()[...] = tab
+            l_pin.numpy()[...] = lens
+            dq.copy_(host["q"], non_blocking=True)
+            dk.copy_(host["k_new"], non_blocking=True)
+            dv.copy_(host["v_new"], non_blocking=True)
+            dslots.copy_(host["slots"], non_blocking=True)
+            dtab.copy_(t_pin, non_blocking=True)
+            dlens.copy_(l_pin, non_blocking=True)
+            pkv.paged_kv_append(dk, dv, dslots, vals["k_cache"], vals["v_cache"], ks, vs)
+            pkv.paged_attention_decode(dq, vals["k_cache"], vals["v_cache"], dtab, dlens, wl.scale, out=st["out"],
+                                       k_scale=ks, v_scale=vs, partition_size=ps, workspace=ws)
+            out_h.copy_(st["out"], non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        if dist:
+            dist.barrier()
+        te0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        te = (time.perf_counter() - te0) / args.steps
+        if dist:
+            t = torch.tensor([te], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            te = float(t.item())
+        e2e = {"value": round(step_bytes * world / te / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(te * 1e3, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "seq_steps_per_s": round(B * world / te, 1)}
+        if not torch.equal(out_h, st["out"].cpu()):
+            raise RuntimeError("e2e output differs from the device-resident step")
+
+    if pkv.device_error(reset=True, device=dev):
+        raise RuntimeError("a kernel flagged a device-side error during the benchmark")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(st, budget_s=args.cpu_budget)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.cache_dtype, "data": "synthetic N(0,1), seeded",
+        "config": {"workload": wl.name, "description": wl.description, "num_seqs": B,
+                   "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "block_size": wl.block_size, "act_dtype": wl.act_dtype, "cache_dtype": wl.cache_dtype,
+                   "mean_context": float(st["lens_h"].mean()), "total_context_tokens": int(st["lens_h"].sum()),
+                   "pool_blocks": st["d"].num_blocks,
+                   "partition_size": pkv.resolve_partition_size(B, wl.num_kv_heads, st["tables_h"].shape[1],
+                                                                wl.block_size, ps),
+                   "l2": "inputs larger than L2 (K/V read per step %.2f GB vs 129 MB L2)" % (dec_bytes / 1e9),
+                   "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
+        "pct_of_peak": round(100 * value / peak, 2),
+        "seq_steps_per_s": round(B * world / (ms_step * 1e-3), 1),
+        "bytes_per_step": {"decode": dec_bytes, "append": app_bytes},
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (partition + merge kernels)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic, "avg_launch_us": round(dec_avg_ms * 1e3, 3),
+                     "algorithmic_bytes_per_launch": dec_bytes},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(st, budget_s=20.0, max_seqs=None):
+    """The float64 oracle on a bounded sample of the same batch (host cores)."""
+    import oracle
+
+    wl, vals = st["wl"], st["vals"]
+    lens = st["lens_h"]
+    order = np.argsort(lens)[::-1] if max_seqs else np.arange(len(lens))
+    # time one sequence first to size the sample to the budget
+    idx = [int(order[0])]
+    code = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3}
+    kc, vc = bits(vals["k_cache"]), bits(vals["v_cache"])
+    ks = float(vals["k_scale"].item()) if "k_scale" in vals else 1.0
+    vs = float(vals["v_scale"].item()) if "v_scale" in vals else 1.0
+    q = bits(vals["q"])
+
+    def run(sel):
+        sel = np.asarray(sel)
+        t = time.perf_counter()
+        oracle.paged_decode(np.ascontiguousarray(q[sel]), code[wl.act_dtype], kc, vc, code[wl.cache_dtype],
+                            st["tables_h"][sel], lens[sel], wl.scale, k_scale=ks, v_scale=vs)
+        return time.perf_counter() - t
+
+    t1 = run(idx)
+    n = int(min(len(lens), max(1, budget_s / max(t1, 1e-6) * 0.8)))
+    sel = np.arange(len(lens))[:n]
+    t = run(sel)
+    e = ELEM[wl.cache_dtype]
+    kv = int(lens[sel].astype(np.int64).sum()) * 2 * wl.num_kv_heads * wl.head_dim * e
+    dec, _ = algorithmic_bytes(wl, lens[sel])
+    return {"value": round(dec / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"float64 oracle decode of {n} of {len(lens)} sequences of the {wl.name} batch "
+                      f"({kv / 1e9:.3f} GB of K/V) in {t:.2f} s",
+            "seconds": round(t, 3)}
+
+
+def run_reference(args):
+    """The reference arm: the float64 CPU oracle, timed on the host cores, same metric."""
+    dist, rank, world, local = _dist()
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_cache_102_gb300 import workloads as W
+    from oracle.block_manager_ref import RefBlockManager
+
+    oracle.build()
+    d = W.draw(args.workload, args.seed)
+    wl = d.workload
+    vals = W.make_values(d, device="cpu")
+    B = len(d.context_lens)
+    ref = RefBlockManager(d.num_blocks, wl.block_size, free_list=d.free_list)
+    for i, c in enumerate(d.context_lens):
+        ref.add_sequence(i, int(c))
+    slots = np.array([ref.append_slot(i)[0] for i in range(B)], np.int64)
+    maxb = max(len(t) for t in ref.tables.values())
+    tables = np.zeros((B, maxb), np.int32)
+    for i in range(B):
+        tables[i, : len(ref.tables[i])] = ref.tables[i]
+    lens = (d.context_lens + 1).astype(np.int32)
+    code = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3}
+    kc, vc = bits(vals["k_cache"]).copy(), bits(vals["v_cache"]).copy()
+    ks = float(vals["k_scale"].item()) if "k_scale" in vals else 1.0
+    vs = float(vals["v_scale"].item()) if "v_scale" in vals else 1.0
+    q = bits(vals["q"])
+    # size each step's sample so that warmup + steps take about budget seconds
+    t = time.perf_counter()
+    oracle.paged_decode(q[:1].copy(), code[wl.act_dtype], kc, vc, code[wl.cache_dtype], tables[:1], lens[:1],
+                        wl.scale, k_scale=ks, v_scale=vs)
+    t1 = max(time.perf_counter() - t, 1e-6) * float(lens.mean()) / float(lens[0])
+    per_step = args.cpu_budget / max(1, args.steps + args.warmup)
+    n = int(min(B, max(1, per_step / t1)))
+    sel = np.arange(n)
+
+    def step():
+        oracle.append(bits(vals["k_new"][sel]), bits(vals["v_new"][sel]), code[wl.act_dtype], slots[sel], kc, vc,
+                      code[wl.cache_dtype], k_scale=ks, v_scale=vs)
+        oracle.paged_decode(np.ascontiguousarray(q[sel]), code[wl.act_dtype], kc, vc, code[wl.cache_dtype],
+                            tables[sel], lens[sel], wl.scale, k_scale=ks, v_scale=vs)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    dec, app = algorithmic_bytes(wl, lens[sel])
+    value = (dec + app) / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic N(0,1), seeded",
+        "config": {"workload": wl.name, "description": wl.description, "sample_seqs": n, "num_seqs": B},
+        "seq_steps_per_s": round(n / dt, 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{n} of {B} sequences of the {wl.name} batch per step (append + decode)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="llama7b")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--partition-size", type=int, default=-1)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

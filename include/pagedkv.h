@@ -1,0 +1,248 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: paged KV-cache decode on GB300 (sm_103a).
+ *
+ * The KV cache lives in fixed-size physical blocks of a shared pool; each
+ * sequence owns a block table mapping its logical blocks to physical ones
+ * (Ultralytics glossary "PagedAttention", section "How paging works";
+ * OptiVerse "Paged KV cache", section "Block table and non-contiguous
+ * allocation").  This library provides the device side of that design --
+ * slot-mapped append, the attention kernel that reads K/V block by block
+ * through the table, the copy-on-write block copy -- and the host-side block
+ * manager that produces the tables and slot mappings.
+ *
+ * Conventions shared by every device entry point
+ *  - Pointers named *_cache, q, k, v, out, block_tables, context_lens,
+ *    slot_mapping, src_dst_pairs, workspace, k_scale, v_scale are DEVICE
+ *    pointers owned by the caller; the library keeps no reference to them
+ *    after the call and never frees them.  All device buffers must be
+ *    16-byte aligned.
+ *  - Cache layout: k_cache and v_cache are separate row-major arrays
+ *    [num_blocks][num_kv_heads][block_size][head_dim] of the cache element
+ *    type.  One (block, kv-head) tile is block_size*head_dim contiguous
+ *    elements.  Flat slot s means block s / block_size, offset s % block_size.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every device call only enqueues work on that stream and
+ *    returns; it is ordered with other work on the same stream.
+ *  - Return value: PKV_OK, or an error code below with a message available
+ *    from pkv_last_error() (per host thread).  An argument error enqueues
+ *    nothing.
+ *  - Index errors that can only be seen on the device (a block id outside
+ *    the pool, a context length outside 1..max_blocks_per_seq*block_size,
+ *    a slot outside the pool) make the kernel skip the offending access and
+ *    set a bit in a per-device error word, read with pkv_device_error().
+ *
+ * Element types: PKV_F16 (IEEE binary16), PKV_BF16 (bfloat16), PKV_E4M3
+ * (OCP FP8 E4M3, cache only; per-tensor float32 scales, value = code*scale).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1, PKV_E4M3 = 2 };
+
+enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = 1,   /* null pointer, unsupported type/head_dim/block_size/group, misalignment */
+    PKV_ERR_SHAPE = 2,     /* inconsistent sizes (e.g. num_q_heads not a multiple of num_kv_heads) */
+    PKV_ERR_CUDA = 3,      /* a CUDA runtime call or kernel launch failed */
+    PKV_ERR_NO_SPACE = 4,  /* block manager: not enough free blocks; state unchanged */
+    PKV_ERR_NOT_FOUND = 5  /* block manager: unknown or duplicate sequence id */
+};
+
+/* Bits of the per-device error word (pkv_device_error). */
+enum pkv_device_error_bits {
+    PKV_DEV_BAD_BLOCK = 1,       /* decode: block table entry outside [0, num_blocks) */
+    PKV_DEV_BAD_CONTEXT_LEN = 2, /* decode: context length outside 1..max_blocks_per_seq*block_size */
+    PKV_DEV_BAD_SLOT = 4,        /* append: slot >= num_blocks*block_size */
+    PKV_DEV_BAD_PAIR = 8,        /* block copy: src or dst outside [0, num_blocks) */
+    PKV_DEV_WAIT_TIMEOUT = 16    /* a kernel gave up waiting on an on-chip barrier (about 2 s) */
+};
+
+/* Partition-size selectors for paged_attention_decode. */
+#define PKV_PARTITION_SINGLE 0 /* one pass over the whole context per (sequence, kv head) */
+#define PKV_PARTITION_AUTO (-1) /* the library picks the partition size */
+
+/*
+ * paged_kv_append -- write each new token's K and V into its slot.
+ * Defined by the Ultralytics glossary "PagedAttention", section "How paging
+ * works" (position pos of a request goes to block_table[pos // block_size],
+ * offset pos % block_size) and OptiVerse "Paged KV cache", section "Block
+ * table and non-contiguous allocation" (token 41 of a 41-token request goes
+ * to the 10th position of its third block).
+ *
+ *  k, v          [num_tokens][num_kv_heads][head_dim] of act_dtype (device).
+ *  slot_mapping  int64 [num_tokens] (device): flat slot of each token;
+ *                a negative slot skips the token (padding).
+ *  k_cache, v_cache  the pools, cache_dtype (device, written).
+ *  cache_dtype   == act_dtype: bytes are copied unchanged (bit-exact);
+ *                PKV_E4M3 with act_dtype F16/BF16: each element x is stored
+ *                as e4m3(x / scale) -- binary32 division, round to nearest
+ *                even, saturating to +-448 -- with scale = *k_scale for K and
+ *                *v_scale for V (device float32 scalars; ignored otherwise).
+ *  head_dim      a multiple of 8 (any block_size >= 1).
+ * Slots >= num_blocks*block_size are skipped and flag PKV_DEV_BAD_SLOT.
+ * Two tokens mapped to the same slot in one call race (one of them wins).
+ */
+int paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                    void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int block_size,
+                    int head_dim, int act_dtype, int cache_dtype, const float* k_scale,
+                    const float* v_scale, void* stream);
+
+/*
+ * paged_attention_decode -- one decode step of attention over a paged cache.
+ * The attention kernel gathers each sequence's keys and values block by
+ * block through its block table (Ultralytics glossary "PagedAttention",
+ * section "How paging works"; OptiVerse "Paged KV cache", section "Block
+ * table and non-contiguous allocation"); query heads share KV heads in
+ * groups (Ultralytics glossary, section "Related techniques": grouped-query
+ * attention).  For sequence b with L = context_lens[b] tokens and query head
+ * h (kv head h / (num_q_heads/num_kv_heads)):
+ *     s_j = scale * <q[b][h], K_b[j]>,  p = softmax(s),  out[b][h] = sum_j p_j V_b[j]
+ * with K_b[j] = k_cache[block_tables[b][j / block_size]][kvh][j % block_size]
+ * (times *k_scale for an E4M3 cache; likewise V).  fp32 online softmax and
+ * accumulation; the output is rounded once to act_dtype.
+ *
+ *  q             [num_seqs][num_q_heads][head_dim] of act_dtype (device).
+ *  block_tables  int32 [num_seqs][max_blocks_per_seq] (device); only the
+ *                first ceil(L/block_size) entries of a row are read.
+ *  context_lens  int32 [num_seqs] (device), each in 1..max_blocks_per_seq*block_size.
+ *  out           [num_seqs][num_q_heads][head_dim] of act_dtype (device, written).
+ *  act_dtype     PKV_F16 or PKV_BF16; cache_dtype == act_dtype or PKV_E4M3.
+ *  head_dim      64 or 128; block_size 16 or 32; group num_q_heads/num_kv_heads
+ *                in {1, 2, 4, 8}.
+ *  partition_size  PKV_PARTITION_SINGLE (0): one pass per (sequence, kv head);
+ *                PKV_PARTITION_AUTO (-1): library choice; > 0: split each
+ *                context into partitions of that many tokens (a multiple of
+ *                32 and of block_size), attended independently and merged by
+ *                their log-sum-exp weights (split-K).
+ *  workspace     device scratch of at least pkv_workspace_size(...) bytes
+ *                when more than one partition is possible; may be NULL when
+ *                that size is 0.  Its contents need no initialisation and
+ *                are undefined after the call; calls sharing a workspace
+ *                must be ordered (same stream).
+ */
+int paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int block_size, int head_dim, int num_blocks,
+                           float scale, void* out, int act_dtype, int cache_dtype,
+                           const float* k_scale, const float* v_scale, int partition_size,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pkv_workspace_size -- bytes of workspace paged_attention_decode needs for
+ * these sizes and partition_size: 0 when every sequence fits one partition,
+ * otherwise room for each (sequence, query head, partition)'s running max,
+ * running sum and normalised partial output in float32.  Host only.
+ */
+size_t pkv_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int max_blocks_per_seq, int block_size, int partition_size);
+
+/*
+ * pkv_resolve_partition_size -- the partition size in tokens that
+ * paged_attention_decode uses for these arguments (a value >= the longest
+ * possible context means a single pass), or -1 if partition_size is not
+ * accepted.  Host only.
+ */
+int pkv_resolve_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
+                               int block_size, int partition_size);
+
+/*
+ * paged_block_copy -- copy whole physical blocks for copy-on-write.
+ * iThome "how to store the KV cache", section "Copy-on-Write": when a
+ * sequence writes into a shared, partly filled block, it gets a new block
+ * holding a copy of the old contents.  For each pair i, block
+ * src_dst_pairs[2i] is copied to block src_dst_pairs[2i+1] in both caches
+ * (all kv heads, all slots): block_bytes = num_kv_heads*block_size*head_dim*
+ * element size of one cache.  Pairs run concurrently: a block must not be
+ * both a destination and a source (or two destinations) in one call.
+ *  src_dst_pairs int32 [num_pairs][2] (device).  block_bytes must be a
+ *                multiple of 16.  num_pairs == 0 enqueues nothing.
+ * Pairs with an id outside [0, num_blocks) are skipped and flag PKV_DEV_BAD_PAIR.
+ */
+int paged_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int num_pairs,
+                     int num_blocks, size_t block_bytes, void* stream);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* pkv_last_error(void);
+
+/*
+ * pkv_device_error -- read (and, if reset != 0, clear) the per-device error
+ * word of the current device: an OR of pkv_device_error_bits set by kernels
+ * since the last reset.  Synchronises `stream` first.  Returns PKV_OK or
+ * PKV_ERR_CUDA.
+ */
+int pkv_device_error(int* bits, int reset, void* stream);
+
+/* Library ABI version (major*100 + minor). */
+int pkv_version(void);
+
+/* ------------------------------------------------------------------------
+ * Host-side block manager (no GPU work).  A free pool of physical block ids
+ * popped first-in first-out, a reference count per block, one block table
+ * per sequence, copy-on-write of a shared last block.
+ *  - Ultralytics glossary "PagedAttention", section "How paging works": a
+ *    request of n tokens takes ceil(n / block_size) blocks; a new block is
+ *    taken only when the last one is full.
+ *  - OptiVerse "Paged KV cache", section "Block table and non-contiguous
+ *    allocation": blocks return to the pool when the request ends.
+ *  - iThome "how to store the KV cache", sections "Physical Block sharing"
+ *    and "Copy-on-Write": forked sequences share blocks with a reference
+ *    count; a writer into a shared, partly filled last block gets a new
+ *    block (reported as a (src, dst) copy pair) and the old block's count
+ *    drops by one; full shared blocks are never copied.
+ * Sequence ids are caller-chosen int64 values.  Not thread-safe: one
+ * manager per thread, or external locking.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* Create a manager over num_blocks blocks of block_size tokens.  free_list
+ * (host, may be NULL) gives the initial free blocks in pop order; NULL means
+ * 0..num_blocks-1.  Returns NULL on invalid arguments. */
+pkv_block_manager* pkv_bm_create(int num_blocks, int block_size, const int32_t* free_list,
+                                 int free_list_len);
+void pkv_bm_destroy(pkv_block_manager* bm);
+
+/* Register a new sequence holding num_tokens tokens (>= 0): allocates
+ * ceil(num_tokens/block_size) blocks.  PKV_ERR_NO_SPACE leaves no trace. */
+int pkv_bm_add_sequence(pkv_block_manager* bm, int64_t seq_id, int num_tokens);
+
+/* Reserve the next token's slot for each of n distinct sequences, in array
+ * order.  slots_out (host int64 [n]) gets the flat slots; cow_pairs_out
+ * (host int32 [2n]) gets the (src, dst) copies to run with paged_block_copy
+ * BEFORE the append, and *num_cow_pairs their count.  All or nothing:
+ * PKV_ERR_NO_SPACE if the pool cannot cover the whole batch. */
+int pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n, int64_t* slots_out,
+                        int32_t* cow_pairs_out, int* num_cow_pairs);
+
+/* Child shares all of parent's blocks (counts + 1) and its length. */
+int pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_id);
+
+/* Release a sequence: counts - 1; blocks reaching 0 go to the back of the free list. */
+int pkv_bm_free_sequence(pkv_block_manager* bm, int64_t seq_id);
+
+/* Write the block tables (host int32 [n][max_blocks_per_seq], unused
+ * entries = pad) and context lengths (host int32 [n], may be NULL) of n
+ * sequences.  PKV_ERR_SHAPE if a table is longer than max_blocks_per_seq. */
+int pkv_bm_get_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
+                      int32_t* tables_out, int max_blocks_per_seq, int32_t pad,
+                      int32_t* context_lens_out);
+
+int pkv_bm_num_free(const pkv_block_manager* bm);
+int pkv_bm_ref_count(const pkv_block_manager* bm, int block); /* -1 if out of range */
+int pkv_bm_context_len(const pkv_block_manager* bm, int64_t seq_id); /* -1 if unknown */
+int pkv_bm_num_seq_blocks(const pkv_block_manager* bm, int64_t seq_id); /* -1 if unknown */
+/* Copy the free list, in pop order, into out (capacity cap); returns its length. */
+int pkv_bm_free_list(const pkv_block_manager* bm, int32_t* out, int cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,245 @@
+"""Paged KV-cache decode on GB300 (sm_103a).
+
+Python binding over the C ABI of ``libpagedkv.so`` (include/pagedkv.h).  The
+functions here only marshal torch tensors into pointers and sizes; all device
+work runs in the library's CUDA kernels, and the block manager runs in the
+library's C++ host code.  There is no CPU fallback: a missing library raises.
+
+    paged_kv_append(k, v, slot_mapping, k_cache, v_cache, ...)
+    paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ...)
+    paged_block_copy(k_cache, v_cache, src_dst_pairs, ...)
+    BlockManager(num_blocks, block_size, free_list=None)
+
+Cache tensors are [num_blocks, num_kv_heads, block_size, head_dim], float16 or
+bfloat16, or uint8 / float8_e4m3fn holding E4M3 codes with float32 per-tensor
+scales (1-element CUDA tensors).
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import numpy as np
+import torch
+
+from . import _native
+from ._native import PagedKVError
+
+F16, BF16, E4M3 = 0, 1, 2
+PARTITION_SINGLE = 0
+PARTITION_AUTO = -1
+
+ERR_INVALID, ERR_SHAPE, ERR_CUDA, ERR_NO_SPACE, ERR_NOT_FOUND = 1, 2, 3, 4, 5
+DEV_BAD_BLOCK, DEV_BAD_CONTEXT_LEN, DEV_BAD_SLOT, DEV_BAD_PAIR, DEV_WAIT_TIMEOUT = 1, 2, 4, 8, 16
+
+__all__ = ["paged_kv_append", "paged_attention_decode", "paged_block_copy", "workspace_size",
+           "resolve_partition_size", "device_error", "BlockManager", "OutOfBlocks", "PagedKVError",
+           "F16", "BF16", "E4M3", "PARTITION_SINGLE", "PARTITION_AUTO", "load"]
+
+
+class OutOfBlocks(PagedKVError):
+    pass
+
+
+def load():
+    """Load libpagedkv.so (raises if it was not built)."""
+    return _native.lib()
+
+
+def _code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return F16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return E4M3
+    raise TypeError(f"unsupported element type {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require_cuda(device, **tensors):
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda or t.device != device:
+            raise ValueError(f"{name} must be a CUDA tensor on {device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
+def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None, stream=None):
+    """Write k, v [T, Hkv, D] into their slots (int64 [T], negative = skip)."""
+    T, Hkv, D = k.shape
+    NB, Hkv2, bs, D2 = k_cache.shape
+    if v.shape != k.shape or v_cache.shape != k_cache.shape or Hkv2 != Hkv or D2 != D:
+        raise ValueError("paged_kv_append: shape mismatch")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.shape != (T,):
+        raise ValueError("paged_kv_append: slot_mapping must be int64 [num_tokens]")
+    _require_cuda(k.device, k=k, v=v, slot_mapping=slot_mapping, k_cache=k_cache, v_cache=v_cache,
+                  k_scale=k_scale, v_scale=v_scale)
+    _native.call("paged_kv_append", _ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
+                 NB, Hkv, bs, D, _code(k), _code(k_cache), _ptr(k_scale), _ptr(v_scale),
+                 _stream(stream, k.device))
+
+
+def resolve_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, partition_size=PARTITION_AUTO):
+    return int(_native.lib().pkv_resolve_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
+                                                        partition_size))
+
+
+def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+                   partition_size=PARTITION_AUTO) -> int:
+    return int(_native.lib().pkv_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                max_blocks_per_seq, block_size, partition_size))
+
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def _workspace(device, stream_ptr: int, nbytes: int) -> torch.Tensor:
+    """A reusable workspace per (device, stream): calls on one stream are ordered."""
+    key = (device.index, stream_ptr)
+    with _ws_lock:
+        buf = _ws_cache.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+            _ws_cache[key] = buf
+        return buf
+
+
+def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, k_scale=None,
+                           v_scale=None, partition_size=PARTITION_AUTO, workspace=None, stream=None):
+    """Decode attention for q [B, Hq, D] over the paged cache; returns out [B, Hq, D]."""
+    B, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("paged_attention_decode: shape mismatch")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("paged_attention_decode: block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("paged_attention_decode: block_tables [B, max_blocks], context_lens [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("paged_attention_decode: out must match q")
+    _require_cuda(q.device, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+                  context_lens=context_lens, out=out, k_scale=k_scale, v_scale=v_scale, workspace=workspace)
+    max_blocks = block_tables.shape[1]
+    s = _stream(stream, q.device)
+    need = workspace_size(B, Hq, Hkv, D, max_blocks, bs, partition_size)
+    if need and workspace is None:
+        workspace = _workspace(q.device, s.value or 0, need)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _native.call("paged_attention_decode", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks,
+                 _ptr(context_lens), B, Hq, Hkv, bs, D, NB, float(scale), _ptr(out), _code(q), _code(k_cache),
+                 _ptr(k_scale), _ptr(v_scale), int(partition_size), _ptr(workspace), ws_bytes, s)
+    return out
+
+
+def paged_block_copy(k_cache, v_cache, src_dst_pairs, stream=None):
+    """Copy whole blocks (K and V) for each (src, dst) row of int32 [P, 2]."""
+    if src_dst_pairs.dtype != torch.int32 or src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
+        raise ValueError("paged_block_copy: src_dst_pairs must be int32 [P, 2]")
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
+        raise ValueError("paged_block_copy: k_cache and v_cache must match")
+    _require_cuda(k_cache.device, k_cache=k_cache, v_cache=v_cache, src_dst_pairs=src_dst_pairs)
+    block_bytes = k_cache[0].numel() * k_cache.element_size()
+    _native.call("paged_block_copy", _ptr(k_cache), _ptr(v_cache), _ptr(src_dst_pairs), src_dst_pairs.shape[0],
+                 k_cache.shape[0], block_bytes, _stream(stream, k_cache.device))
+
+
+def device_error(reset: bool = True, stream=None, device=None) -> int:
+    """Read (and by default clear) the current device's kernel error bits."""
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    bits = ctypes.c_int(0)
+    _native.call("pkv_device_error", ctypes.byref(bits), int(reset), _stream(stream, device))
+    return bits.value
+
+
+class BlockManager:
+    """Host-side block allocator (C++ in libpagedkv.so): FIFO free list,
+    per-block reference counts, copy-on-write of a shared last block."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_list=None):
+        lib = _native.lib()
+        fl = None if free_list is None else np.ascontiguousarray(free_list, dtype=np.int32)
+        self._h = lib.pkv_bm_create(num_blocks, block_size,
+                                    None if fl is None else fl.ctypes.data_as(ctypes.c_void_p),
+                                    0 if fl is None else len(fl))
+        if not self._h:
+            raise PagedKVError("pkv_bm_create", 1, lib.pkv_last_error().decode())
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            _native.lib().pkv_bm_destroy(h)
+            self._h = None
+
+    def _check(self, func, code):
+        if code == ERR_NO_SPACE:
+            raise OutOfBlocks(func, code, _native.lib().pkv_last_error().decode())
+        _native.check(func, code)
+
+    def add_sequence(self, seq_id: int, num_tokens: int) -> None:
+        self._check("pkv_bm_add_sequence", _native.lib().pkv_bm_add_sequence(self._h, int(seq_id), int(num_tokens)))
+
+    def append_slots(self, seq_ids):
+        """Reserve the next slot of each sequence; returns (slots int64 [n], cow_pairs int32 [k, 2])."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = len(ids)
+        slots = np.empty(n, np.int64)
+        pairs = np.empty((max(n, 1), 2), np.int32)
+        npairs = ctypes.c_int(0)
+        self._check("pkv_bm_append_slots", _native.lib().pkv_bm_append_slots(
+            self._h, ids.ctypes.data_as(ctypes.c_void_p), n, slots.ctypes.data_as(ctypes.c_void_p),
+            pairs.ctypes.data_as(ctypes.c_void_p), ctypes.byref(npairs)))
+        return slots, pairs[: npairs.value].copy()
+
+    def fork(self, parent_id: int, child_id: int) -> None:
+        self._check("pkv_bm_fork", _native.lib().pkv_bm_fork(self._h, int(parent_id), int(child_id)))
+
+    def free_sequence(self, seq_id: int) -> None:
+        self._check("pkv_bm_free_sequence", _native.lib().pkv_bm_free_sequence(self._h, int(seq_id)))
+
+    def tables(self, seq_ids, max_blocks_per_seq: int | None = None, pad: int = 0):
+        """Block tables int32 [n, max_blocks_per_seq] (pad-filled) and context lengths int32 [n]."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        if max_blocks_per_seq is None:
+            max_blocks_per_seq = max([self.num_seq_blocks(s) for s in ids] + [1])
+        t = np.empty((len(ids), max_blocks_per_seq), np.int32)
+        lens = np.empty(len(ids), np.int32)
+        self._check("pkv_bm_get_tables", _native.lib().pkv_bm_get_tables(
+            self._h, ids.ctypes.data_as(ctypes.c_void_p), len(ids), t.ctypes.data_as(ctypes.c_void_p),
+            max_blocks_per_seq, pad, lens.ctypes.data_as(ctypes.c_void_p)))
+        return t, lens
+
+    @property
+    def num_free(self) -> int:
+        return int(_native.lib().pkv_bm_num_free(self._h))
+
+    def ref_count(self, block: int) -> int:
+        return int(_native.lib().pkv_bm_ref_count(self._h, int(block)))
+
+    def context_len(self, seq_id: int) -> int:
+        return int(_native.lib().pkv_bm_context_len(self._h, int(seq_id)))
+
+    def num_seq_blocks(self, seq_id: int) -> int:
+        return int(_native.lib().pkv_bm_num_seq_blocks(self._h, int(seq_id)))
+
+    def free_list(self) -> np.ndarray:
+        n = int(_native.lib().pkv_bm_free_list(self._h, None, 0))
+        out = np.empty(n, np.int32)
+        _native.lib().pkv_bm_free_list(self._h, out.ctypes.data_as(ctypes.c_void_p), n)
+        return out

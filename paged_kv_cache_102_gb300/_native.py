@@ -1,0 +1,79 @@
+"""ctypes loader for libpagedkv.so (built in-tree by ``build.py``).
+
+There is no fallback: if the library is missing or fails to load, every call
+raises.  Argument types mirror include/pagedkv.h one to one.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
+
+_lock = threading.Lock()
+_lib = None
+
+P = ctypes.c_void_p
+I32 = ctypes.c_int
+I64 = ctypes.c_int64
+SZ = ctypes.c_size_t
+F32 = ctypes.c_float
+
+# name -> (restype, argtypes), in the order of include/pagedkv.h
+SIGNATURES = {
+    "paged_kv_append": (I32, [P, P, P, I32, P, P, I32, I32, I32, I32, I32, I32, P, P, P]),
+    "paged_attention_decode": (I32, [P, P, P, P, I32, P, I32, I32, I32, I32, I32, I32, F32, P, I32, I32, P, P,
+                                     I32, P, SZ, P]),
+    "pkv_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
+    "pkv_resolve_partition_size": (I32, [I32, I32, I32, I32, I32]),
+    "paged_block_copy": (I32, [P, P, P, I32, I32, SZ, P]),
+    "pkv_last_error": (ctypes.c_char_p, []),
+    "pkv_device_error": (I32, [P, I32, P]),
+    "pkv_version": (I32, []),
+    "pkv_bm_create": (P, [I32, I32, P, I32]),
+    "pkv_bm_destroy": (None, [P]),
+    "pkv_bm_add_sequence": (I32, [P, I64, I32]),
+    "pkv_bm_append_slots": (I32, [P, P, I32, P, P, P]),
+    "pkv_bm_fork": (I32, [P, I64, I64]),
+    "pkv_bm_free_sequence": (I32, [P, I64]),
+    "pkv_bm_get_tables": (I32, [P, P, I32, P, I32, I32, P]),
+    "pkv_bm_num_free": (I32, [P]),
+    "pkv_bm_ref_count": (I32, [P, I32]),
+    "pkv_bm_context_len": (I32, [P, I64]),
+    "pkv_bm_num_seq_blocks": (I32, [P, I64]),
+    "pkv_bm_free_list": (I32, [P, P, I32]),
+}
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, func: str, code: int, msg: str):
+        super().__init__(f"{func} failed with status {code}: {msg}")
+        self.code = code
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: run paged_kv_cache_102_gb300.build.build() "
+                                  "(or __graft_entry__.build()) first; there is no CPU fallback")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def check(func: str, code: int) -> None:
+    if code != 0:
+        raise PagedKVError(func, code, lib().pkv_last_error().decode())
+
+
+def call(func: str, *args) -> None:
+    check(func, getattr(lib(), func)(*args))

@@ -1,0 +1,241 @@
+// C-ABI entry points of libpagedkv.so: argument checks, partition-size
+// choice, workspace carving and kernel dispatch.  Declarations and the
+// contract of each call are in include/pagedkv.h.
+#include <cmath>
+#include <mutex>
+#include <string>
+
+#include "../../include/pagedkv.h"
+#include "kernels.h"
+#include "pkv_error.h"
+
+// Per-device error word written by the kernels (OR of pkv_device_error_bits).
+static __device__ int g_pkv_device_error;
+
+namespace pkv {
+
+namespace {
+thread_local std::string t_last_error;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device address of g_pkv_device_error on the current device.
+int* device_error_word() {
+    static std::mutex mu;
+    static int* addr[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pkv_device_error) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<int*>(p);
+    }
+    return addr[dev];
+}
+
+int cuda_fail(const char* where, cudaError_t e) {
+    return fail(PKV_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr int kStageTokens = 32;  // tokens per shared-memory stage of the decode kernel
+constexpr int kAutoPartition = 512;
+
+}  // namespace
+
+void set_error(const std::string& msg) { t_last_error = msg; }
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_last_error(void) { return t_last_error.c_str(); }
+
+int pkv_version(void) { return 100; }
+
+int pkv_device_error(int* bits, int reset, void* stream) {
+    if (!bits) return fail(PKV_ERR_INVALID, "pkv_device_error: bits is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail("pkv_device_error: stream synchronize", e);
+    int* word = device_error_word();
+    if (!word) return fail(PKV_ERR_CUDA, "pkv_device_error: cannot resolve the device error word");
+    e = cudaMemcpy(bits, word, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail("pkv_device_error: read", e);
+    if (reset) {
+        e = cudaMemset(word, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail("pkv_device_error: reset", e);
+    }
+    return PKV_OK;
+}
+
+int pkv_resolve_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int block_size,
+                               int partition_size) {
+    (void)num_seqs;
+    (void)num_kv_heads;
+    if (max_blocks_per_seq < 1 || block_size < 1) return -1;
+    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+    const long long single = (max_ctx + kStageTokens - 1) / kStageTokens * kStageTokens;
+    long long P;
+    if (partition_size == PKV_PARTITION_SINGLE) {
+        P = single;
+    } else if (partition_size == PKV_PARTITION_AUTO) {
+        P = kAutoPartition;
+    } else if (partition_size > 0) {
+        if (partition_size % kStageTokens != 0 || partition_size % block_size != 0) return -1;
+        P = partition_size;
+    } else {
+        return -1;
+    }
+    if (P >= single) P = single;
+    if (P > 0x7fffffff) return -1;
+    return static_cast<int>(P);
+}
+
+size_t pkv_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int max_blocks_per_seq, int block_size, int partition_size) {
+    const int P = pkv_resolve_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
+                                             partition_size);
+    if (P <= 0 || num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+    const long long parts = (max_ctx + P - 1) / P;
+    if (parts <= 1) return 0;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * static_cast<size_t>(parts);
+    return align_up(rows * 2 * sizeof(float), 256) + rows * static_cast<size_t>(head_dim) * sizeof(float);
+}
+
+int paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens, void* k_cache,
+                    void* v_cache, int num_blocks, int num_kv_heads, int block_size, int head_dim, int act_dtype,
+                    int cache_dtype, const float* k_scale, const float* v_scale, void* stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0 || head_dim <= 0 ||
+        head_dim % 8 != 0)
+        return fail(PKV_ERR_INVALID, "paged_kv_append: sizes must be positive and head_dim a multiple of 8");
+    if (act_dtype != PKV_F16 && act_dtype != PKV_BF16)
+        return fail(PKV_ERR_INVALID, "paged_kv_append: act_dtype must be PKV_F16 or PKV_BF16");
+    if (cache_dtype != act_dtype && cache_dtype != PKV_E4M3)
+        return fail(PKV_ERR_INVALID, "paged_kv_append: cache_dtype must equal act_dtype or be PKV_E4M3");
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+        return fail(PKV_ERR_INVALID, "paged_kv_append: null pointer");
+    if (cache_dtype == PKV_E4M3 && (!k_scale || !v_scale))
+        return fail(PKV_ERR_INVALID, "paged_kv_append: an E4M3 cache needs k_scale and v_scale");
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return fail(PKV_ERR_INVALID, "paged_kv_append: buffers must be 16-byte aligned (slot_mapping 8)");
+    int* err = device_error_word();
+    if (!err) return fail(PKV_ERR_CUDA, "paged_kv_append: cannot resolve the device error word");
+    AppendParams p{k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, err,
+                   num_tokens, num_kv_heads, head_dim, block_size, num_blocks};
+    cudaError_t e = launch_append(p, act_dtype, cache_dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("paged_kv_append: launch", e);
+    return PKV_OK;
+}
+
+int paged_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int num_pairs, int num_blocks,
+                     size_t block_bytes, void* stream) {
+    if (num_pairs < 0 || num_blocks <= 0 || block_bytes == 0 || block_bytes % 16 != 0)
+        return fail(PKV_ERR_INVALID, "paged_block_copy: num_pairs >= 0, num_blocks > 0, block_bytes a positive multiple of 16");
+    if (num_pairs == 0) return PKV_OK;
+    if (num_pairs > 65535 * 64) return fail(PKV_ERR_INVALID, "paged_block_copy: too many pairs in one call");
+    if (!k_cache || !v_cache || !src_dst_pairs) return fail(PKV_ERR_INVALID, "paged_block_copy: null pointer");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_dst_pairs, 4))
+        return fail(PKV_ERR_INVALID, "paged_block_copy: caches must be 16-byte aligned");
+    int* err = device_error_word();
+    if (!err) return fail(PKV_ERR_CUDA, "paged_block_copy: cannot resolve the device error word");
+    CopyParams p{k_cache, v_cache, src_dst_pairs, err, block_bytes, num_blocks};
+    cudaError_t e = launch_block_copy(p, num_pairs, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("paged_block_copy: launch", e);
+    return PKV_OK;
+}
+
+int paged_attention_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int block_size, int head_dim, int num_blocks, float scale, void* out,
+                           int act_dtype, int cache_dtype, const float* k_scale, const float* v_scale,
+                           int partition_size, void* workspace, size_t workspace_bytes, void* stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: sizes must be positive");
+    if (num_q_heads % num_kv_heads != 0)
+        return fail(PKV_ERR_SHAPE, "paged_attention_decode: num_q_heads must be a multiple of num_kv_heads");
+    const int G = num_q_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: query heads per kv head must be 1, 2, 4 or 8");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: head_dim must be 64 or 128");
+    if (block_size != 16 && block_size != 32)
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: block_size must be 16 or 32");
+    if (act_dtype != PKV_F16 && act_dtype != PKV_BF16)
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: act_dtype must be PKV_F16 or PKV_BF16");
+    if (cache_dtype != act_dtype && cache_dtype != PKV_E4M3)
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: cache_dtype must equal act_dtype or be PKV_E4M3");
+    if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID, "paged_attention_decode: scale must be finite");
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: null pointer");
+    if (cache_dtype == PKV_E4M3 && (!k_scale || !v_scale))
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: an E4M3 cache needs k_scale and v_scale");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(workspace, 16))
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: q, caches, out, workspace must be 16-byte aligned");
+    const int P = pkv_resolve_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, partition_size);
+    if (P <= 0)
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: partition_size must be 0, -1 or a positive multiple of 32 and of block_size");
+    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+    if (max_ctx > 0x7fffffffLL) return fail(PKV_ERR_INVALID, "paged_attention_decode: table too long");
+    const int max_parts = static_cast<int>((max_ctx + P - 1) / P);
+    if (max_parts > 65535 || num_kv_heads > 65535 || num_seqs > 65535)
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: grid too large (partitions, kv heads or sequences > 65535)");
+    const size_t need = pkv_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                           block_size, partition_size);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: workspace of " + std::to_string(need) +
+                                         " bytes required (pkv_workspace_size)");
+    int* err = device_error_word();
+    if (!err) return fail(PKV_ERR_CUDA, "paged_attention_decode: cannot resolve the device error word");
+
+    DecodeParams p{};
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = out;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * static_cast<size_t>(max_parts);
+    p.ws_ml = need ? static_cast<float*>(workspace) : nullptr;
+    p.ws_o = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * 2 * sizeof(float), 256))
+                  : nullptr;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.err = err;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.partition_size = P;
+    p.max_parts = max_parts;
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (act_dtype == PKV_F16)
+        e = cache_dtype == PKV_E4M3 ? launch_decode_f16_e4m3(p, head_dim, block_size, G, s)
+                                    : launch_decode_f16_f16(p, head_dim, block_size, G, s);
+    else
+        e = cache_dtype == PKV_E4M3 ? launch_decode_bf16_e4m3(p, head_dim, block_size, G, s)
+                                    : launch_decode_bf16_bf16(p, head_dim, block_size, G, s);
+    if (e != cudaSuccess) return cuda_fail("paged_attention_decode: partition kernel launch", e);
+    if (max_parts > 1) {
+        MergeParams m{context_lens, p.ws_ml, p.ws_o, out, num_q_heads, head_dim, P, max_parts,
+                      static_cast<int>(max_ctx)};
+        e = launch_merge(m, act_dtype, num_seqs, s);
+        if (e != cudaSuccess) return cuda_fail("paged_attention_decode: merge kernel launch", e);
+    }
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// Kernel parameter blocks and launchers (host-visible, no device code).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kMaxDevices = 64;
+
+struct AppendParams {
+    const void* k;
+    const void* v;
+    const int64_t* slot_mapping;
+    void* k_cache;
+    void* v_cache;
+    const float* k_scale;
+    const float* v_scale;
+    int* err;
+    int num_tokens;
+    int num_kv_heads;
+    int head_dim;
+    int block_size;
+    int num_blocks;
+};
+
+struct CopyParams {
+    void* k_cache;
+    void* v_cache;
+    const int32_t* pairs;
+    int* err;
+    size_t block_bytes;
+    int num_blocks;
+};
+
+struct DecodeParams {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    void* out;
+    float* ws_ml;  // [num_seqs][num_q_heads][max_parts][2]: (max in log2 units, sum)
+    float* ws_o;   // [num_seqs][num_q_heads][max_parts][head_dim]: normalised partial outputs
+    const float* k_scale;
+    const float* v_scale;
+    int* err;
+    int max_blocks_per_seq;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int num_blocks;
+    int partition_size;  // tokens per partition, a multiple of 32 and of the block size
+    int max_parts;
+    float scale_log2;  // scale * log2(e)
+};
+
+struct MergeParams {
+    const int32_t* context_lens;
+    const float* ws_ml;
+    const float* ws_o;
+    void* out;
+    int num_q_heads;
+    int head_dim;
+    int partition_size;
+    int max_parts;
+    int max_context;
+};
+
+cudaError_t launch_append(const AppendParams& p, int act, int cache, cudaStream_t stream);
+cudaError_t launch_block_copy(const CopyParams& p, int num_pairs, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, int act, int num_seqs, cudaStream_t stream);
+
+// Partition kernel for one (act, cache) pair; returns cudaErrorInvalidValue
+// for a (head_dim, block_size, group) it was not built for.
+cudaError_t launch_decode_f16_f16(const DecodeParams& p, int D, int BS, int G, cudaStream_t s);
+cudaError_t launch_decode_bf16_bf16(const DecodeParams& p, int D, int BS, int G, cudaStream_t s);
+cudaError_t launch_decode_f16_e4m3(const DecodeParams& p, int D, int BS, int G, cudaStream_t s);
+cudaError_t launch_decode_bf16_e4m3(const DecodeParams& p, int D, int BS, int G, cudaStream_t s);
+
+}  // namespace pkv

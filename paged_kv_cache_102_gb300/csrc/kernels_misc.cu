@@ -1,0 +1,158 @@
+// Slot-mapped KV append, copy-on-write block copy and the split-K merge.
+#include "kernels.h"
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// Append (Ultralytics glossary "PagedAttention", section "How paging works":
+// the key of position pos goes to block table[pos // bs], offset pos % bs).
+// One thread per 8-element chunk of one (token, kv head) row, grid-stride.
+// Same type: one 16-byte load and store per chunk for K and for V (bit copy).
+// E4M3 cache: x / scale in binary32 (correctly rounded division), converted
+// with round-to-nearest-even and saturation to +-448.
+// ---------------------------------------------------------------------------
+template <int ACT, int CACHE>
+__global__ void __launch_bounds__(256) paged_kv_append_kernel(AppendParams p) {
+    const int chunks_per_row = p.head_dim / 8;
+    const int64_t total = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * chunks_per_row;
+    const int64_t num_slots = static_cast<int64_t>(p.num_blocks) * p.block_size;
+    float ks = 1.f, vs = 1.f;
+    if (CACHE == kE4M3) {
+        ks = *p.k_scale;
+        vs = *p.v_scale;
+    }
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int c = static_cast<int>(i % chunks_per_row);
+        const int64_t th = i / chunks_per_row;  // token * Hkv + head
+        const int h = static_cast<int>(th % p.num_kv_heads);
+        const int64_t t = th / p.num_kv_heads;
+        const int64_t slot = p.slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            atomicOr(p.err, kErrBadSlot);
+            continue;
+        }
+        const int64_t blk = slot / p.block_size;
+        const int64_t off = slot % p.block_size;
+        const int64_t dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * p.head_dim + c * 8;
+        const int64_t src = th * p.head_dim + c * 8;
+        const uint4 kin = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k) + src);
+        const uint4 vin = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v) + src);
+        if (CACHE == ACT) {
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.k_cache) + dst) = kin;
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.v_cache) + dst) = vin;
+        } else {
+            const uint16_t* ke = reinterpret_cast<const uint16_t*>(&kin);
+            const uint16_t* ve = reinterpret_cast<const uint16_t*>(&vin);
+            uint8_t kq[8], vq[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                kq[j] = __nv_cvt_float_to_fp8(__fdiv_rn(act_to_float<ACT>(ke[j]), ks), __NV_SATFINITE, __NV_E4M3);
+                vq[j] = __nv_cvt_float_to_fp8(__fdiv_rn(act_to_float<ACT>(ve[j]), vs), __NV_SATFINITE, __NV_E4M3);
+            }
+            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.k_cache) + dst) = *reinterpret_cast<const uint2*>(kq);
+            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.v_cache) + dst) = *reinterpret_cast<const uint2*>(vq);
+        }
+    }
+}
+
+cudaError_t launch_append(const AppendParams& p, int act, int cache, cudaStream_t stream) {
+    const int64_t total = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * (p.head_dim / 8);
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t want = (total + threads - 1) / threads;
+    const int blocks = static_cast<int>(want < 152 * 16 ? want : 152 * 16);
+    if (act == kF16 && cache == kF16)
+        paged_kv_append_kernel<kF16, kF16><<<blocks, threads, 0, stream>>>(p);
+    else if (act == kBF16 && cache == kBF16)
+        paged_kv_append_kernel<kBF16, kBF16><<<blocks, threads, 0, stream>>>(p);
+    else if (act == kF16 && cache == kE4M3)
+        paged_kv_append_kernel<kF16, kE4M3><<<blocks, threads, 0, stream>>>(p);
+    else if (act == kBF16 && cache == kE4M3)
+        paged_kv_append_kernel<kBF16, kE4M3><<<blocks, threads, 0, stream>>>(p);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Copy-on-write block copy (iThome "how to store the KV cache", section
+// "Copy-on-Write": the new block receives a copy of the old block's
+// contents).  grid.x = pair, grid.y = 16 KB chunk of the block; 16-byte
+// vectors, K and V.
+// ---------------------------------------------------------------------------
+constexpr int kCopyChunkBytes = 16384;
+
+__global__ void __launch_bounds__(256) paged_block_copy_kernel(CopyParams p) {
+    const int pair = blockIdx.x;
+    const int src = p.pairs[2 * pair];
+    const int dst = p.pairs[2 * pair + 1];
+    if (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.num_blocks) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(p.err, kErrBadPair);
+        return;
+    }
+    const size_t begin = static_cast<size_t>(blockIdx.y) * kCopyChunkBytes;
+    const size_t end = min(begin + kCopyChunkBytes, p.block_bytes);
+    const size_t so = static_cast<size_t>(src) * p.block_bytes;
+    const size_t d0 = static_cast<size_t>(dst) * p.block_bytes;
+    const unsigned char* ks = static_cast<const unsigned char*>(p.k_cache) + so;
+    const unsigned char* vs = static_cast<const unsigned char*>(p.v_cache) + so;
+    unsigned char* kd = static_cast<unsigned char*>(p.k_cache) + d0;
+    unsigned char* vd = static_cast<unsigned char*>(p.v_cache) + d0;
+    for (size_t o = begin + threadIdx.x * 16; o < end; o += blockDim.x * 16) {
+        const uint4 a = *reinterpret_cast<const uint4*>(ks + o);
+        const uint4 b = *reinterpret_cast<const uint4*>(vs + o);
+        *reinterpret_cast<uint4*>(kd + o) = a;
+        *reinterpret_cast<uint4*>(vd + o) = b;
+    }
+}
+
+cudaError_t launch_block_copy(const CopyParams& p, int num_pairs, cudaStream_t stream) {
+    if (num_pairs == 0) return cudaSuccess;
+    const unsigned chunks = static_cast<unsigned>((p.block_bytes + kCopyChunkBytes - 1) / kCopyChunkBytes);
+    paged_block_copy_kernel<<<dim3(num_pairs, chunks), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Split-K merge.  Each partition p of a sequence left (m_p, l_p, o_p) with
+// o_p already divided by l_p and m_p in log2 units; the full softmax is
+//   out = sum_p w_p o_p / sum_p w_p,  w_p = l_p * 2^(m_p - max_p m_p).
+// One CTA of head_dim threads per (query head, sequence); sequences that fit
+// one partition were written directly by the partition kernel.
+// ---------------------------------------------------------------------------
+template <int ACT>
+__global__ void paged_decode_merge_kernel(MergeParams p) {
+    const int h = blockIdx.x;
+    const int seq = blockIdx.y;
+    const int d = threadIdx.x;
+    const int L = p.context_lens[seq];
+    if (L < 1 || L > p.max_context) return;  // flagged by the partition kernel
+    const int n_parts = (L + p.partition_size - 1) / p.partition_size;
+    if (n_parts <= 1) return;
+    const size_t row = static_cast<size_t>(seq) * p.num_q_heads + h;
+    const float* ml = p.ws_ml + row * p.max_parts * 2;
+    const float* o = p.ws_o + row * p.max_parts * p.head_dim;
+    float M = -INFINITY;
+    for (int i = 0; i < n_parts; ++i) M = fmaxf(M, ml[2 * i]);
+    float num = 0.f, den = 0.f;
+    for (int i = 0; i < n_parts; ++i) {
+        const float w = ml[2 * i + 1] * exp2f(ml[2 * i] - M);
+        num = fmaf(w, o[static_cast<size_t>(i) * p.head_dim + d], num);
+        den += w;
+    }
+    static_cast<uint16_t*>(p.out)[row * p.head_dim + d] = float_to_act<ACT>(num / den);
+}
+
+cudaError_t launch_merge(const MergeParams& p, int act, int num_seqs, cudaStream_t stream) {
+    dim3 grid(p.num_q_heads, num_seqs);
+    if (act == kF16)
+        paged_decode_merge_kernel<kF16><<<grid, p.head_dim, 0, stream>>>(p);
+    else
+        paged_decode_merge_kernel<kBF16><<<grid, p.head_dim, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,169 @@
+// Device helpers shared by the sm_103a kernels: element conversion, mbarrier
+// and bulk-copy (TMA) wrappers written as inline PTX, bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+enum : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
+
+// Bits of the per-device error word (mirrors pkv_device_error_bits).
+enum : int { kErrBadBlock = 1, kErrBadLen = 2, kErrBadSlot = 4, kErrBadPair = 8, kErrTimeout = 16 };
+
+// Longest time a kernel waits on one on-chip barrier before it reports
+// kErrTimeout and stops (nanoseconds of %globaltimer).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier -------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Makes initialised barriers visible to the other threads and to the async (TMA) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait until the phase with the given parity has completed; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// ---- bulk async copy (TMA, non-tensor form) -------------------------------
+// L2 policy for data read exactly once per launch.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Copy `bytes` (multiple of 16, both addresses 16-byte aligned) from global to
+// this CTA's shared memory; completion is counted on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// ---- element conversion ---------------------------------------------------
+// 16 bytes of cache elements -> floats (8 for 16-bit types, 16 for E4M3).
+template <int T>
+struct Vec16;
+
+template <>
+struct Vec16<kBF16> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void to_float(const uint4& u, float* f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+template <>
+struct Vec16<kF16> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void to_float(const uint4& u, float* f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+            float2 t = __half22float2(h);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+};
+
+template <>
+struct Vec16<kE4M3> {
+    static constexpr int N = 16;
+    __device__ __forceinline__ static void to_float(const uint4& u, float* f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * j)) & 0xffffu);
+                __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+                __half2 h = *reinterpret_cast<__half2*>(&hr);
+                float2 t = __half22float2(h);
+                f[4 * i + 2 * j] = t.x;
+                f[4 * i + 2 * j + 1] = t.y;
+            }
+        }
+    }
+};
+
+// Activation (16-bit) scalar conversion.
+template <int T>
+__device__ __forceinline__ float act_to_float(uint16_t bits);
+template <>
+__device__ __forceinline__ float act_to_float<kBF16>(uint16_t bits) {
+    return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+}
+template <>
+__device__ __forceinline__ float act_to_float<kF16>(uint16_t bits) {
+    return __half2float(__ushort_as_half(bits));
+}
+
+template <int T>
+__device__ __forceinline__ uint16_t float_to_act(float x);
+template <>
+__device__ __forceinline__ uint16_t float_to_act<kBF16>(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <>
+__device__ __forceinline__ uint16_t float_to_act<kF16>(float x) {
+    return __half_as_ushort(__float2half_rn(x));
+}
+
+}  // namespace pkv

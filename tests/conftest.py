@@ -34,3 +34,13 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.fail("GPU test collected on a machine without a CUDA device")
     return torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="session")
+def pkv_lib():
+    """Build (if stale) and load libpagedkv.so; no GPU needed to load it."""
+    from paged_kv_cache_102_gb300 import build as pkv_build
+    pkv_build.build()
+    import paged_kv_cache_102_gb300 as pkv
+    pkv.load()
+    return pkv

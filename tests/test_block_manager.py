@@ -1,0 +1,128 @@
+"""The C++ block manager (libpagedkv.so) against the naive oracle allocator
+and the pages' worked examples."""
+import numpy as np
+import pytest
+
+from oracle.block_manager_ref import OutOfBlocks as RefOutOfBlocks
+from oracle.block_manager_ref import RefBlockManager
+from tests.conftest import golden
+
+
+def test_t1_t2_t3_tables(pkv_lib):
+    g = golden("t1_ultralytics_40_tokens.json")
+    bm = pkv_lib.BlockManager(g["pool_blocks"], g["block_size"], free_list=g["free_list"])
+    bm.add_sequence(0, g["num_tokens"])
+    t, lens = bm.tables([0])
+    assert list(t[0]) == g["expected_block_table"] and lens[0] == 40
+    g = golden("t2_optiverse_41_tokens.json")
+    bm = pkv_lib.BlockManager(64, g["block_size"], free_list=g["free_list"])
+    bm.add_sequence(7, g["num_tokens"])
+    slots, pairs = bm.append_slots([7])
+    assert slots[0] == g["expected_next_slot"] and len(pairs) == 0
+    for _ in range(42, g["last_token_filling_block"] + 1):
+        bm.append_slots([7])
+    assert bm.num_seq_blocks(7) == 3
+    bm.append_slots([7])
+    assert bm.num_seq_blocks(7) == 4
+    n0 = bm.num_free
+    bm.free_sequence(7)
+    assert bm.num_free - n0 == 4
+    g = golden("t3_optiverse_825_tokens.json")
+    bm = pkv_lib.BlockManager(100, 16)
+    bm.add_sequence(0, g["num_tokens"])
+    assert bm.num_seq_blocks(0) == g["expected_blocks"]
+
+
+def test_t4_copy_on_write(pkv_lib):
+    g = golden("t4_ithome_copy_on_write.json")
+    bm = pkv_lib.BlockManager(8, g["block_size"], free_list=g["free_list"])
+    bm.add_sequence(1, len(g["prompt_tokens"]))  # A1
+    bm.fork(1, 2)  # A2
+    assert {str(b): bm.ref_count(b) for b in g["expected_prompt_table"]} == g["expected_ref_counts_after_fork"]
+    slots, pairs = bm.append_slots([1, 2])  # A1 writes first, then A2
+    assert [list(p) for p in pairs] == [g["expected_cow_pair_of_A1"]]
+    assert list(slots) == [g["expected_slot_A1"], g["expected_slot_A2"]]
+    t, _ = bm.tables([1, 2])
+    assert list(t[0]) == g["expected_table_A1"] and list(t[1]) == g["expected_table_A2"]
+    assert {str(b): bm.ref_count(b) for b in (7, 1, 3)} == g["expected_ref_counts_after_write"]
+
+
+def _run_random(pkv_lib, seed, n_ops=600):
+    rng = np.random.default_rng(seed)
+    NB, bs = int(rng.integers(8, 64)), int(rng.choice([1, 4, 16]))
+    fl = rng.permutation(NB).astype(np.int32)
+    ref = RefBlockManager(NB, bs, free_list=fl)
+    bm = pkv_lib.BlockManager(NB, bs, free_list=fl)
+    live, next_id = [], 0
+    for _ in range(n_ops):
+        op = rng.integers(0, 4)
+        if op == 0 or not live:
+            n = int(rng.integers(0, 3 * bs + 2))
+            try:
+                ref.add_sequence(next_id, n)
+                ok = True
+            except RefOutOfBlocks:
+                ok = False
+            if ok:
+                bm.add_sequence(next_id, n)
+                live.append(next_id)
+            else:
+                with pytest.raises(pkv_lib.OutOfBlocks):
+                    bm.add_sequence(next_id, n)
+            next_id += 1
+        elif op == 1:
+            k = int(rng.integers(1, len(live) + 1))
+            batch = [int(x) for x in rng.choice(live, size=k, replace=False)]
+            # the oracle handles writers one at a time; the batch call is all or nothing
+            snap = (list(ref.free), list(ref.ref), {s: list(t) for s, t in ref.tables.items()}, dict(ref.lens))
+            try:
+                want = [ref.append_slot(s) for s in batch]
+                ok = True
+            except RefOutOfBlocks:
+                ref.free, ref.ref, ref.tables, ref.lens = snap
+                ok = False
+            if ok:
+                slots, pairs = bm.append_slots(batch)
+                assert list(slots) == [w[0] for w in want]
+                assert [tuple(p) for p in pairs] == [w[1] for w in want if w[1] is not None]
+            else:
+                with pytest.raises(pkv_lib.OutOfBlocks):
+                    bm.append_slots(batch)
+        elif op == 2:
+            parent = int(rng.choice(live))
+            ref.fork(parent, next_id)
+            bm.fork(parent, next_id)
+            live.append(next_id)
+            next_id += 1
+        else:
+            s = live.pop(int(rng.integers(0, len(live))))
+            ref.free_sequence(s)
+            bm.free_sequence(s)
+        assert list(bm.free_list()) == ref.free
+        assert [bm.ref_count(b) for b in range(NB)] == ref.ref
+    for s in live:
+        t, lens = bm.tables([s])
+        assert list(t[0][: len(ref.tables[s])]) == ref.tables[s] and lens[0] == ref.lens[s]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_operations_match_oracle(pkv_lib, seed):
+    _run_random(pkv_lib, seed)
+
+
+def test_errors(pkv_lib):
+    bm = pkv_lib.BlockManager(4, 16)
+    bm.add_sequence(1, 10)
+    with pytest.raises(pkv_lib.PagedKVError):
+        bm.add_sequence(1, 3)  # id in use
+    with pytest.raises(pkv_lib.PagedKVError):
+        bm.append_slots([1, 1])  # repeated id
+    with pytest.raises(pkv_lib.PagedKVError):
+        bm.free_sequence(9)
+    with pytest.raises(pkv_lib.OutOfBlocks):
+        bm.add_sequence(2, 64)
+    assert bm.num_free == 3 and bm.context_len(1) == 10 and bm.context_len(9) == -1
+    with pytest.raises(pkv_lib.PagedKVError):
+        pkv_lib.BlockManager(4, 16, free_list=[0, 0])
+    t, lens = bm.tables([1], max_blocks_per_seq=3, pad=-1)
+    assert list(t[0]) == [0, -1, -1] and lens[0] == 10

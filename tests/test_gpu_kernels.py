@@ -1,0 +1,260 @@
+"""GPU parity of the three kernels against the float64 oracle, through the
+C ABI (via the thin binding).  Append and block copy must be bit-exact;
+attention must be within the stated tolerance of the float64 oracle."""
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.block_manager_ref import RefBlockManager
+from tests.parity import ACT_CODE, TOL, assert_attention_close, bits
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module")
+def pkv(pkv_lib, cuda_device):
+    pkv_lib.device_error(reset=True)
+    yield pkv_lib
+    assert pkv_lib.device_error(reset=True) == 0, "a kernel flagged a device-side error"
+
+
+def _gen(seed):
+    return torch.Generator().manual_seed(seed)
+
+
+# ----------------------------------------------------------------- append ---
+@pytest.mark.parametrize("act,cache,Hkv,D,bs,T", [
+    ("f16", "f16", 8, 64, 16, 4),
+    ("bf16", "bf16", 32, 128, 16, 64),
+    ("bf16", "bf16", 8, 128, 32, 300),
+    ("f16", "f16", 3, 40, 5, 17),
+    ("bf16", "e4m3", 40, 128, 16, 256),
+    ("f16", "e4m3", 8, 64, 32, 33),
+])
+def test_append_bit_exact(pkv, act, cache, Hkv, D, bs, T):
+    g = _gen(T * 7 + D)
+    NB = T // bs + 8
+    k = (torch.randn(T, Hkv, D, generator=g) * 3).to(DT[act])
+    v = (torch.randn(T, Hkv, D, generator=g) * 3).to(DT[act])
+    slots = torch.randperm(NB * bs, generator=g)[:T].to(torch.int64)
+    slots[::5] = -1  # padding tokens are skipped
+    if cache == "e4m3":
+        kc = torch.randint(0, 256, (NB, Hkv, bs, D), dtype=torch.uint8, generator=g)
+        ks, vs = torch.tensor([0.011], dtype=torch.float32), torch.tensor([0.027], dtype=torch.float32)
+    else:
+        kc = torch.randn(NB, Hkv, bs, D, generator=g).to(DT[act])
+        ks = vs = None
+    vc = kc.clone()
+    ref_k, ref_v = bits(kc).copy(), bits(vc).copy()
+    code = oracle.E4M3 if cache == "e4m3" else ACT_CODE[DT[act]]
+    oracle.append(bits(k), bits(v), ACT_CODE[DT[act]], slots.numpy(), ref_k, ref_v, code,
+                  k_scale=1.0 if ks is None else float(ks), v_scale=1.0 if vs is None else float(vs))
+    dk, dv = kc.cuda(), vc.cuda()
+    pkv.paged_kv_append(k.cuda(), v.cuda(), slots.cuda(), dk, dv,
+                        None if ks is None else ks.cuda(), None if vs is None else vs.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(dk), ref_k)
+    assert np.array_equal(bits(dv), ref_v)
+
+
+def test_append_e4m3_rounding_sweep(pkv):
+    """Every E4M3 decision (ties, subnormals, saturation) matches the oracle's encoder."""
+    g = _gen(99)
+    Hkv, D, bs = 1, 128, 16
+    T = 4096
+    x = torch.cat([torch.randn(T * D // 2, generator=g) * 200, torch.randn(T * D // 2, generator=g) * 0.02])
+    mids = torch.from_numpy(oracle.decode_elements(np.arange(0, 0x7F, dtype=np.uint8), oracle.E4M3))
+    mids = ((mids[:-1] + mids[1:]) / 2).float()
+    x[: mids.numel()] = mids
+    x[mids.numel(): 2 * mids.numel()] = -mids
+    k = x.reshape(T, Hkv, D).to(torch.bfloat16)
+    slots = torch.arange(T, dtype=torch.int64)
+    kc = torch.zeros(T // bs, Hkv, bs, D, dtype=torch.uint8)
+    ref_k, ref_v = bits(kc).copy(), bits(kc).copy()
+    oracle.append(bits(k), bits(k), oracle.BF16, slots.numpy(), ref_k, ref_v, oracle.E4M3, k_scale=1.0, v_scale=0.5)
+    dk, dv = kc.cuda(), kc.clone().cuda()
+    one = torch.tensor([1.0], device="cuda")
+    half = torch.tensor([0.5], device="cuda")
+    pkv.paged_kv_append(k.cuda(), k.cuda(), slots.cuda(), dk, dv, one, half)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(dk), ref_k) and np.array_equal(bits(dv), ref_v)
+
+
+def test_append_flags_bad_slot(pkv):
+    NB, Hkv, bs, D = 4, 2, 16, 64
+    k = torch.randn(2, Hkv, D, dtype=torch.float16, device="cuda")
+    kc = torch.zeros(NB, Hkv, bs, D, dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = torch.tensor([NB * bs, 3], dtype=torch.int64, device="cuda")
+    pkv.paged_kv_append(k, k, slots, kc, vc)
+    assert pkv.device_error(reset=True) == pkv.DEV_BAD_SLOT
+    assert torch.equal(kc[0, :, 3], k[1])  # the valid token still landed
+    assert kc.count_nonzero() == k[1].count_nonzero()
+
+
+# ------------------------------------------------------------- block copy ---
+@pytest.mark.parametrize("Hkv,bs,D,dtype,P", [(32, 16, 128, torch.float16, 7), (8, 32, 64, torch.bfloat16, 33),
+                                              (40, 16, 128, torch.uint8, 5), (1, 4, 8, torch.float16, 3)])
+def test_block_copy_bit_exact(pkv, Hkv, bs, D, dtype, P):
+    g = _gen(P)
+    NB = 3 * P + 4
+    if dtype == torch.uint8:
+        kc = torch.randint(0, 256, (NB, Hkv, bs, D), dtype=dtype, generator=g)
+        vc = torch.randint(0, 256, (NB, Hkv, bs, D), dtype=dtype, generator=g)
+    else:
+        kc = torch.randn(NB, Hkv, bs, D, generator=g).to(dtype)
+        vc = torch.randn(NB, Hkv, bs, D, generator=g).to(dtype)
+    perm = torch.randperm(NB, generator=g)
+    pairs = torch.stack([perm[:P], perm[P:2 * P]], dim=1).to(torch.int32).contiguous()
+    rk, rv = bits(kc).copy(), bits(vc).copy()
+    oracle.block_copy(rk, rv, pairs.numpy())
+    dk, dv = kc.cuda(), vc.cuda()
+    pkv.paged_block_copy(dk, dv, pairs.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(dk), rk) and np.array_equal(bits(dv), rv)
+
+
+def test_block_copy_flags_bad_pair(pkv):
+    kc = torch.randn(4, 2, 16, 64, device="cuda").half()
+    vc = kc.clone()
+    before = kc.clone()
+    pairs = torch.tensor([[0, 4], [1, 2]], dtype=torch.int32, device="cuda")
+    pkv.paged_block_copy(kc, vc, pairs)
+    assert pkv.device_error(reset=True) == pkv.DEV_BAD_PAIR
+    assert torch.equal(kc[2], before[1]) and torch.equal(kc[0], before[0])
+
+
+# ----------------------------------------------------------------- decode ---
+def _random_paged(g, B, Hq, Hkv, D, bs, lens, act, cache, extra_blocks=5):
+    """Random pool, shuffled tables from the oracle allocator, queries."""
+    nblk = [-(-int(L) // bs) for L in lens]
+    NB = sum(nblk) + extra_blocks
+    fl = torch.randperm(NB, generator=g).numpy().astype(np.int32)
+    ref = RefBlockManager(NB, bs, free_list=fl)
+    for i, L in enumerate(lens):
+        ref.add_sequence(i, int(L))
+    maxb = max(nblk) + 1
+    tables = np.full((B, maxb), -7, np.int32)  # entries past a sequence's blocks are never read
+    for i in range(B):
+        tables[i, : nblk[i]] = ref.tables[i]
+    q = torch.randn(B, Hq, D, generator=g).to(DT[act])
+    if cache == "e4m3":
+        kc = torch.randint(0, 256, (NB, Hkv, bs, D), dtype=torch.uint8, generator=g)
+        vc = torch.randint(0, 256, (NB, Hkv, bs, D), dtype=torch.uint8, generator=g)
+        kc[(kc & 0x7F) == 0x7F] = 0x3C  # no NaN codes in the pool
+        vc[(vc & 0x7F) == 0x7F] = 0x3C
+    else:
+        kc = torch.randn(NB, Hkv, bs, D, generator=g).to(DT[act])
+        vc = torch.randn(NB, Hkv, bs, D, generator=g).to(DT[act])
+    return q, kc, vc, tables, np.asarray(lens, np.int32)
+
+
+def _run_decode(pkv, q, kc, vc, tables, lens, scale, partition_size, ks=None, vs=None):
+    out = pkv.paged_attention_decode(q.cuda(), kc.cuda(), vc.cuda(), torch.from_numpy(tables).cuda(),
+                                     torch.from_numpy(lens).cuda(), scale,
+                                     k_scale=None if ks is None else torch.tensor([ks], device="cuda"),
+                                     v_scale=None if vs is None else torch.tensor([vs], device="cuda"),
+                                     partition_size=partition_size)
+    torch.cuda.synchronize()
+    return out
+
+
+CASES = [
+    # act, cache, Hq, Hkv, D, bs
+    ("f16", "f16", 8, 8, 64, 16),
+    ("bf16", "bf16", 4, 4, 128, 16),
+    ("bf16", "bf16", 16, 2, 128, 32),
+    ("f16", "f16", 8, 4, 64, 32),
+    ("bf16", "bf16", 8, 2, 64, 16),
+    ("bf16", "e4m3", 4, 4, 128, 16),
+    ("f16", "e4m3", 8, 1, 64, 32),
+    ("bf16", "e4m3", 16, 4, 128, 32),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+@pytest.mark.parametrize("partition_size", [0, -1, 32, 64, 128])
+def test_decode_parity_sweep(pkv, case, partition_size):
+    act, cache, Hq, Hkv, D, bs = case
+    if partition_size > 0 and partition_size % bs:
+        pytest.skip("partition must be a multiple of the block size")
+    g = _gen(zlib.crc32(repr((case, partition_size)).encode()))
+    lens = [1, 2, bs - 1, bs, bs + 1, 31, 32, 33, 64, 95, 129, 300, 517]
+    B = len(lens)
+    q, kc, vc, tables, lens = _random_paged(g, B, Hq, Hkv, D, bs, lens, act, cache)
+    scale = 1.0 / math.sqrt(D)
+    ks, vs = (0.0173, 0.031) if cache == "e4m3" else (1.0, 1.0)
+    code = oracle.E4M3 if cache == "e4m3" else ACT_CODE[DT[act]]
+    want = oracle.paged_decode(bits(q), ACT_CODE[DT[act]], bits(kc), bits(vc), code, tables, lens, scale,
+                               k_scale=ks, v_scale=vs)
+    got = _run_decode(pkv, q, kc, vc, tables, lens, scale, partition_size,
+                      *((ks, vs) if cache == "e4m3" else (None, None)))
+    assert_attention_close(got, want, TOL[cache if cache == "e4m3" else act], rounding_slack=True)
+
+
+def test_decode_closed_forms(pkv):
+    """L = 1 gives v_0 exactly; equal keys give the mean of V."""
+    g = _gen(5)
+    B, H, D, bs = 3, 4, 128, 16
+    q, kc, vc, tables, _ = _random_paged(g, B, H, H, D, bs, [1, 1, 1], "bf16", "bf16")
+    lens = np.array([1, 1, 1], np.int32)
+    out = _run_decode(pkv, q, kc, vc, tables, lens, 0.1, -1)
+    v0 = torch.stack([vc[tables[b, 0], :, 0] for b in range(B)])
+    assert torch.equal(out.cpu(), v0)
+    # equal keys across a 100-token sequence -> uniform weights
+    q, kc, vc, tables, _ = _random_paged(g, 1, H, H, D, bs, [100], "f16", "f16")
+    kc[:] = kc[0, :, 0:1, :]
+    out = _run_decode(pkv, q, kc, vc, tables, np.array([100], np.int32), 0.3, 32)
+    blocks = [int(b) for b in tables[0, :7]]
+    vals = torch.cat([vc[b] for b in blocks], dim=1)[:, :100].double().mean(dim=1)
+    assert (out[0].cpu().double() - vals).abs().max() < 2e-3
+
+
+def test_decode_long_context_split(pkv):
+    """A 20000-token context, several partition sizes, vs the oracle."""
+    g = _gen(11)
+    q, kc, vc, tables, lens = _random_paged(g, 2, 8, 2, 128, 16, [20000, 12345], "bf16", "bf16")
+    want = oracle.paged_decode(bits(q), oracle.BF16, bits(kc), bits(vc), oracle.BF16, tables, lens, 1 / math.sqrt(128))
+    for ps in (0, 512, 2048):
+        got = _run_decode(pkv, q, kc, vc, tables, lens, 1 / math.sqrt(128), ps)
+        assert_attention_close(got, want, TOL["bf16"])
+
+
+def test_decode_flags_bad_inputs(pkv):
+    g = _gen(3)
+    q, kc, vc, tables, lens = _random_paged(g, 2, 4, 4, 64, 16, [20, 40], "f16", "f16")
+    bad_len = lens.copy()
+    bad_len[1] = tables.shape[1] * 16 + 1
+    _run_decode(pkv, q, kc, vc, tables, bad_len, 0.125, -1)
+    assert pkv.device_error(reset=True) == pkv.DEV_BAD_CONTEXT_LEN
+    bad_tab = tables.copy()
+    bad_tab[0, 1] = kc.shape[0] + 3
+    _run_decode(pkv, q, kc, vc, bad_tab, lens, 0.125, -1)
+    assert pkv.device_error(reset=True) == pkv.DEV_BAD_BLOCK
+    bad_len[1] = 0
+    _run_decode(pkv, q, kc, vc, tables, bad_len, 0.125, 0)
+    assert pkv.device_error(reset=True) == pkv.DEV_BAD_CONTEXT_LEN
+
+
+def test_decode_empty_batch_and_streams(pkv):
+    q = torch.empty(0, 4, 64, dtype=torch.float16, device="cuda")
+    kc = torch.zeros(2, 4, 16, 64, dtype=torch.float16, device="cuda")
+    out = pkv.paged_attention_decode(q, kc, kc, torch.zeros(0, 1, dtype=torch.int32, device="cuda"),
+                                     torch.zeros(0, dtype=torch.int32, device="cuda"), 0.1)
+    assert out.shape == (0, 4, 64)
+    # a side stream is honoured
+    g = _gen(8)
+    q, kc, vc, tables, lens = _random_paged(g, 4, 8, 8, 64, 16, [40, 17, 33, 2], "f16", "f16")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = pkv.paged_attention_decode(q.cuda(), kc.cuda(), vc.cuda(), torch.from_numpy(tables).cuda(),
+                                         torch.from_numpy(lens).cuda(), 0.125, stream=s)
+    s.synchronize()
+    want = oracle.paged_decode(bits(q), oracle.F16, bits(kc), bits(vc), oracle.F16, tables, lens, 0.125)
+    assert_attention_close(out, want, TOL["f16"], rounding_slack=True)
