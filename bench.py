@@ -193,14 +193,15 @@ def run_native(args):
     dec_bytes, app_bytes = algorithmic_bytes(wl, st["lens_h"])
     step_bytes = dec_bytes + app_bytes
 
-    sampler = ClockSampler(dev.index if not os.environ.get("CUDA_VISIBLE_DEVICES") else
-                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler = None if args.ncu else ClockSampler(
+        dev.index if not os.environ.get("CUDA_VISIBLE_DEVICES") else
+        int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     # keep the GPU busy long enough for the clock sampler to see it under load
     t_soak = time.time()
-    while time.time() - t_soak < 0.6:
+    while sampler is not None and time.time() - t_soak < 0.6:
         for _ in range(20):
             step()
         torch.cuda.synchronize(dev)
@@ -223,7 +224,7 @@ def run_native(args):
     t1 = time.time()
     ms_total = ev_start.elapsed_time(ev_end)
     dec_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
-    clocks = sampler.stop(t_soak, t1)
+    clocks = sampler.stop(t_soak, t1) if sampler else None
     if dist:
         t = torch.tensor([ms_total], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -238,7 +239,7 @@ def run_native(args):
 
     # end to end through the public API: pinned host inputs -> device, step, output -> host
     e2e = None
-    if not args.no_e2e:
+    if not (args.no_e2e or args.ncu):
         host = {k: vals[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
         host["slots"] = st["slots"].cpu().pin_memory()
         t_pin = torch.empty(st["tables_h"].shape, dtype=torch.int32).pin_memory()
@@ -287,7 +288,7 @@ def run_native(args):
         raise RuntimeError("a kernel flagged a device-side error during the benchmark")
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.ncu):
         cpu = cpu_baseline(st, budget_s=args.cpu_budget)
 
     if rank != 0:
@@ -346,13 +347,18 @@ def cpu_baseline(st, budget_s=20.0, max_seqs=None):
     t1 = run(idx)
     n = int(min(len(lens), max(1, budget_s / max(t1, 1e-6) * 0.8)))
     sel = np.arange(len(lens))[:n]
-    t = run(sel)
+    # repeat the sample until about budget_s seconds of CPU work have been timed
+    t, reps = 0.0, 0
+    while reps == 0 or t < budget_s * 0.8:
+        t += run(sel)
+        reps += 1
+    t /= reps
     e = ELEM[wl.cache_dtype]
     kv = int(lens[sel].astype(np.int64).sum()) * 2 * wl.num_kv_heads * wl.head_dim * e
     dec, _ = algorithmic_bytes(wl, lens[sel])
     return {"value": round(dec / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"float64 oracle decode of {n} of {len(lens)} sequences of the {wl.name} batch "
-                      f"({kv / 1e9:.3f} GB of K/V) in {t:.2f} s",
+                      f"({kv / 1e9:.3f} GB of K/V), {reps} repetitions, {t:.3f} s each",
             "seconds": round(t, 3)}
 
 
@@ -431,7 +437,9 @@ def main():
     ap.add_argument("--partition-size", type=int, default=-1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ncu", action="store_true",
+                    help="profiling run: only warmup + timed steps (no clock soak, e2e or CPU baseline)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
