@@ -169,6 +169,48 @@ int pkv_resolve_partition_size(int num_seqs, int num_kv_heads, int max_blocks_pe
 int paged_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int num_pairs,
                      int num_blocks, size_t block_bytes, void* stream);
 
+/* Size of the fixed scratch array behind paged_attention_decode_noalloc. */
+#define PKV_NOALLOC_MAX_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * paged_attention_decode_noalloc -- paged_attention_decode without a
+ * caller-provided workspace, for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a library convenience, not a step of
+ * the method.
+ *
+ * Who needs it: an engine that reserves all free device memory up front for
+ * its own pool (a further cudaMalloc would fail or compete with it), a host
+ * framework that forbids allocation on its decode path because cudaMalloc can
+ * block and synchronise the device, or a plain C caller without a device
+ * allocator.  Such callers cannot provide the split-K workspace.
+ *
+ * Arguments and results are those of paged_attention_decode, minus workspace
+ * and workspace_bytes.  The caller still passes every input and output.
+ * The split-K scratch is a file-scope device array of
+ * PKV_NOALLOC_MAX_WORKSPACE_BYTES (16 MiB); every GPU that loads the library
+ * holds it until the process exits.  This call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *  - Requests whose pkv_workspace_size(...) exceeds the limit are rejected
+ *    with PKV_ERR_INVALID and a message naming both sizes (nothing is
+ *    enqueued).  Larger partitions, fewer sequences or a shorter table
+ *    shrink the need.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it.  Make
+ *    that first call before any stream capture.
+ *  - Every call on a device shares the one array, and it keeps the previous
+ *    call's contents.  Nothing in it needs to start at zero: each call writes
+ *    all the partials it reads.  Calls that overlap on the GPU (different
+ *    streams without ordering, or several host threads) race on the array
+ *    and give wrong results; order them on one stream.
+ */
+int paged_attention_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int block_size, int head_dim, int num_blocks,
+                                   float scale, void* out, int act_dtype, int cache_dtype,
+                                   const float* k_scale, const float* v_scale, int partition_size,
+                                   void* stream);
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char* pkv_last_error(void);
 
