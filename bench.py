@@ -167,6 +167,7 @@ def run_native(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pkv.load()
+    pkv.set_kernel_path(args.kernel_path)
     st = setup(pkv, W, args.workload, args.seed + rank, dev)
     wl, vals = st["wl"], st["vals"]
     B = len(st["ids"])
@@ -305,7 +306,8 @@ def run_native(args):
                    "partition_size": pkv.resolve_partition_size(B, wl.num_kv_heads, st["tables_h"].shape[1],
                                                                 wl.block_size, ps),
                    "l2": "inputs larger than L2 (K/V read per step %.2f GB vs 129 MB L2)" % (dec_bytes / 1e9),
-                   "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
+                   "parallelism": f"replicas x{world} (sequences sharded, no collective)",
+                   "kernel_path": args.kernel_path},
         "pct_of_peak": round(100 * value / peak, 2),
         "seq_steps_per_s": round(B * world / (ms_step * 1e-3), 1),
         "bytes_per_step": {"decode": dec_bytes, "append": app_bytes},
@@ -435,6 +437,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--partition-size", type=int, default=-1)
+    ap.add_argument("--kernel-path", type=int, default=0,
+                    help="decode kernel: 0 library choice, 1 CUDA-core, 2/3 tensor-core (1 or 2 CTAs per SM)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

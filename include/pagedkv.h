@@ -211,6 +211,27 @@ int paged_attention_decode_noalloc(const void* q, const void* k_cache, const voi
                                    const float* k_scale, const float* v_scale, int partition_size,
                                    void* stream);
 
+/* Kernel paths of paged_attention_decode (pkv_set_kernel_path). */
+enum pkv_kernel_path {
+    PKV_PATH_AUTO = 0,        /* library choice (default) */
+    PKV_PATH_CUDA_CORE = 1,   /* CUDA-core kernel for every shape */
+    PKV_PATH_TENSOR = 2,      /* tensor-core grouped-query kernel, 5 stages, 1 CTA per SM */
+    PKV_PATH_TENSOR_2CTA = 3  /* tensor-core grouped-query kernel, 2 stages, 2 CTAs per SM */
+};
+
+/*
+ * pkv_set_kernel_path -- choose the decode kernel for later calls in this
+ * process (all threads, all devices); returns the previous choice, or -1 for
+ * an unknown value.  PKV_PATH_AUTO uses the tensor-core kernel (2 CTAs per
+ * SM) when
+ * num_q_heads/num_kv_heads >= 4, head_dim is 128, the cache is 16-bit and
+ * partitions are at most 512 tokens, and the CUDA-core kernel otherwise.
+ * Forcing a tensor-core path on a shape it does not serve makes
+ * paged_attention_decode return PKV_ERR_INVALID.  Both kernels compute the
+ * same function; this is a tuning and testing switch.
+ */
+int pkv_set_kernel_path(int path);
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char* pkv_last_error(void);
 

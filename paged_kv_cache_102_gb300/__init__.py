@@ -31,9 +31,10 @@ PARTITION_AUTO = -1
 
 ERR_INVALID, ERR_SHAPE, ERR_CUDA, ERR_NO_SPACE, ERR_NOT_FOUND = 1, 2, 3, 4, 5
 DEV_BAD_BLOCK, DEV_BAD_CONTEXT_LEN, DEV_BAD_SLOT, DEV_BAD_PAIR, DEV_WAIT_TIMEOUT = 1, 2, 4, 8, 16
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR, PATH_TENSOR_2CTA = 0, 1, 2, 3
 
 __all__ = ["paged_kv_append", "paged_attention_decode", "paged_block_copy", "workspace_size",
-           "resolve_partition_size", "device_error", "BlockManager", "OutOfBlocks", "PagedKVError",
+           "resolve_partition_size", "device_error", "set_kernel_path", "BlockManager", "OutOfBlocks", "PagedKVError",
            "F16", "BF16", "E4M3", "PARTITION_SINGLE", "PARTITION_AUTO", "load"]
 
 
@@ -89,6 +90,14 @@ def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=
     _native.call("paged_kv_append", _ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
                  NB, Hkv, bs, D, _code(k), _code(k_cache), _ptr(k_scale), _ptr(v_scale),
                  _stream(stream, k.device))
+
+
+def set_kernel_path(path: int) -> int:
+    """Select the decode kernel (PATH_*) for later calls; returns the previous choice."""
+    prev = int(_native.lib().pkv_set_kernel_path(int(path)))
+    if prev < 0:
+        raise ValueError(f"unknown kernel path {path}")
+    return prev
 
 
 def resolve_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, partition_size=PARTITION_AUTO):

@@ -34,6 +34,7 @@ SIGNATURES = {
     "pkv_last_error": (ctypes.c_char_p, []),
     "pkv_device_error": (I32, [P, I32, P]),
     "pkv_version": (I32, []),
+    "pkv_set_kernel_path": (I32, [I32]),
     "pkv_bm_create": (P, [I32, I32, P, I32]),
     "pkv_bm_destroy": (None, [P]),
     "pkv_bm_add_sequence": (I32, [P, I64, I32]),

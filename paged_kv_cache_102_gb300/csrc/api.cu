@@ -1,6 +1,7 @@
 // C-ABI entry points of libpagedkv.so: argument checks, partition-size
 // choice, workspace carving and kernel dispatch.  Declarations and the
 // contract of each call are in include/pagedkv.h.
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <string>
@@ -43,6 +44,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr int kStageTokens = 32;  // tokens per shared-memory stage of the decode kernel
 constexpr int kAutoPartition = 512;
 
+std::atomic<int> g_kernel_path{PKV_PATH_AUTO};
+
 }  // namespace
 
 void set_error(const std::string& msg) { t_last_error = msg; }
@@ -56,6 +59,11 @@ extern "C" {
 const char* pkv_last_error(void) { return t_last_error.c_str(); }
 
 int pkv_version(void) { return 100; }
+
+int pkv_set_kernel_path(int path) {
+    if (path < PKV_PATH_AUTO || path > PKV_PATH_TENSOR_2CTA) return -1;
+    return g_kernel_path.exchange(path);
+}
 
 int pkv_device_error(int* bits, int reset, void* stream) {
     if (!bits) return fail(PKV_ERR_INVALID, "pkv_device_error: bits is NULL");
@@ -222,7 +230,16 @@ int paged_attention_decode(const void* q, const void* k_cache, const void* v_cac
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (act_dtype == PKV_F16)
+    const int path = g_kernel_path.load();
+    const bool tc_ok = decode_tc_supported(head_dim, block_size, G, act_dtype, cache_dtype, P);
+    if ((path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA) && !tc_ok)
+        return fail(PKV_ERR_INVALID, "paged_attention_decode: the tensor-core path needs head_dim 128, a 16-bit "
+                                     "cache, 2/4/8 query heads per kv head and partitions of at most 512 tokens");
+    const bool use_tc = path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA ||
+                        (path == PKV_PATH_AUTO && tc_ok && G >= 4);
+    if (use_tc)
+        e = launch_decode_tc(p, act_dtype, block_size, G, path == PKV_PATH_TENSOR ? 0 : 1, s);
+    else if (act_dtype == PKV_F16)
         e = cache_dtype == PKV_E4M3 ? launch_decode_f16_e4m3(p, head_dim, block_size, G, s)
                                     : launch_decode_f16_f16(p, head_dim, block_size, G, s);
     else

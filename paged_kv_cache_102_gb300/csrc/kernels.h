@@ -79,4 +79,10 @@ cudaError_t launch_decode_bf16_bf16(const DecodeParams& p, int D, int BS, int G,
 cudaError_t launch_decode_f16_e4m3(const DecodeParams& p, int D, int BS, int G, cudaStream_t s);
 cudaError_t launch_decode_bf16_e4m3(const DecodeParams& p, int D, int BS, int G, cudaStream_t s);
 
+// Tensor-core grouped-query path (head_dim 128, 16-bit cache, group 2/4/8,
+// partitions of at most 512 tokens).  variant 0: 5 stages, 1 CTA/SM;
+// variant 1: 2 stages, 2 CTAs/SM.
+bool decode_tc_supported(int head_dim, int block_size, int group, int act, int cache, int partition_size);
+cudaError_t launch_decode_tc(const DecodeParams& p, int act, int BS, int G, int variant, cudaStream_t s);
+
 }  // namespace pkv

@@ -258,3 +258,67 @@ def test_decode_empty_batch_and_streams(pkv):
     s.synchronize()
     want = oracle.paged_decode(bits(q), oracle.F16, bits(kc), bits(vc), oracle.F16, tables, lens, 0.125)
     assert_attention_close(out, want, TOL["f16"], rounding_slack=True)
+
+
+# ------------------------------------------------------ tensor-core GQA path ---
+TC_CASES = [
+    # act, Hq, Hkv, bs
+    ("bf16", 16, 2, 16),
+    ("bf16", 32, 8, 32),
+    ("f16", 16, 4, 16),
+    ("bf16", 8, 4, 32),
+    ("f16", 8, 2, 16),
+]
+
+
+@pytest.fixture
+def kernel_path(pkv):
+    prev = pkv.set_kernel_path(pkv.PATH_AUTO)
+    yield pkv
+    pkv.set_kernel_path(prev)
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: "-".join(map(str, c)))
+@pytest.mark.parametrize("path", [2, 3])
+@pytest.mark.parametrize("partition_size", [-1, 128, 256, 64])
+def test_decode_tensor_core_parity(kernel_path, case, path, partition_size):
+    pkv = kernel_path
+    act, Hq, Hkv, bs = case
+    if partition_size > 0 and partition_size % bs:
+        pytest.skip("partition must be a multiple of the block size")
+    g = _gen(zlib.crc32(repr((case, path, partition_size)).encode()))
+    lens = [1, 2, 15, 16, 17, 100, 127, 128, 129, 255, 256, 257, 511, 512, 513, 1000, 1531]
+    q, kc, vc, tables, lens = _random_paged(g, len(lens), Hq, Hkv, 128, bs, lens, act, act)
+    scale = 1.0 / math.sqrt(128)
+    want = oracle.paged_decode(bits(q), ACT_CODE[DT[act]], bits(kc), bits(vc), ACT_CODE[DT[act]], tables, lens, scale)
+    pkv.set_kernel_path(path)
+    got = _run_decode(pkv, q, kc, vc, tables, lens, scale, partition_size)
+    assert_attention_close(got, want, TOL[act], rounding_slack=True)
+
+
+@pytest.mark.parametrize("path", [1, 2, 3])
+def test_decode_ignores_unwritten_slots(kernel_path, path):
+    """NaN in the never-written slots of each sequence's last block does not reach the output."""
+    pkv = kernel_path
+    g = _gen(77)
+    lens = [5, 37, 130, 300]
+    q, kc, vc, tables, lens = _random_paged(g, 4, 16, 4, 128, 16, lens, "bf16", "bf16")
+    want = oracle.paged_decode(bits(q), oracle.BF16, bits(kc), bits(vc), oracle.BF16, tables, lens, 0.09)
+    for b, L in enumerate(lens):
+        last = int(tables[b, (L - 1) // 16])
+        kc[last, :, L % 16 or 16:] = float("nan")
+        vc[last, :, L % 16 or 16:] = float("nan")
+    pkv.set_kernel_path(path)
+    got = _run_decode(pkv, q, kc, vc, tables, lens, 0.09, -1)
+    assert_attention_close(got, want, TOL["bf16"], rounding_slack=True)
+
+
+def test_tensor_path_refuses_unsupported_shapes(kernel_path):
+    pkv = kernel_path
+    g = _gen(4)
+    q, kc, vc, tables, lens = _random_paged(g, 2, 8, 8, 128, 16, [20, 40], "bf16", "bf16")  # group 1
+    pkv.set_kernel_path(pkv.PATH_TENSOR)
+    with pytest.raises(pkv.PagedKVError):
+        _run_decode(pkv, q, kc, vc, tables, lens, 0.1, -1)
+    with pytest.raises(ValueError):
+        pkv.set_kernel_path(9)
