@@ -122,10 +122,11 @@ int paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
  *                32 and of block_size), attended independently and merged by
  *                their log-sum-exp weights (split-K).
  *  workspace     device scratch of at least pkv_workspace_size(...) bytes
- *                when more than one partition is possible; may be NULL when
- *                that size is 0.  Its contents need no initialisation and
- *                are undefined after the call; calls sharing a workspace
- *                must be ordered (same stream).
+ *                (never less than 256: a work counter that the call zeroes
+ *                itself, plus the split-K partials when more than one
+ *                partition is possible).  Its contents need no
+ *                initialisation and are undefined after the call; calls
+ *                sharing a workspace must be ordered (same stream).
  */
 int paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
                            const int32_t* block_tables, int max_blocks_per_seq,
@@ -137,9 +138,11 @@ int paged_attention_decode(const void* q, const void* k_cache, const void* v_cac
 
 /*
  * pkv_workspace_size -- bytes of workspace paged_attention_decode needs for
- * these sizes and partition_size: 0 when every sequence fits one partition,
- * otherwise room for each (sequence, query head, partition)'s running max,
- * running sum and normalised partial output in float32.  Host only.
+ * these sizes and partition_size: a 256-byte header (the work counter of the
+ * tensor-core kernel's dynamic scheduling) and, when more than one partition
+ * is possible, room for each (sequence, query head, partition)'s running
+ * max, running sum and normalised partial output in float32.  0 only for
+ * invalid arguments.  Host only.
  */
 size_t pkv_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                           int max_blocks_per_seq, int block_size, int partition_size);
@@ -198,8 +201,9 @@ int paged_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs,
  *    (cudaGetSymbolAddress, with that device current) and caches it.  Make
  *    that first call before any stream capture.
  *  - Every call on a device shares the one array, and it keeps the previous
- *    call's contents.  Nothing in it needs to start at zero: each call writes
- *    all the partials it reads.  Calls that overlap on the GPU (different
+ *    call's contents.  Each call zeroes the work counter it needs (an
+ *    asynchronous 4-byte memset on the stream) and writes all the partials
+ *    it reads, so no clearing is needed between calls.  Calls that overlap on the GPU (different
  *    streams without ordering, or several host threads) race on the array
  *    and give wrong results; order them on one stream.
  */

@@ -43,6 +43,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kStageTokens = 32;  // tokens per shared-memory stage of the decode kernel
 constexpr int kAutoPartition = 512;
+constexpr size_t kWorkspaceHeader = 256;  // work counter of the tensor-core path
 
 std::atomic<int> g_kernel_path{PKV_PATH_AUTO};
 
@@ -111,9 +112,10 @@ size_t pkv_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int h
     if (P <= 0 || num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
     const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
     const long long parts = (max_ctx + P - 1) / P;
-    if (parts <= 1) return 0;
+    if (parts <= 1) return kWorkspaceHeader;
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * static_cast<size_t>(parts);
-    return align_up(rows * 2 * sizeof(float), 256) + rows * static_cast<size_t>(head_dim) * sizeof(float);
+    return kWorkspaceHeader + align_up(rows * 2 * sizeof(float), 256) +
+           rows * static_cast<size_t>(head_dim) * sizeof(float);
 }
 
 int paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens, void* k_cache,
@@ -199,7 +201,7 @@ int paged_attention_decode(const void* q, const void* k_cache, const void* v_cac
         return fail(PKV_ERR_INVALID, "paged_attention_decode: grid too large (partitions, kv heads or sequences > 65535)");
     const size_t need = pkv_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                            block_size, partition_size);
-    if (need > 0 && (!workspace || workspace_bytes < need))
+    if (!workspace || workspace_bytes < need)
         return fail(PKV_ERR_INVALID, "paged_attention_decode: workspace of " + std::to_string(need) +
                                          " bytes required (pkv_workspace_size)");
     int* err = device_error_word();
@@ -213,9 +215,11 @@ int paged_attention_decode(const void* q, const void* k_cache, const void* v_cac
     p.context_lens = context_lens;
     p.out = out;
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * static_cast<size_t>(max_parts);
-    p.ws_ml = need ? static_cast<float*>(workspace) : nullptr;
-    p.ws_o = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * 2 * sizeof(float), 256))
-                  : nullptr;
+    char* ws = static_cast<char*>(workspace);
+    p.work_counter = reinterpret_cast<int*>(ws);
+    p.ws_ml = max_parts > 1 ? reinterpret_cast<float*>(ws + kWorkspaceHeader) : nullptr;
+    p.ws_o = max_parts > 1 ? reinterpret_cast<float*>(ws + kWorkspaceHeader + align_up(rows * 2 * sizeof(float), 256))
+                           : nullptr;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     p.err = err;
@@ -231,7 +235,7 @@ int paged_attention_decode(const void* q, const void* k_cache, const void* v_cac
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     const int path = g_kernel_path.load();
-    const bool tc_ok = decode_tc_supported(head_dim, block_size, G, act_dtype, cache_dtype, P);
+    const bool tc_ok = decode_tc_supported(num_seqs, head_dim, block_size, G, act_dtype, cache_dtype, P);
     if ((path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA) && !tc_ok)
         return fail(PKV_ERR_INVALID, "paged_attention_decode: the tensor-core path needs head_dim 128, a 16-bit "
                                      "cache, 2/4/8 query heads per kv head and partitions of at most 512 tokens");

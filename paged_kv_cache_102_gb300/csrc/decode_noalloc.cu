@@ -67,14 +67,13 @@ extern "C" int paged_attention_decode_noalloc(const void* q, const void* k_cache
                              "-byte scratch; use fewer sequences, a shorter table or a larger partition_size, "
                              "or call paged_attention_decode with your own workspace");
     void* scratch = nullptr;
-    if (need > 0) {
-        int rc = scratch_address(&scratch);
-        if (rc != PKV_OK) return rc;
-    }
-    // The partition kernel writes every partial the merge kernel reads, so the
-    // scratch needs no clearing between calls.
+    int rc = scratch_address(&scratch);
+    if (rc != PKV_OK) return rc;
+    // The decode call zeroes the work counter itself and the partition kernel
+    // writes every partial the merge kernel reads, so the scratch needs no
+    // clearing between calls.
     return paged_attention_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                                   num_q_heads, num_kv_heads, block_size, head_dim, num_blocks, scale, out, act_dtype,
                                   cache_dtype, k_scale, v_scale, partition_size, scratch,
-                                  need > 0 ? static_cast<size_t>(PKV_NOALLOC_MAX_WORKSPACE_BYTES) : 0, stream);
+                                  static_cast<size_t>(PKV_NOALLOC_MAX_WORKSPACE_BYTES), stream);
 }

@@ -88,8 +88,9 @@ cudaError_t by_shape(const DecodeParams& p, const CUtensorMap& km, const CUtenso
 
 }  // namespace
 
-bool decode_tc_supported(int head_dim, int block_size, int group, int act, int cache, int partition_size) {
-    return head_dim == kTcD && (block_size == 16 || block_size == 32) && (group == 2 || group == 4 || group == 8) &&
+bool decode_tc_supported(int num_seqs, int head_dim, int block_size, int group, int act, int cache,
+                         int partition_size) {
+    return num_seqs <= kTcMaxSeqs && head_dim == kTcD && (block_size == 16 || block_size == 32) && (group == 2 || group == 4 || group == 8) &&
            act == cache && (act == kF16 || act == kBF16) && partition_size <= kTcMaxTiles * kTcTile &&
            encode_fn() != nullptr;
 }
@@ -100,6 +101,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int act, int BS, int G, int 
     if (!make_map(&km, p.k_cache, act, cache_rows, BS) || !make_map(&vm, p.v_cache, act, cache_rows, BS) ||
         !make_map(&qm, p.q, act, static_cast<uint64_t>(p.num_seqs) * p.num_q_heads, G))
         return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(p.work_counter, 0, sizeof(int), s);
+    if (e != cudaSuccess) return e;
     // variant 0: five 32 KB stages, one CTA per SM; variant 1: two stages, two CTAs per SM
     if (act == kBF16)
         return variant == 0 ? by_shape<kBF16, 5>(p, km, vm, qm, BS, G, 1, s) : by_shape<kBF16, 2>(p, km, vm, qm, BS, G, 2, s);

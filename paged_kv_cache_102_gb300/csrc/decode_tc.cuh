@@ -10,24 +10,32 @@
 // O = V^T P is [D x G], so it runs on the tensor cores and the K/V bytes are
 // read once for all G heads.
 //
-// Work item: (sequence, kv head, partition of up to 512 tokens).  The kernel
-// is persistent: each CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...
-// Roles (192 threads):
-//  warp 0   producer: table entries -> 2-D TMA loads (128-byte swizzle) of
-//           each (block, kv head) tile, two 64-column halves of head_dim,
-//           into a ring of 128-token stages; K tiles of an item, then its V
-//           tiles; Q rows of the item's G heads.
-//  warp 1   MMA: allocates tensor memory; S[t][h] = sum_d K[t][d] Q[h][d]
-//           with M = 128 tokens, N = 16 (G heads, padded), K = 128 (D), one
-//           16-column slot per tile; then O[d][h] = sum_t V[t][d] P[t][h]
-//           with M = 128 (D), N = 16, K = tokens.
+// Work item: (sequence, kv head, partition of up to 512 tokens).  Only
+// non-empty items are numbered (a per-sequence prefix sum in shared memory).
+// The kernel is persistent and balances ragged lengths dynamically: the
+// producer of each CTA claims the next item number from a counter in the
+// workspace (zeroed before the launch) and passes it to the other roles
+// through a 4-entry queue in shared memory.  Roles (192 threads):
+//  warp 0    producer: claims, block-table entries (fetched one item ahead) ->
+//            2-D TMA loads (128-byte swizzle) of each (block, kv head) tile as
+//            two 64-column halves of head_dim, into a ring of 128-token
+//            stages.  Order: K(0), then for each item n: K(n+1), V(n).
+//  warp 1    MMA: S = K Q^T (M = 128 tokens, N = 16, K = 128) into a
+//            16-column slot per tile; O = V^T P (M = 128 = D, N = 16, K =
+//            tokens).  Order: S(0), then for each n: S(n+1), O(n).
 //  warps 2-5 softmax + epilogue: thread i owns tensor-memory lane i (token i
-//           of each tile for S, dimension i of O).  They take the
-//           partition-wide max and sum per head (no online rescaling: the
-//           whole partition's scores sit in tensor memory), write P in bf16
-//           (or f16) in the MMA's shared-memory layout, and finally write the
-//           output (one partition) or the split-K partial (m, l, O/l).
-// All barrier waits are bounded (kWaitLimitNs); on a timeout the CTA stops
+//            of a tile for S, dimension i of O).  Partition-wide max and sum
+//            per head (the whole partition's scores sit in tensor memory, so
+//            there is no online rescaling), P written in the MMA's shared
+//            memory layout, then the output (one partition) or the split-K
+//            partial (m, l, O/l).  Order: softmax(0), then for each n:
+//            softmax(n+1), epilogue(n).
+// S, O (tensor memory), Q and P (shared memory) are double-buffered by item
+// parity, so the MMA and softmax roles run one item ahead of the epilogue.
+// N = 16 columns are computed for at most 8 heads: rows 8-15 of the Q and P
+// operands alias the next 1 KB of shared memory, and the matching output
+// columns are never read.
+// Every barrier wait is bounded (kWaitLimitNs); on a timeout the CTA stops
 // issuing work, drains its in-flight copies and MMAs, frees tensor memory and
 // reports kErrTimeout.
 #pragma once
@@ -38,28 +46,34 @@
 namespace pkv {
 
 constexpr int kTcThreads = 192;
-constexpr int kTcTile = 128;        // tokens per tile (MMA M of S = K Q^T)
-constexpr int kTcMaxTiles = 4;      // tiles per item: partitions of at most 512 tokens
-constexpr int kTcD = 128;           // head_dim served by this kernel
-constexpr int kTcN = 16;            // MMA N: query heads padded to 16
-constexpr int kTcHalf = kTcTile * 128;       // one 64-column half of a tile: 128 rows x 128 bytes
-constexpr int kTcStage = 2 * kTcHalf;        // 32 KB
-constexpr int kTcQBytes = 2 * kTcN * 128;    // 4 KB
-constexpr int kTcPTile = 2 * kTcN * 128;     // P of one tile: 2 token halves x 16 rows x 128 bytes
-constexpr int kTcTmemCols = 128;             // S: 4 x 16 columns, O: 16 columns
-constexpr int kTcOCol = kTcMaxTiles * kTcN;  // 64
+constexpr int kTcTile = 128;                  // tokens per tile (MMA M of S = K Q^T)
+constexpr int kTcMaxTiles = 4;                // partitions of at most 512 tokens
+constexpr int kTcD = 128;                     // head_dim served by this kernel
+constexpr int kTcN = 16;                      // MMA N: query heads padded to 16
+constexpr int kTcHalf = kTcTile * 128;        // one 64-column half of a tile: 128 rows x 128 B
+constexpr int kTcStage = 2 * kTcHalf;         // 32 KB
+constexpr int kTcQBuf = 3 * 1024;             // Q: two 8-row halves + 1 KB that rows 8-15 of half 1 alias
+constexpr int kTcPBuf = (2 * kTcMaxTiles + 1) * 1024;  // P: tile x token-half 8-row regions + alias pad
+constexpr int kTcSlotCols = kTcMaxTiles * kTcN + kTcN;  // S (4 x 16) + O (16) per buffer
+constexpr int kTcTmemCols = 256;              // two buffers of 80 columns, rounded to a power of 2
+constexpr int kTcMaxSeqs = 2048;              // sequences served (lengths and item prefix in shared memory)
+constexpr int kTcQueue = 4;                   // claimed items in flight between the roles
 
 template <int NS>
 struct TcSmem {
     static constexpr int RING = 0;
     static constexpr int Q = NS * kTcStage;
-    static constexpr int P = Q + kTcQBytes;
-    static constexpr int BARS = P + kTcMaxTiles * kTcPTile;
-    // full[NS], empty[NS], q_full, q_empty, s_full, p_full, o_full, tmem_free, final
-    static constexpr int NBARS = 2 * NS + 7;
+    static constexpr int P = Q + 2 * kTcQBuf;
+    static constexpr int LENS = P + 2 * kTcPBuf;
+    static constexpr int PREFIX = LENS + kTcMaxSeqs * 4;      // items before each sequence, [B + 1]
+    static constexpr int QUEUE = PREFIX + (kTcMaxSeqs + 1) * 4;
+    static constexpr int BARS = (QUEUE + kTcQueue * 4 + 7) / 8 * 8;
+    // full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_free[2], final,
+    // item_full[4], item_empty[4]
+    static constexpr int NBARS = 2 * NS + 13 + 2 * kTcQueue;
     static constexpr int RED = BARS + NBARS * 8;
-    static constexpr int RED_FLOATS = 2 * 4 * 8;  // red_max[4][8], red_sum[4][8]
-    static constexpr int MISC = RED + RED_FLOATS * 4;  // tmem base, abort flag
+    static constexpr int RED_FLOATS = 64 + 32;  // red_max[4][8], red_sum[4][8], stats[2][2][8]
+    static constexpr int MISC = RED + RED_FLOATS * 4;
     static constexpr int BYTES = MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
 };
@@ -68,18 +82,26 @@ struct TcItem {
     int seq, kvh, part, tok_begin, n_tok, n_tiles;
 };
 
-__device__ __forceinline__ bool tc_item(int idx, const DecodeParams& p, int BS, TcItem& it) {
-    it.part = idx % p.max_parts;
-    const int rest = idx / p.max_parts;
-    it.kvh = rest % p.num_kv_heads;
-    it.seq = rest / p.num_kv_heads;
-    const int L = p.context_lens[it.seq];
-    if (L < 1 || L > p.max_blocks_per_seq * BS) return false;
+// Item number ci (0 <= ci < prefix[B]) -> (sequence, kv head, partition).
+// prefix[s] = number of items of sequences before s; a sequence of L tokens
+// has num_kv_heads * ceil(L / partition_size) items, kv head major.
+__device__ __forceinline__ void tc_decode_item(int ci, const DecodeParams& p, const int* lens, const int* prefix,
+                                               TcItem& it) {
+    int lo = 0, hi = p.num_seqs;  // find the last s with prefix[s] <= ci
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= ci) lo = mid;
+        else hi = mid;
+    }
+    const int L = lens[lo];
+    const int parts = (L + p.partition_size - 1) / p.partition_size;
+    const int r = ci - prefix[lo];
+    it.seq = lo;
+    it.kvh = r / parts;
+    it.part = r - it.kvh * parts;
     it.tok_begin = it.part * p.partition_size;
-    if (it.tok_begin >= L) return false;
     it.n_tok = min(p.partition_size, L - it.tok_begin);
     it.n_tiles = (it.n_tok + kTcTile - 1) / kTcTile;
-    return true;
 }
 
 // Bounded wait that also gives up when another role has aborted.
@@ -123,35 +145,78 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     static_assert(kTcMaxTiles * kTcTile / BS <= 32, "one warp holds the table entries of an item");
 
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sm =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* ring = sm + S::RING;
     unsigned char* qbuf = sm + S::Q;
     unsigned char* pbuf = sm + S::P;
+    int* s_lens = reinterpret_cast<int*>(sm + S::LENS);
+    int* s_prefix = reinterpret_cast<int*>(sm + S::PREFIX);
+    volatile int* item_q = reinterpret_cast<volatile int*>(sm + S::QUEUE);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BARS);
     uint64_t* full = bars;
     uint64_t* empty = bars + NS;
     uint64_t* q_full = bars + 2 * NS;
-    uint64_t* q_empty = q_full + 1;
-    uint64_t* s_full = q_full + 2;
-    uint64_t* p_full = q_full + 3;
-    uint64_t* o_full = q_full + 4;
-    uint64_t* tmem_free = q_full + 5;
-    uint64_t* final_bar = q_full + 6;
+    uint64_t* q_empty = q_full + 2;
+    uint64_t* s_full = q_full + 4;
+    uint64_t* p_full = q_full + 6;
+    uint64_t* o_full = q_full + 8;
+    uint64_t* o_free = q_full + 10;
+    uint64_t* final_bar = q_full + 12;
+    uint64_t* item_full = q_full + 13;
+    uint64_t* item_empty = item_full + kTcQueue;
     float* red_max = reinterpret_cast<float*>(sm + S::RED);
     float* red_sum = red_max + 32;
+    float* stats = red_max + 64;  // [buffer][max, sum][8]
     uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(sm + S::MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::MISC + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int total_items = p.num_seqs * p.num_kv_heads * p.max_parts;
+    const int B = p.num_seqs;  // <= kTcMaxSeqs (checked on the host)
 
+    // Lengths and the exclusive prefix of items per sequence (a sequence with a
+    // length outside 1..max_blocks*BS has no items).
+    {
+        const int chunk = (B + kTcThreads - 1) / kTcThreads;
+        const int s0 = min(B, threadIdx.x * chunk), s1 = min(B, s0 + chunk);
+        int local = 0;
+        for (int s = s0; s < s1; ++s) {
+            const int L = p.context_lens[s];
+            s_lens[s] = L;
+            if (L >= 1 && L <= p.max_blocks_per_seq * BS)
+                local += p.num_kv_heads * ((L + p.partition_size - 1) / p.partition_size);
+        }
+        int incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        int* warp_tot = reinterpret_cast<int*>(red_max);
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += warp_tot[w];
+        int run = base + incl - local;
+        for (int s = s0; s < s1; ++s) {
+            s_prefix[s] = run;
+            const int L = s_lens[s];
+            if (L >= 1 && L <= p.max_blocks_per_seq * BS)
+                run += p.num_kv_heads * ((L + p.partition_size - 1) / p.partition_size);
+        }
+        if (threadIdx.x == kTcThreads - 1) s_prefix[B] = base + incl;
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        for (int i = 0; i < 7; ++i) mbar_init(&q_full[i], 1);
+        for (int i = 0; i < 13; ++i) mbar_init(&q_full[i], 1);
+        for (int i = 0; i < kTcQueue; ++i) {
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], 2);  // the MMA warp and the softmax warps
+        }
         *abort_flag = 0;
         mbar_init_fence();
         tc::prefetch_tensormap(&kmap);
@@ -166,22 +231,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_base_smem;
+    const int total = s_prefix[B];
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
         const uint64_t policy = l2_policy_evict_first();
-        uint32_t use = 0;  // stage uses issued so far
-        int qn = 0;        // items whose Q was loaded
-        for (int idx = blockIdx.x; idx < total_items; idx += gridDim.x) {
-            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            TcItem it;
-            if (!tc_item(idx, p, BS, it)) {
-                if (lane == 0 && it.part == 0 && it.kvh == 0) {
-                    const int L = p.context_lens[it.seq];
-                    if (L < 1 || L > p.max_blocks_per_seq * BS) atomicOr(p.err, kErrBadLen);
-                }
-                continue;
+        uint32_t use = 0;  // ring stages armed so far
+        int nq = 0;        // Q tiles requested so far
+        int nclaim = 0;    // queue entries written so far
+        bool ok = true;
+        if (lane == 0) {
+            // sequences with a context length outside 1..max_blocks*BS are skipped; report them once
+            for (int s = blockIdx.x; s < B; s += gridDim.x) {
+                const int L = s_lens[s];
+                if (L < 1 || L > p.max_blocks_per_seq * BS) atomicOr(p.err, kErrBadLen);
             }
+        }
+        // Claim the next item for this CTA and pass it to the other roles; false
+        // at the end of the work (the end marker is queued) or on an abort.
+        auto claim = [&](TcItem& it) {
+            int ci = -1;
+            bool good = true;
+            if (lane == 0) {
+                ci = atomicAdd(p.work_counter, 1);
+                if (ci >= total) ci = -1;
+                const int slot = nclaim % kTcQueue;
+                if (nclaim >= kTcQueue) good = tc_wait(&item_empty[slot], ((nclaim / kTcQueue) - 1) & 1, abort_flag, p.err);
+                if (good) {
+                    item_q[slot] = ci;
+                    mbar_arrive(&item_full[slot]);
+                }
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            ci = __shfl_sync(0xffffffffu, ci, 0);
+            if (!good) {
+                ok = false;
+                return false;
+            }
+            ++nclaim;
+            if (ci < 0) return false;
+            tc_decode_item(ci, p, s_lens, s_prefix, it);
+            return true;
+        };
+        auto table_entry = [&](const TcItem& it) {
             const int n_blk = (it.n_tok + BS - 1) / BS;
             int phys = -1;
             if (lane < n_blk) {
@@ -191,122 +283,172 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     phys = -1;
                 }
             }
-            bool ok = true;
+            return phys;
+        };
+        // Arm one ring stage with tile t of an item; `map` is the K or V tensor map.
+        auto issue_tile = [&](const TcItem& it, int phys, int t, const CUtensorMap* map) {
+            const int n_blk = (it.n_tok + BS - 1) / BS;
+            int pb[BPT];
+#pragma unroll
+            for (int j = 0; j < BPT; ++j) pb[j] = __shfl_sync(0xffffffffu, phys, (t * BPT + j) & 31);
+            bool good = true;
             if (lane == 0) {
-                if (qn > 0) ok = tc_wait(q_empty, (qn - 1) & 1, abort_flag, p.err);
-                if (ok) {
-                    mbar_arrive_expect_tx(q_full, 2 * G * 128);
-                    const int row = it.seq * p.num_q_heads + it.kvh * G;
-                    tc::tma_load_2d(qbuf, &qmap, 0, row, q_full, policy);
-                    tc::tma_load_2d(qbuf + kTcN * 128, &qmap, 64, row, q_full, policy);
-                }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            ++qn;
-            for (int pass = 0; pass < 2 && ok; ++pass) {
-                const CUtensorMap* map = pass == 0 ? &kmap : &vmap;
-                for (int t = 0; t < it.n_tiles && ok; ++t) {
-                    int pb[BPT];
+                const int s = use % NS;
+                if (use >= NS) good = tc_wait(&empty[s], ((use / NS) - 1) & 1, abort_flag, p.err);
+                if (good) {
+                    uint32_t bytes = 0;
 #pragma unroll
-                    for (int j = 0; j < BPT; ++j) pb[j] = __shfl_sync(0xffffffffu, phys, (t * BPT + j) & 31);
-                    if (lane == 0) {
-                        const int s = use % NS;
-                        if (use >= NS) ok = tc_wait(&empty[s], ((use / NS) - 1) & 1, abort_flag, p.err);
-                        if (ok) {
-                            uint32_t bytes = 0;
+                    for (int j = 0; j < BPT; ++j)
+                        if (t * BPT + j < n_blk && pb[j] >= 0) bytes += BS * 256;
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    unsigned char* st = ring + s * kTcStage;
 #pragma unroll
-                            for (int j = 0; j < BPT; ++j)
-                                if (t * BPT + j < n_blk && pb[j] >= 0) bytes += BS * 256;
-                            mbar_arrive_expect_tx(&full[s], bytes);
-                            unsigned char* st = ring + s * kTcStage;
-#pragma unroll
-                            for (int j = 0; j < BPT; ++j) {
-                                if (t * BPT + j < n_blk && pb[j] >= 0) {
-                                    const int y = (pb[j] * p.num_kv_heads + it.kvh) * BS;
-                                    tc::tma_load_2d(st + j * BS * 128, map, 0, y, &full[s], policy);
-                                    tc::tma_load_2d(st + kTcHalf + j * BS * 128, map, 64, y, &full[s], policy);
-                                }
-                            }
+                    for (int j = 0; j < BPT; ++j) {
+                        if (t * BPT + j < n_blk && pb[j] >= 0) {
+                            const int y = (pb[j] * p.num_kv_heads + it.kvh) * BS;
+                            tc::tma_load_2d(st + j * BS * 128, map, 0, y, &full[s], policy);
+                            tc::tma_load_2d(st + kTcHalf + j * BS * 128, map, 64, y, &full[s], policy);
                         }
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (ok) ++use;  // only stages actually armed are drained below
                 }
             }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (good) ++use;
+            return good;
+        };
+        auto issue_q_and_k = [&](const TcItem& it, int phys, int k) {
+            bool good = true;
+            if (lane == 0) {
+                const int b = k & 1;
+                if (k >= 2) good = tc_wait(&q_empty[b], ((k >> 1) - 1) & 1, abort_flag, p.err);
+                if (good) {
+                    mbar_arrive_expect_tx(&q_full[b], 2 * G * 128);
+                    const int row = it.seq * p.num_q_heads + it.kvh * G;
+                    tc::tma_load_2d(qbuf + b * kTcQBuf, &qmap, 0, row, &q_full[b], policy);
+                    tc::tma_load_2d(qbuf + b * kTcQBuf + 1024, &qmap, 64, row, &q_full[b], policy);
+                }
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) return false;
+            ++nq;
+            for (int t = 0; t < it.n_tiles; ++t)
+                if (!issue_tile(it, phys, t, &kmap)) return false;
+            return true;
+        };
+
+        TcItem cur, nxt, nn;
+        bool have_c = claim(cur);
+        int phys_c = have_c ? table_entry(cur) : -1;
+        bool have_n = have_c && claim(nxt);
+        int phys_n = have_n ? table_entry(nxt) : -1;
+        if (have_c && ok) ok = issue_q_and_k(cur, phys_c, 0);
+        for (int k = 0; have_c && ok; ++k) {
+            const bool have_nn = have_n && claim(nn);  // claims run two items ahead of the V loads
+            const int phys_nn = have_nn ? table_entry(nn) : -1;
             if (!ok) break;
+            if (have_n) ok = issue_q_and_k(nxt, phys_n, k + 1);
+            for (int t = 0; t < cur.n_tiles && ok; ++t) ok = issue_tile(cur, phys_c, t, &vmap);
+            have_c = have_n;
+            cur = nxt;
+            phys_c = phys_n;
+            have_n = have_nn;
+            nxt = nn;
+            phys_n = phys_nn;
         }
         // Leave only when every copy into this CTA's shared memory has landed.
         if (lane == 0) {
             const uint32_t first = use > static_cast<uint32_t>(NS) ? use - NS : 0;
             for (uint32_t u = first; u < use; ++u)
                 if (!mbar_wait(&full[u % NS], (u / NS) & 1)) atomicOr(p.err, kErrTimeout);
-            if (qn > 0 && !mbar_wait(q_full, (qn - 1) & 1)) atomicOr(p.err, kErrTimeout);
+            for (int k = nq > 2 ? nq - 2 : 0; k < nq; ++k)
+                if (!mbar_wait(&q_full[k & 1], (k >> 1) & 1)) atomicOr(p.err, kErrTimeout);
         }
     } else if (warp == 1) {
         // --------------------------------------------------------------------- MMA
         uint32_t use = 0;
-        int n = 0;  // valid items processed
-        for (int idx = blockIdx.x; idx < total_items; idx += gridDim.x) {
-            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            TcItem it;
-            if (!tc_item(idx, p, BS, it)) continue;
-            bool ok = true;
+        int nread = 0;
+        // 1: an item, 0: end of work, -1: abort
+        auto read_item = [&](TcItem& it) {
+            const int slot = nread % kTcQueue;
+            bool good = true;
+            int ci = -1;
             if (lane == 0) {
-                ok = tc_wait(q_full, n & 1, abort_flag, p.err);
-                if (ok && n > 0) ok = tc_wait(tmem_free, (n - 1) & 1, abort_flag, p.err);
+                good = tc_wait(&item_full[slot], (nread / kTcQueue) & 1, abort_flag, p.err);
+                if (good) {
+                    ci = item_q[slot];
+                    mbar_arrive(&item_empty[slot]);
+                }
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            good = __shfl_sync(0xffffffffu, good, 0);
+            ci = __shfl_sync(0xffffffffu, ci, 0);
+            ++nread;
+            if (!good) return -1;
+            if (ci < 0) return 0;
+            tc_decode_item(ci, p, s_lens, s_prefix, it);
+            return 1;
+        };
+        auto mma_s = [&](const TcItem& it, int k) {
+            const int b = k & 1;
+            bool good = true;
+            if (lane == 0) good = tc_wait(&q_full[b], (k >> 1) & 1, abort_flag, p.err);
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) return false;
             tc::fence_after_sync();
-            // S = K Q^T, one 16-column slot per tile
-            for (int t = 0; t < it.n_tiles && ok; ++t) {
+            const uint32_t qb = smem_addr(qbuf + b * kTcQBuf);
+            for (int t = 0; t < it.n_tiles; ++t) {
                 const int s = use % NS;
-                if (lane == 0) ok = tc_wait(&full[s], (use / NS) & 1, abort_flag, p.err);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
+                if (lane == 0) good = tc_wait(&full[s], (use / NS) & 1, abort_flag, p.err);
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) return false;
                 tc::fence_after_sync();
                 if (lane == 0) {
                     const uint32_t kb = smem_addr(ring + s * kTcStage);
-                    const uint32_t qb = smem_addr(qbuf);
 #pragma unroll
-                    for (int k = 0; k < kTcD / 16; ++k) {
-                        const uint32_t off = (k >> 2) * kTcHalf + (k & 3) * 32;
-                        const uint32_t qoff = (k >> 2) * (kTcN * 128) + (k & 3) * 32;
-                        tc::mma_f16(tmem + t * kTcN, tc::desc_sw128(kb + off, 16, 1024),
-                                    tc::desc_sw128(qb + qoff, 16, 1024), IDESC_S, k > 0);
+                    for (int kk = 0; kk < kTcD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kTcHalf + (kk & 3) * 32;
+                        const uint32_t qoff = (kk >> 2) * 1024 + (kk & 3) * 32;
+                        tc::mma_f16(tmem + b * kTcSlotCols + t * kTcN, tc::desc_sw128(kb + off, 16, 1024),
+                                    tc::desc_sw128(qb + qoff, 16, 1024), IDESC_S, kk > 0);
                     }
                     tc::commit(&empty[s]);
                 }
                 __syncwarp();
                 ++use;
             }
-            if (!ok) break;
             if (lane == 0) {
-                tc::commit(q_empty);
-                tc::commit(s_full);
-                ok = tc_wait(p_full, n & 1, abort_flag, p.err);
+                tc::commit(&q_empty[b]);
+                tc::commit(&s_full[b]);
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            __syncwarp();
+            return true;
+        };
+        auto mma_o = [&](const TcItem& it, int k) {
+            const int b = k & 1;
+            bool good = true;
+            if (lane == 0) {
+                good = tc_wait(&p_full[b], (k >> 1) & 1, abort_flag, p.err);
+                if (good && k >= 2) good = tc_wait(&o_free[b], ((k >> 1) - 1) & 1, abort_flag, p.err);
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) return false;
             tc::fence_after_sync();
-            // O = V^T P over the item's tiles
-            for (int t = 0; t < it.n_tiles && ok; ++t) {
+            const uint32_t pbase = smem_addr(pbuf + b * kTcPBuf);
+            for (int t = 0; t < it.n_tiles; ++t) {
                 const int s = use % NS;
-                ok = __all_sync(0xffffffffu, tc_wait(&full[s], (use / NS) & 1, abort_flag, p.err));
-                if (!ok) break;
+                good = __all_sync(0xffffffffu, tc_wait(&full[s], (use / NS) & 1, abort_flag, p.err));
+                if (!good) return false;
                 unsigned char* vb = ring + s * kTcStage;
                 const int valid = min(kTcTile, it.n_tok - t * kTcTile);
                 const int ksteps = (valid + 15) / 16;
                 // rows past the context inside the last 16-token step: zero them so
-                // that unwritten pool slots cannot leak NaN through P = 0
+                // that never-written pool slots cannot turn P = 0 into NaN
                 const int zero_rows = ksteps * 16 - valid;
                 if (zero_rows > 0) {
                     for (int i = lane; i < zero_rows * 16; i += 32) {
                         const int r = valid + (i >> 4);
                         const int c = i & 15;  // 16-byte chunk of the 256-byte row (two halves)
-                        unsigned char* dst = vb + (c >> 3) * kTcHalf + r * 128 + (c & 7) * 16;
-                        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(vb + (c >> 3) * kTcHalf + r * 128 + (c & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
                     }
                     tc::fence_proxy_async_smem();
                     __syncwarp();
@@ -314,21 +456,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc::fence_after_sync();
                 if (lane == 0) {
                     const uint32_t vaddr = smem_addr(vb);
-                    const uint32_t pb = smem_addr(pbuf + t * kTcPTile);
                     for (int j = 0; j < ksteps; ++j) {
-                        const uint32_t poff = (j >> 2) * (kTcN * 128) + (j & 3) * 32;
-                        tc::mma_f16(tmem + kTcOCol, tc::desc_sw128(vaddr + j * 2048, kTcHalf, 1024),
-                                    tc::desc_sw128(pb + poff, 16, 1024), IDESC_O, (t > 0 || j > 0) ? 1u : 0u);
+                        const uint32_t poff = (2 * t + (j >> 2)) * 1024 + (j & 3) * 32;
+                        tc::mma_f16(tmem + b * kTcSlotCols + kTcMaxTiles * kTcN,
+                                    tc::desc_sw128(vaddr + j * 2048, kTcHalf, 1024),
+                                    tc::desc_sw128(pbase + poff, 16, 1024), IDESC_O, (t > 0 || j > 0) ? 1u : 0u);
                     }
                     tc::commit(&empty[s]);
                 }
                 __syncwarp();
                 ++use;
             }
-            if (!ok) break;
-            if (lane == 0) tc::commit(o_full);
+            if (lane == 0) tc::commit(&o_full[b]);
             __syncwarp();
-            ++n;
+            return true;
+        };
+
+        TcItem cur, nxt;
+        int rc = read_item(cur);
+        bool ok = rc >= 0;
+        if (rc > 0) ok = mma_s(cur, 0);
+        for (int k = 0; rc > 0 && ok; ++k) {
+            const int rn = read_item(nxt);
+            if (rn < 0) break;
+            if (rn > 0) ok = mma_s(nxt, k + 1);
+            if (ok) ok = mma_o(cur, k);
+            rc = rn;
+            cur = nxt;
         }
         // every MMA this thread issued has completed before tensor memory is freed
         if (lane == 0) {
@@ -342,21 +496,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int row = q4 * 32 + lane;  // token of each tile (S) / dimension d (O)
         const int tid = threadIdx.x - 64;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-        int n = 0;
-        for (int idx = blockIdx.x; idx < total_items; idx += gridDim.x) {
-            TcItem it;
-            if (!tc_item(idx, p, BS, it)) continue;
-            // Every wait below is followed by a barrier that all 128 threads
-            // reach; a failure is OR-reduced there so that the four warps
-            // leave together and no named barrier is left waiting.
-            bool ok = __all_sync(0xffffffffu, tc_wait(s_full, n & 1, abort_flag, p.err));
+        int nread = 0;
+
+        // Every wait below is followed by a barrier that all 128 threads reach;
+        // a failure is OR-reduced there so that the four warps leave together
+        // and no named barrier is left waiting.
+        auto read_item = [&](TcItem& it) {
+            const int slot = nread % kTcQueue;
+            const bool good =
+                __all_sync(0xffffffffu, tc_wait(&item_full[slot], (nread / kTcQueue) & 1, abort_flag, p.err));
+            const int ci = good ? item_q[slot] : -1;
+            ++nread;
+            if (named_bar_or(3, 128, !good)) return -1;
+            if (tid == 0) mbar_arrive(&item_empty[slot]);
+            if (ci < 0) return 0;
+            tc_decode_item(ci, p, s_lens, s_prefix, it);
+            return 1;
+        };
+        auto softmax = [&](const TcItem& it, int k) {
+            const int b = k & 1;
+            const bool good = __all_sync(0xffffffffu, tc_wait(&s_full[b], (k >> 1) & 1, abort_flag, p.err));
             float sc[kTcMaxTiles][G] = {};
-            if (ok) {
+            if (good) {
                 tc::fence_after_sync();
 #pragma unroll
                 for (int t = 0; t < kTcMaxTiles; ++t)
-                    if (t < it.n_tiles) tc::TmemLd<G>::load(lane_addr + t * kTcN, sc[t]);
+                    if (t < it.n_tiles) tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN, sc[t]);
                 tc::tmem_wait_ld();
+                tc::fence_before_sync();  // these reads precede the next MMA into this S buffer
                 float mx[G];
 #pragma unroll
                 for (int g = 0; g < G; ++g) mx[g] = -INFINITY;
@@ -380,23 +547,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int g = 0; g < G; ++g) red_max[q4 * 8 + g] = mx[g];
                 }
             }
-            if (named_bar_or(1, 128, !ok)) break;
+            if (named_bar_or(1, 128, !good)) return false;
             float M[G], sum[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 M[g] = fmaxf(fmaxf(red_max[g], red_max[8 + g]), fmaxf(red_max[16 + g], red_max[24 + g]));
                 sum[g] = 0.f;
             }
+            unsigned char* pb = pbuf + b * kTcPBuf;
 #pragma unroll
             for (int t = 0; t < kTcMaxTiles; ++t) {
                 if (t < it.n_tiles) {
-                    unsigned char* pt = pbuf + t * kTcPTile + (row >> 6) * (kTcN * 128);
+                    unsigned char* pt = pb + (2 * t + (row >> 6)) * 1024;
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         const float pv = sc[t][g] == -INFINITY ? 0.f : exp2f(sc[t][g] - M[g]);
                         sum[g] += pv;
-                        const int chunk = ((row & 63) >> 3) ^ (g & 7);
-                        *reinterpret_cast<uint16_t*>(pt + g * 128 + chunk * 16 + (row & 7) * 2) = float_to_act<ACT>(pv);
+                        const int chunk = ((row & 63) >> 3) ^ g;
+                        *reinterpret_cast<uint16_t*>(pt + g * 128 + chunk * 16 + (row & 7) * 2) =
+                            float_to_act<ACT>(pv);
                     }
                 }
             }
@@ -411,27 +580,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc::fence_proxy_async_smem();
             asm volatile("bar.sync 2, 128;" ::: "memory");
-            float Lsum[G];
+            if (tid == 0) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) Lsum[g] = red_sum[g] + red_sum[8 + g] + red_sum[16 + g] + red_sum[24 + g];
-            if (tid == 0) mbar_arrive(p_full);
-
-            ok = __all_sync(0xffffffffu, tc_wait(o_full, n & 1, abort_flag, p.err));
-            float o[G];
-            if (ok) {
+                for (int g = 0; g < G; ++g) {
+                    stats[b * 16 + g] = M[g];
+                    stats[b * 16 + 8 + g] = red_sum[g] + red_sum[8 + g] + red_sum[16 + g] + red_sum[24 + g];
+                }
+                mbar_arrive(&p_full[b]);
+            }
+            return true;
+        };
+        auto epilogue = [&](const TcItem& it, int k) {
+            const int b = k & 1;
+            const bool good = __all_sync(0xffffffffu, tc_wait(&o_full[b], (k >> 1) & 1, abort_flag, p.err));
+            float o[G] = {};
+            if (good) {
                 tc::fence_after_sync();
-                tc::TmemLd<G>::load(lane_addr + kTcOCol, o);
+                tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + kTcMaxTiles * kTcN, o);
                 tc::tmem_wait_ld();
                 tc::fence_before_sync();
             }
-            if (named_bar_or(1, 128, !ok)) break;
-            if (tid == 0) mbar_arrive(tmem_free);
-
+            // also orders the stats written by the softmax of this item before the reads below
+            if (named_bar_or(1, 128, !good)) return false;
+            if (tid == 0) mbar_arrive(&o_free[b]);
             const int d = row;
-            const bool single = p.max_parts == 1 || p.context_lens[it.seq] <= p.partition_size;
+            const bool single = p.max_parts == 1 || s_lens[it.seq] <= p.partition_size;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float val = o[g] / Lsum[g];
+                const float Mg = stats[b * 16 + g];
+                const float Lg = stats[b * 16 + 8 + g];
+                const float val = o[g] / Lg;
                 const size_t hrow = static_cast<size_t>(it.seq) * p.num_q_heads + it.kvh * G + g;
                 if (single) {
                     static_cast<uint16_t*>(p.out)[hrow * kTcD + d] = float_to_act<ACT>(val);
@@ -439,12 +617,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const size_t slot = hrow * p.max_parts + it.part;
                     p.ws_o[slot * kTcD + d] = val;
                     if (d == 0) {
-                        p.ws_ml[slot * 2] = M[g];
-                        p.ws_ml[slot * 2 + 1] = Lsum[g];
+                        p.ws_ml[slot * 2] = Mg;
+                        p.ws_ml[slot * 2 + 1] = Lg;
                     }
                 }
             }
-            ++n;
+            return true;
+        };
+
+        TcItem cur, nxt;
+        int rc = read_item(cur);
+        bool ok = rc >= 0;
+        if (rc > 0) ok = softmax(cur, 0);
+        for (int k = 0; rc > 0 && ok; ++k) {
+            const int rn = read_item(nxt);
+            if (rn < 0) break;
+            if (rn > 0) ok = softmax(nxt, k + 1);
+            if (ok) ok = epilogue(cur, k);
+            rc = rn;
+            cur = nxt;
         }
     }
 

@@ -43,6 +43,7 @@ struct DecodeParams {
     void* out;
     float* ws_ml;  // [num_seqs][num_q_heads][max_parts][2]: (max in log2 units, sum)
     float* ws_o;   // [num_seqs][num_q_heads][max_parts][head_dim]: normalised partial outputs
+    int* work_counter;  // workspace header: next item to claim (tensor-core path), zero at launch
     const float* k_scale;
     const float* v_scale;
     int* err;
@@ -82,7 +83,8 @@ cudaError_t launch_decode_bf16_e4m3(const DecodeParams& p, int D, int BS, int G,
 // Tensor-core grouped-query path (head_dim 128, 16-bit cache, group 2/4/8,
 // partitions of at most 512 tokens).  variant 0: 5 stages, 1 CTA/SM;
 // variant 1: 2 stages, 2 CTAs/SM.
-bool decode_tc_supported(int head_dim, int block_size, int group, int act, int cache, int partition_size);
+bool decode_tc_supported(int num_seqs, int head_dim, int block_size, int group, int act, int cache,
+                         int partition_size);
 cudaError_t launch_decode_tc(const DecodeParams& p, int act, int BS, int G, int variant, cudaStream_t s);
 
 }  // namespace pkv

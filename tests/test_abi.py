@@ -59,6 +59,7 @@ def test_decode_argument_checks(pkv_lib):
     assert _decode(lib, maxb=200, part=512) == 1    # needs a workspace, none given
     assert "workspace" in lib.pkv_last_error().decode()
     assert _decode(lib, B=0) == 0                   # nothing to do
+    assert _decode(lib, maxb=4, ws=None) == 1       # the header is always needed
 
 
 def test_partition_and_workspace_sizes(pkv_lib):
@@ -68,11 +69,12 @@ def test_partition_and_workspace_sizes(pkv_lib):
     assert lib.pkv_resolve_partition_size(4, 8, 129, 16, -1) == 512
     assert lib.pkv_resolve_partition_size(4, 8, 8, 16, 512) == 128        # whole context fits one
     assert lib.pkv_resolve_partition_size(4, 8, 129, 32, 48) == -1
-    assert lib.pkv_workspace_size(4, 8, 8, 128, 8, 16, 512) == 0
+    assert lib.pkv_workspace_size(4, 8, 8, 128, 8, 16, 512) == 256  # the work-counter header only
     parts = -(-129 * 16 // 512)
     rows = 4 * 8 * parts
     ml = -(-(rows * 2 * 4) // 256) * 256
-    assert lib.pkv_workspace_size(4, 8, 8, 128, 129, 16, 512) == ml + rows * 128 * 4
+    assert lib.pkv_workspace_size(4, 8, 8, 128, 129, 16, 512) == 256 + ml + rows * 128 * 4
+    assert lib.pkv_workspace_size(4, 8, 8, 128, 129, 16, 48) == 0  # invalid partition size
 
 
 def test_append_and_copy_argument_checks(pkv_lib):
