@@ -141,8 +141,13 @@ def _traffic(workload: str):
         return None
 
 
-def setup(pkv, W, workload: str, seed: int, dev):
-    d = W.draw(workload, seed)
+def setup(pkv, W, workload: str, seed: int, dev, batch: int = 0):
+    import dataclasses
+    wl = W.WORKLOADS[workload]
+    if batch:
+        # a smaller batch of the same workload (profiling captures that must stay small)
+        wl = dataclasses.replace(wl, batch=batch, name=f"{wl.name}[batch={batch}]")
+    d = W.draw(wl, seed)
     wl = d.workload
     vals = W.make_values(d, device=dev)
     B = len(d.context_lens)
@@ -168,7 +173,7 @@ def run_native(args):
     torch.cuda.set_device(dev)
     pkv.load()
     pkv.set_kernel_path(args.kernel_path)
-    st = setup(pkv, W, args.workload, args.seed + rank, dev)
+    st = setup(pkv, W, args.workload, args.seed + rank, dev, args.batch)
     wl, vals = st["wl"], st["vals"]
     B = len(st["ids"])
     ps = args.partition_size
@@ -176,7 +181,8 @@ def run_native(args):
                               wl.block_size, ps)
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     max_parts = math.ceil(st["tables_h"].shape[1] * wl.block_size /
-                          pkv.resolve_partition_size(B, wl.num_kv_heads, st["tables_h"].shape[1], wl.block_size, ps))
+                          pkv.resolve_partition_size(B, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                                     st["tables_h"].shape[1], wl.block_size, ps))
     ks, vs = vals.get("k_scale"), vals.get("v_scale")
     stream = torch.cuda.current_stream(dev)
     npairs = st["pairs"].shape[0]
@@ -303,8 +309,8 @@ def run_native(args):
                    "block_size": wl.block_size, "act_dtype": wl.act_dtype, "cache_dtype": wl.cache_dtype,
                    "mean_context": float(st["lens_h"].mean()), "total_context_tokens": int(st["lens_h"].sum()),
                    "pool_blocks": st["d"].num_blocks,
-                   "partition_size": pkv.resolve_partition_size(B, wl.num_kv_heads, st["tables_h"].shape[1],
-                                                                wl.block_size, ps),
+                   "partition_size": pkv.resolve_partition_size(B, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                                                st["tables_h"].shape[1], wl.block_size, ps),
                    "l2": "inputs larger than L2 (K/V read per step %.2f GB vs 129 MB L2)" % (dec_bytes / 1e9),
                    "parallelism": f"replicas x{world} (sequences sharded, no collective)",
                    "kernel_path": args.kernel_path},
@@ -437,6 +443,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--partition-size", type=int, default=-1)
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling only)")
     ap.add_argument("--kernel-path", type=int, default=0,
                     help="decode kernel: 0 library choice, 1 CUDA-core, 2/3 tensor-core (1 or 2 CTAs per SM)")
     ap.add_argument("--no-e2e", action="store_true")

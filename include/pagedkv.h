@@ -151,10 +151,12 @@ size_t pkv_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int h
  * pkv_resolve_partition_size -- the partition size in tokens that
  * paged_attention_decode uses for these arguments (a value >= the longest
  * possible context means a single pass), or -1 if partition_size is not
- * accepted.  Host only.
+ * accepted.  PKV_PARTITION_AUTO gives 512 when num_q_heads/num_kv_heads >= 4,
+ * head_dim is 128 and num_seqs <= 2048 (the shapes the tensor-core kernel
+ * serves), else 1024.  Host only.
  */
-int pkv_resolve_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
-                               int block_size, int partition_size);
+int pkv_resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int max_blocks_per_seq, int block_size, int partition_size);
 
 /*
  * paged_block_copy -- copy whole physical blocks for copy-on-write.

@@ -100,9 +100,10 @@ def set_kernel_path(path: int) -> int:
     return prev
 
 
-def resolve_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, partition_size=PARTITION_AUTO):
-    return int(_native.lib().pkv_resolve_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
-                                                        partition_size))
+def resolve_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+                           partition_size=PARTITION_AUTO):
+    return int(_native.lib().pkv_resolve_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                        max_blocks_per_seq, block_size, partition_size))
 
 
 def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,

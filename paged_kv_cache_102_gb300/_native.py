@@ -29,7 +29,7 @@ SIGNATURES = {
     "paged_attention_decode_noalloc": (I32, [P, P, P, P, I32, P, I32, I32, I32, I32, I32, I32, F32, P, I32, I32,
                                              P, P, I32, P]),
     "pkv_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
-    "pkv_resolve_partition_size": (I32, [I32, I32, I32, I32, I32]),
+    "pkv_resolve_partition_size": (I32, [I32, I32, I32, I32, I32, I32, I32]),
     "paged_block_copy": (I32, [P, P, P, I32, I32, SZ, P]),
     "pkv_last_error": (ctypes.c_char_p, []),
     "pkv_device_error": (I32, [P, I32, P]),

@@ -42,7 +42,8 @@ int cuda_fail(const char* where, cudaError_t e) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kStageTokens = 32;  // tokens per shared-memory stage of the decode kernel
-constexpr int kAutoPartition = 512;
+constexpr int kAutoPartition = 1024;
+constexpr int kAutoPartitionGrouped = 512;
 constexpr size_t kWorkspaceHeader = 256;  // work counter of the tensor-core path
 
 std::atomic<int> g_kernel_path{PKV_PATH_AUTO};
@@ -82,18 +83,20 @@ int pkv_device_error(int* bits, int reset, void* stream) {
     return PKV_OK;
 }
 
-int pkv_resolve_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int block_size,
-                               int partition_size) {
-    (void)num_seqs;
-    (void)num_kv_heads;
-    if (max_blocks_per_seq < 1 || block_size < 1) return -1;
+int pkv_resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int max_blocks_per_seq, int block_size, int partition_size) {
+    if (max_blocks_per_seq < 1 || block_size < 1 || num_kv_heads < 1 || num_q_heads < 1) return -1;
     const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
     const long long single = (max_ctx + kStageTokens - 1) / kStageTokens * kStageTokens;
     long long P;
     if (partition_size == PKV_PARTITION_SINGLE) {
         P = single;
     } else if (partition_size == PKV_PARTITION_AUTO) {
-        P = kAutoPartition;
+        // the tensor-core grouped-query kernel holds 512 tokens of scores in tensor
+        // memory; the CUDA-core kernel amortises its per-partition work over 1024
+        const int G = num_q_heads / num_kv_heads;
+        const bool grouped = G >= 4 && head_dim == 128 && num_seqs <= 2048;
+        P = grouped ? kAutoPartitionGrouped : kAutoPartition;
     } else if (partition_size > 0) {
         if (partition_size % kStageTokens != 0 || partition_size % block_size != 0) return -1;
         P = partition_size;
@@ -107,8 +110,8 @@ int pkv_resolve_partition_size(int num_seqs, int num_kv_heads, int max_blocks_pe
 
 size_t pkv_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                           int max_blocks_per_seq, int block_size, int partition_size) {
-    const int P = pkv_resolve_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
-                                             partition_size);
+    const int P = pkv_resolve_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                             block_size, partition_size);
     if (P <= 0 || num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
     const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
     const long long parts = (max_ctx + P - 1) / P;
@@ -191,7 +194,8 @@ int paged_attention_decode(const void* q, const void* k_cache, const void* v_cac
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(workspace, 16))
         return fail(PKV_ERR_INVALID, "paged_attention_decode: q, caches, out, workspace must be 16-byte aligned");
-    const int P = pkv_resolve_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, partition_size);
+    const int P = pkv_resolve_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                             block_size, partition_size);
     if (P <= 0)
         return fail(PKV_ERR_INVALID, "paged_attention_decode: partition_size must be 0, -1 or a positive multiple of 32 and of block_size");
     const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;

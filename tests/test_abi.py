@@ -64,11 +64,13 @@ def test_decode_argument_checks(pkv_lib):
 
 def test_partition_and_workspace_sizes(pkv_lib):
     lib = pkv_lib._native.lib()
-    assert lib.pkv_resolve_partition_size(4, 8, 129, 16, 0) == 2080       # single pass: 2064 -> 2080
-    assert lib.pkv_resolve_partition_size(4, 8, 129, 16, 512) == 512
-    assert lib.pkv_resolve_partition_size(4, 8, 129, 16, -1) == 512
-    assert lib.pkv_resolve_partition_size(4, 8, 8, 16, 512) == 128        # whole context fits one
-    assert lib.pkv_resolve_partition_size(4, 8, 129, 32, 48) == -1
+    assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 129, 16, 0) == 2080   # single pass: 2064 -> 2080
+    assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 129, 16, 512) == 512
+    assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 129, 16, -1) == 1024  # CUDA-core shapes
+    assert lib.pkv_resolve_partition_size(4, 64, 8, 128, 129, 16, -1) == 512  # tensor-core shapes
+    assert lib.pkv_resolve_partition_size(4, 64, 8, 64, 129, 16, -1) == 1024
+    assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 8, 16, 512) == 128    # whole context fits one
+    assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 129, 32, 48) == -1
     assert lib.pkv_workspace_size(4, 8, 8, 128, 8, 16, 512) == 256  # the work-counter header only
     parts = -(-129 * 16 // 512)
     rows = 4 * 8 * parts
