@@ -153,13 +153,43 @@ def setup(pkv, W, workload: str, seed: int, dev, batch: int = 0):
     B = len(d.context_lens)
     ids = np.arange(B)
     bm = pkv.BlockManager(d.num_blocks, wl.block_size, free_list=d.free_list)
-    for i, c in enumerate(d.context_lens):
-        bm.add_sequence(i, int(c))
+    cow_pairs = 0
+    if wl.samples_per_prompt > 1:
+        # parallel sampling: each prompt's blocks are shared by its samples (ref count n);
+        # every sample then appends its divergent tokens one step at a time, which
+        # copies the shared partial block on the first divergent write of all but the
+        # last holder (untimed set-up; the timed step is the next token of every sample)
+        n = wl.samples_per_prompt
+        for pi, plen in enumerate(d.prompt_lens):
+            bm.add_sequence(pi * n, int(plen))
+            for j in range(1, n):
+                bm.fork(pi * n, pi * n + j)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed + 1000)
+        act = W.DTYPES[wl.act_dtype]
+        for step in range(int(d.divergent.max())):
+            active = np.nonzero(d.divergent > step)[0]
+            slots, pairs = bm.append_slots(active)
+            if len(pairs):
+                cow_pairs += len(pairs)
+                pkv.paged_block_copy(vals["k_cache"], vals["v_cache"], torch.from_numpy(pairs).to(dev))
+            kn = torch.randn(len(active), wl.num_kv_heads, wl.head_dim, generator=g, device=dev).to(act)
+            vn = torch.randn(len(active), wl.num_kv_heads, wl.head_dim, generator=g, device=dev).to(act)
+            pkv.paged_kv_append(kn, vn, torch.from_numpy(slots).to(dev), vals["k_cache"], vals["v_cache"])
+    else:
+        for i, c in enumerate(d.context_lens):
+            bm.add_sequence(i, int(c))
     slots, pairs = bm.append_slots(ids)
+    cow_pairs += len(pairs)
+    if len(pairs):
+        # copies needed before this step's own append (run once; the timed step rewrites the same slots)
+        pkv.paged_block_copy(vals["k_cache"], vals["v_cache"], torch.from_numpy(pairs).to(dev))
     tables, lens = bm.tables(ids)
+    unique_blocks = len({int(b) for i in ids for b in tables[i, : -(-int(lens[i]) // wl.block_size)]})
     st = dict(d=d, wl=wl, vals=vals, bm=bm, ids=ids, slots_h=slots, tables_h=tables, lens_h=lens,
-              slots=torch.from_numpy(slots).to(dev), pairs=torch.from_numpy(pairs).to(dev),
-              tables=torch.from_numpy(tables).to(dev), lens=torch.from_numpy(lens).to(dev))
+              slots=torch.from_numpy(slots).to(dev), pairs=torch.zeros((0, 2), dtype=torch.int32, device=dev),
+              tables=torch.from_numpy(tables).to(dev), lens=torch.from_numpy(lens).to(dev),
+              cow_pairs=cow_pairs, unique_blocks=unique_blocks)
     st["out"] = torch.empty_like(vals["q"])
     return st
 
@@ -309,6 +339,9 @@ def run_native(args):
                    "block_size": wl.block_size, "act_dtype": wl.act_dtype, "cache_dtype": wl.cache_dtype,
                    "mean_context": float(st["lens_h"].mean()), "total_context_tokens": int(st["lens_h"].sum()),
                    "pool_blocks": st["d"].num_blocks,
+                   "unique_kv_bytes_read": st["unique_blocks"] * wl.num_kv_heads * wl.block_size * wl.head_dim
+                                           * 2 * ELEM[wl.cache_dtype],
+                   "cow_block_copies_in_setup": st["cow_pairs"],
                    "partition_size": pkv.resolve_partition_size(B, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
                                                                 st["tables_h"].shape[1], wl.block_size, ps),
                    "l2": "inputs larger than L2 (K/V read per step %.2f GB vs 129 MB L2)" % (dec_bytes / 1e9),

@@ -238,6 +238,31 @@ enum pkv_kernel_path {
  */
 int pkv_set_kernel_path(int path);
 
+/* Directions of paged_block_swap. */
+enum pkv_swap_direction { PKV_SWAP_OUT = 0, PKV_SWAP_IN = 1 };
+
+/*
+ * paged_block_swap -- move whole physical blocks between the pools and a
+ * staging buffer, for preemption by swapping (the PagedAttention notes page,
+ * section on preemption: swapping moves the KV cache of a sequence that is
+ * not running to CPU memory and brings it back when there is room; small
+ * blocks make many small transfers).
+ *  block_ids  int32 [num_ids] (device): physical blocks, in staging order.
+ *  staging    [num_ids][2][block_bytes] bytes: for entry i, the K block then
+ *             the V block.  Pinned host memory (cudaHostAlloc, or registered
+ *             with cudaHostRegister) or device memory; the kernel reads or
+ *             writes it directly, in one launch for the whole list.
+ *  direction  PKV_SWAP_OUT: staging[i] = block block_ids[i] of k_cache, v_cache;
+ *             PKV_SWAP_IN:  block block_ids[i] = staging[i].
+ *  block_bytes one block of one cache (num_kv_heads*block_size*head_dim*elem),
+ *             a multiple of 16.  Unregistered pageable host memory is
+ *             refused (PKV_ERR_INVALID).  Ids outside [0, num_blocks) are
+ *             skipped and flag PKV_DEV_BAD_PAIR.  Swap-in ids must be distinct.
+ */
+int paged_block_swap(void* k_cache, void* v_cache, const int32_t* block_ids, int num_ids,
+                     int num_blocks, size_t block_bytes, void* staging, int direction,
+                     void* stream);
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char* pkv_last_error(void);
 
@@ -303,6 +328,42 @@ int pkv_bm_get_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n
                       int32_t* tables_out, int max_blocks_per_seq, int32_t pad,
                       int32_t* context_lens_out);
 
+/* Prefix caching (the PagedAttention notes page, on automatic prefix
+ * caching: a block is looked up by a hash of its own tokens and all tokens
+ * before it; Ultralytics glossary, section "Sharing blocks between
+ * sequences": hashing full blocks extends sharing across requests).
+ * Register a new sequence from its prompt token ids: every full block is
+ * keyed by a chained 64-bit FNV-1a hash of (previous block's key, this
+ * block's tokens); the blocks of the longest prefix already registered are
+ * shared (counts + 1) and *num_cached_tokens (host) receives the number of
+ * leading tokens whose K/V are already in the pool (a multiple of
+ * block_size); the remaining blocks are taken from the pool and its full
+ * blocks registered.  The caller writes K/V for tokens from
+ * *num_cached_tokens on.  A registered block whose count drops to 0 keeps
+ * its contents on a least-recently-freed list and is reused for new
+ * allocations (and unregistered) only when the free list is empty.  Only
+ * prompt blocks are registered; a 64-bit key match is trusted.
+ * PKV_ERR_NO_SPACE leaves no trace. */
+int pkv_bm_add_sequence_cached(pkv_block_manager* bm, int64_t seq_id, const int32_t* tokens,
+                               int num_tokens, int* num_cached_tokens);
+/* Preemption by swapping (the PagedAttention notes page, section on
+ * preemption).  pkv_bm_swap_out writes the sequence's block table (logical
+ * order, host int32, capacity cap) to blocks_out and *n, then releases the
+ * blocks (counts - 1) and keeps the sequence as swapped out (its length is
+ * remembered; it holds no blocks).  Run paged_block_swap(PKV_SWAP_OUT) on
+ * those blocks before any later call reuses them on the same stream.
+ * pkv_bm_swap_in gives a swapped-out sequence ceil(len/block_size) fresh
+ * private blocks (sharing with forks is not restored), writes them to
+ * blocks_out, and makes it resident; run paged_block_swap(PKV_SWAP_IN) into
+ * them.  A swapped-out sequence cannot append, fork or appear in tables;
+ * pkv_bm_free_sequence accepts it.  PKV_ERR_NO_SPACE leaves no trace. */
+int pkv_bm_swap_out(pkv_block_manager* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n);
+int pkv_bm_swap_in(pkv_block_manager* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n);
+
+/* Blocks registered in the prefix cache (in use or waiting on the LRU list). */
+int pkv_bm_num_cached_blocks(const pkv_block_manager* bm);
+
+/* Blocks available for allocation: the free list plus cached blocks with count 0. */
 int pkv_bm_num_free(const pkv_block_manager* bm);
 int pkv_bm_ref_count(const pkv_block_manager* bm, int block); /* -1 if out of range */
 int pkv_bm_context_len(const pkv_block_manager* bm, int64_t seq_id); /* -1 if unknown */

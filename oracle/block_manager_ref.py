@@ -17,9 +17,17 @@ dicts, one operation at a time, written from the pages:
   holding a copy, and the old block's count drops by one; full shared blocks
   stay shared with unchanged counts.
 
+* PagedAttention notes, section on automatic prefix caching: a KV block is
+  looked up by all tokens up to and including it; equal keys are equal
+  blocks.  Here the key is the exact token prefix itself (a tuple), not a
+  hash of it.
+
 Readings where the pages are silent: freed blocks go to the back of the free
 list; writers are processed one at a time in call order, and a writer copies
 only while the block's count is above 1, so the last holder writes in place.
+Prefix cache: only full prompt blocks are registered; a registered block whose
+count reaches 0 keeps its contents on a least-recently-freed list and is taken
+(and forgotten) only when the free list is empty.
 """
 from __future__ import annotations
 
@@ -36,11 +44,21 @@ class RefBlockManager:
         self.ref = [0] * num_blocks
         self.tables: dict[int, list[int]] = {}
         self.lens: dict[int, int] = {}
+        self.prefix_of_block: dict[int, tuple] = {}  # registered block -> its token prefix
+        self.block_of_prefix: dict[tuple, int] = {}
+        self.lru: list[int] = []  # registered blocks with count 0, least recently freed first
+
+    def available(self) -> int:
+        return len(self.free) + len(self.lru)
 
     def _take(self) -> int:
-        if not self.free:
+        if self.free:
+            b = self.free.pop(0)
+        elif self.lru:
+            b = self.lru.pop(0)
+            del self.block_of_prefix[self.prefix_of_block.pop(b)]
+        else:
             raise OutOfBlocks("no free block")
-        b = self.free.pop(0)
         self.ref[b] = 1
         return b
 
@@ -48,8 +66,8 @@ class RefBlockManager:
         """Give a new request ceil(num_tokens / bs) blocks (its prompt)."""
         assert seq not in self.tables
         need = -(-num_tokens // self.block_size)
-        if need > len(self.free):
-            raise OutOfBlocks(f"need {need} blocks, {len(self.free)} free")
+        if need > self.available():
+            raise OutOfBlocks(f"need {need} blocks, {self.available()} free")
         self.tables[seq] = [self._take() for _ in range(need)]
         self.lens[seq] = num_tokens
         return list(self.tables[seq])
@@ -72,6 +90,40 @@ class RefBlockManager:
         self.lens[seq] = pos + 1
         return table[pos // bs] * bs + pos % bs, cow
 
+    def add_sequence_cached(self, seq, tokens) -> int:
+        """Register a prompt by its token ids, sharing the blocks of the longest
+        registered prefix of full blocks; returns the number of leading tokens
+        whose blocks were shared."""
+        assert seq not in self.tables
+        tokens = [int(t) for t in tokens]
+        bs = self.block_size
+        n_full = len(tokens) // bs
+        n_blocks = -(-len(tokens) // bs)
+        shared = []
+        for i in range(n_full):
+            key = tuple(tokens[: (i + 1) * bs])
+            if key not in self.block_of_prefix:
+                break
+            shared.append(self.block_of_prefix[key])
+        revived = sum(1 for b in shared if self.ref[b] == 0)
+        if n_blocks - len(shared) > self.available() - revived:
+            raise OutOfBlocks("not enough free blocks")
+        for b in shared:
+            if self.ref[b] == 0:
+                self.lru.remove(b)
+            self.ref[b] += 1
+        table = list(shared)
+        for i in range(len(shared), n_blocks):
+            b = self._take()
+            if i < n_full:
+                key = tuple(tokens[: (i + 1) * bs])
+                self.block_of_prefix[key] = b
+                self.prefix_of_block[b] = key
+            table.append(b)
+        self.tables[seq] = table
+        self.lens[seq] = len(tokens)
+        return len(shared) * bs
+
     def fork(self, parent: int, child: int) -> None:
         """The child shares every block of the parent (counts + 1)."""
         assert child not in self.tables
@@ -82,11 +134,41 @@ class RefBlockManager:
 
     def free_sequence(self, seq: int) -> None:
         """Release a finished request: counts - 1, blocks at 0 go back to the pool."""
+        if seq in getattr(self, "swapped", {}):
+            del self.swapped[seq]
+            return
         for b in self.tables.pop(seq):
             self.ref[b] -= 1
             if self.ref[b] == 0:
-                self.free.append(b)
+                if b in self.prefix_of_block:
+                    self.lru.append(b)
+                else:
+                    self.free.append(b)
         del self.lens[seq]
+
+    def swap_out(self, seq) -> list:
+        """Preemption by swapping (PagedAttention notes, section on preemption):
+        release the sequence's blocks, remember its length; returns its table."""
+        table = self.tables.pop(seq)
+        for b in table:
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                if b in self.prefix_of_block:
+                    self.lru.append(b)
+                else:
+                    self.free.append(b)
+        self.swapped = getattr(self, "swapped", {})
+        self.swapped[seq] = self.lens.pop(seq)
+        return table
+
+    def swap_in(self, seq) -> list:
+        """Give a swapped-out sequence ceil(len / bs) fresh blocks; returns them."""
+        n = -(-self.swapped[seq] // self.block_size)
+        if n > self.available():
+            raise OutOfBlocks("not enough free blocks")
+        self.lens[seq] = self.swapped.pop(seq)
+        self.tables[seq] = [self._take() for _ in range(n)]
+        return list(self.tables[seq])
 
     def unused_slots(self, seq: int) -> int:
         """Slots allocated to the request but not yet written."""

@@ -32,8 +32,9 @@ PARTITION_AUTO = -1
 ERR_INVALID, ERR_SHAPE, ERR_CUDA, ERR_NO_SPACE, ERR_NOT_FOUND = 1, 2, 3, 4, 5
 DEV_BAD_BLOCK, DEV_BAD_CONTEXT_LEN, DEV_BAD_SLOT, DEV_BAD_PAIR, DEV_WAIT_TIMEOUT = 1, 2, 4, 8, 16
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR, PATH_TENSOR_2CTA = 0, 1, 2, 3
+SWAP_OUT, SWAP_IN = 0, 1
 
-__all__ = ["paged_kv_append", "paged_attention_decode", "paged_block_copy", "workspace_size",
+__all__ = ["paged_kv_append", "paged_attention_decode", "paged_block_copy", "paged_block_swap", "workspace_size",
            "resolve_partition_size", "device_error", "set_kernel_path", "BlockManager", "OutOfBlocks", "PagedKVError",
            "F16", "BF16", "E4M3", "PARTITION_SINGLE", "PARTITION_AUTO", "load"]
 
@@ -168,6 +169,23 @@ def paged_block_copy(k_cache, v_cache, src_dst_pairs, stream=None):
                  k_cache.shape[0], block_bytes, _stream(stream, k_cache.device))
 
 
+def paged_block_swap(k_cache, v_cache, block_ids, staging, direction, stream=None):
+    """Copy whole blocks between the pools and staging [n, 2, block_bytes] (uint8,
+    pinned host or device).  direction: SWAP_OUT (pools -> staging) or SWAP_IN."""
+    if block_ids.dtype != torch.int32 or block_ids.dim() != 1:
+        raise ValueError("paged_block_swap: block_ids must be int32 [n]")
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
+        raise ValueError("paged_block_swap: k_cache and v_cache must match")
+    _require_cuda(k_cache.device, k_cache=k_cache, v_cache=v_cache, block_ids=block_ids)
+    block_bytes = k_cache[0].numel() * k_cache.element_size()
+    if staging.numel() * staging.element_size() < block_ids.numel() * 2 * block_bytes or not staging.is_contiguous():
+        raise ValueError("paged_block_swap: staging must be contiguous with room for [n, 2, block_bytes]")
+    if not staging.is_cuda and not staging.is_pinned():
+        raise ValueError("paged_block_swap: host staging must be pinned memory")
+    _native.call("paged_block_swap", _ptr(k_cache), _ptr(v_cache), _ptr(block_ids), block_ids.numel(),
+                 k_cache.shape[0], block_bytes, _ptr(staging), int(direction), _stream(stream, k_cache.device))
+
+
 def device_error(reset: bool = True, stream=None, device=None) -> int:
     """Read (and by default clear) the current device's kernel error bits."""
     device = device or torch.device("cuda", torch.cuda.current_device())
@@ -204,6 +222,37 @@ class BlockManager:
 
     def add_sequence(self, seq_id: int, num_tokens: int) -> None:
         self._check("pkv_bm_add_sequence", _native.lib().pkv_bm_add_sequence(self._h, int(seq_id), int(num_tokens)))
+
+    def add_sequence_cached(self, seq_id: int, tokens) -> int:
+        """Register a prompt by token ids, sharing the longest cached prefix of
+        full blocks; returns how many leading tokens are already in the pool."""
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        cached = ctypes.c_int(0)
+        self._check("pkv_bm_add_sequence_cached", _native.lib().pkv_bm_add_sequence_cached(
+            self._h, int(seq_id), toks.ctypes.data_as(ctypes.c_void_p), len(toks), ctypes.byref(cached)))
+        return cached.value
+
+    def swap_out(self, seq_id: int) -> np.ndarray:
+        """Release a sequence's blocks, keeping it as swapped out; returns the
+        blocks (logical order) whose contents must be staged out first."""
+        n = max(self.num_seq_blocks(seq_id), 0)
+        out = np.empty(max(n, 1), np.int32)
+        cnt = ctypes.c_int(0)
+        self._check("pkv_bm_swap_out", _native.lib().pkv_bm_swap_out(
+            self._h, int(seq_id), out.ctypes.data_as(ctypes.c_void_p), len(out), ctypes.byref(cnt)))
+        return out[: cnt.value].copy()
+
+    def swap_in(self, seq_id: int, max_blocks: int) -> np.ndarray:
+        """Give a swapped-out sequence fresh blocks; returns them (logical order)."""
+        out = np.empty(max(max_blocks, 1), np.int32)
+        cnt = ctypes.c_int(0)
+        self._check("pkv_bm_swap_in", _native.lib().pkv_bm_swap_in(
+            self._h, int(seq_id), out.ctypes.data_as(ctypes.c_void_p), len(out), ctypes.byref(cnt)))
+        return out[: cnt.value].copy()
+
+    @property
+    def num_cached_blocks(self) -> int:
+        return int(_native.lib().pkv_bm_num_cached_blocks(self._h))
 
     def append_slots(self, seq_ids):
         """Reserve the next slot of each sequence; returns (slots int64 [n], cow_pairs int32 [k, 2])."""

@@ -31,6 +31,7 @@ SIGNATURES = {
     "pkv_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
     "pkv_resolve_partition_size": (I32, [I32, I32, I32, I32, I32, I32, I32]),
     "paged_block_copy": (I32, [P, P, P, I32, I32, SZ, P]),
+    "paged_block_swap": (I32, [P, P, P, I32, I32, SZ, P, I32, P]),
     "pkv_last_error": (ctypes.c_char_p, []),
     "pkv_device_error": (I32, [P, I32, P]),
     "pkv_version": (I32, []),
@@ -42,6 +43,10 @@ SIGNATURES = {
     "pkv_bm_fork": (I32, [P, I64, I64]),
     "pkv_bm_free_sequence": (I32, [P, I64]),
     "pkv_bm_get_tables": (I32, [P, P, I32, P, I32, I32, P]),
+    "pkv_bm_add_sequence_cached": (I32, [P, I64, P, I32, P]),
+    "pkv_bm_num_cached_blocks": (I32, [P]),
+    "pkv_bm_swap_out": (I32, [P, I64, P, I32, P]),
+    "pkv_bm_swap_in": (I32, [P, I64, P, I32, P]),
     "pkv_bm_num_free": (I32, [P]),
     "pkv_bm_ref_count": (I32, [P, I32]),
     "pkv_bm_context_len": (I32, [P, I64]),

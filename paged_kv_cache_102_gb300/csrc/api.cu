@@ -165,6 +165,31 @@ int paged_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs,
     return PKV_OK;
 }
 
+int paged_block_swap(void* k_cache, void* v_cache, const int32_t* block_ids, int num_ids, int num_blocks,
+                     size_t block_bytes, void* staging, int direction, void* stream) {
+    if (num_ids < 0 || num_blocks <= 0 || block_bytes == 0 || block_bytes % 16 != 0 ||
+        (direction != PKV_SWAP_OUT && direction != PKV_SWAP_IN))
+        return fail(PKV_ERR_INVALID, "paged_block_swap: bad sizes or direction");
+    if (num_ids == 0) return PKV_OK;
+    if (num_ids > 0x7fffffff / 2) return fail(PKV_ERR_INVALID, "paged_block_swap: too many blocks");
+    if (!k_cache || !v_cache || !block_ids || !staging) return fail(PKV_ERR_INVALID, "paged_block_swap: null pointer");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(staging, 16) || !aligned(block_ids, 4))
+        return fail(PKV_ERR_INVALID, "paged_block_swap: buffers must be 16-byte aligned");
+    cudaPointerAttributes attr{};
+    cudaError_t e = cudaPointerGetAttributes(&attr, staging);
+    if (e != cudaSuccess) return cuda_fail("paged_block_swap: staging pointer", e);
+    if (attr.type == cudaMemoryTypeUnregistered)
+        return fail(PKV_ERR_INVALID, "paged_block_swap: staging must be device memory or pinned/registered host memory");
+    int* err = device_error_word();
+    if (!err) return fail(PKV_ERR_CUDA, "paged_block_swap: cannot resolve the device error word");
+    void* dev_staging = attr.type == cudaMemoryTypeHost && attr.devicePointer ? attr.devicePointer : staging;
+    SwapParams p{k_cache, v_cache, block_ids, dev_staging, err, block_bytes, num_blocks,
+                 direction == PKV_SWAP_OUT ? 1 : 0};
+    e = launch_block_swap(p, num_ids, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("paged_block_swap: launch", e);
+    return PKV_OK;
+}
+
 int paged_attention_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                            int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
                            int num_kv_heads, int block_size, int head_dim, int num_blocks, float scale, void* out,

@@ -12,9 +12,21 @@
 // to store the KV cache", sections "Physical Block sharing" and
 // "Copy-on-Write").  Writers are handled in call order; the last holder of
 // a block writes in place.
+//
+// Prefix caching (PagedAttention notes, section on Automatic Prefix Caching:
+// a KV block is looked up by a hash of its own tokens and all tokens before
+// it; equal hashes mean equal blocks; Ultralytics glossary "PagedAttention",
+// section "Sharing blocks between sequences": hashing full blocks extends
+// sharing across requests).  pkv_bm_add_sequence_cached keys every full
+// block of a prompt by a chained 64-bit FNV-1a hash over (previous block's
+// hash, this block's token ids), reuses the blocks already registered for
+// the longest matching prefix, and registers the new full blocks.  A freed
+// block that is registered keeps its contents and waits on an LRU list; it
+// is taken (and unregistered) only when the free list is empty.
 #include <cstdint>
 #include <cstring>
 #include <deque>
+#include <list>
 #include <string>
 #include <unordered_map>
 #include <unordered_set>
@@ -28,7 +40,37 @@ namespace {
 struct Sequence {
     std::vector<int32_t> blocks;
     int64_t len = 0;
+    bool swapped = false;  // contents staged outside the pool; no blocks held
 };
+
+}  // namespace
+
+namespace {
+
+// FNV-1a, 64-bit: offset basis 14695981039346656037, prime 1099511628211.
+constexpr uint64_t kFnvBasis = 14695981039346656037ull;
+constexpr uint64_t kFnvPrime = 1099511628211ull;
+
+uint64_t fnv1a_bytes(uint64_t h, const void* data, size_t n) {
+    const unsigned char* p = static_cast<const unsigned char*>(data);
+    for (size_t i = 0; i < n; ++i) {
+        h ^= p[i];
+        h *= kFnvPrime;
+    }
+    return h;
+}
+
+// Hash of a full block: chained over the previous block's hash and this block's tokens.
+uint64_t block_hash(uint64_t parent, const int32_t* tokens, int n) {
+    uint64_t h = fnv1a_bytes(kFnvBasis, &parent, sizeof(parent));
+    for (int i = 0; i < n; ++i) {
+        const uint32_t t = static_cast<uint32_t>(tokens[i]);
+        const unsigned char b[4] = {static_cast<unsigned char>(t), static_cast<unsigned char>(t >> 8),
+                                    static_cast<unsigned char>(t >> 16), static_cast<unsigned char>(t >> 24)};
+        h = fnv1a_bytes(h, b, 4);
+    }
+    return h;
+}
 
 }  // namespace
 
@@ -38,15 +80,48 @@ struct pkv_block_manager {
     std::deque<int32_t> free_list;
     std::vector<int32_t> ref;
     std::unordered_map<int64_t, Sequence> seqs;
+    // prefix cache
+    std::unordered_map<uint64_t, int32_t> cached;  // hash -> block
+    std::vector<uint64_t> hash_of;                 // per block, valid when registered[b]
+    std::vector<char> registered;
+    std::list<int32_t> evictable;  // registered blocks with count 0, least recently freed first
+    std::vector<std::list<int32_t>::iterator> evict_pos;
 
+    int available() const { return static_cast<int>(free_list.size() + evictable.size()); }
+
+    void unregister(int32_t b) {
+        if (registered[b]) {
+            cached.erase(hash_of[b]);
+            registered[b] = 0;
+        }
+    }
     int32_t take() {
-        int32_t b = free_list.front();
-        free_list.pop_front();
+        int32_t b;
+        if (!free_list.empty()) {
+            b = free_list.front();
+            free_list.pop_front();
+        } else {
+            b = evictable.front();
+            evictable.pop_front();
+            unregister(b);
+        }
         ref[b] = 1;
         return b;
     }
     void release(int32_t b) {
-        if (--ref[b] == 0) free_list.push_back(b);
+        if (--ref[b] == 0) {
+            if (registered[b]) {
+                evictable.push_back(b);
+                evict_pos[b] = std::prev(evictable.end());
+            } else {
+                free_list.push_back(b);
+            }
+        }
+    }
+    // A registered block is referenced again.
+    void revive(int32_t b) {
+        if (ref[b] == 0) evictable.erase(evict_pos[b]);
+        ++ref[b];
     }
 };
 
@@ -62,6 +137,9 @@ pkv_block_manager* pkv_bm_create(int num_blocks, int block_size, const int32_t* 
     bm->num_blocks = num_blocks;
     bm->block_size = block_size;
     bm->ref.assign(num_blocks, 0);
+    bm->hash_of.assign(num_blocks, 0);
+    bm->registered.assign(num_blocks, 0);
+    bm->evict_pos.resize(num_blocks);
     if (free_list == nullptr) {
         for (int i = 0; i < num_blocks; ++i) bm->free_list.push_back(i);
     } else {
@@ -86,7 +164,7 @@ int pkv_bm_add_sequence(pkv_block_manager* bm, int64_t seq_id, int num_tokens) {
     if (!bm || num_tokens < 0) return pkv::fail(PKV_ERR_INVALID, "pkv_bm_add_sequence: bad arguments");
     if (bm->seqs.count(seq_id)) return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_add_sequence: sequence id already in use");
     int64_t need = (static_cast<int64_t>(num_tokens) + bm->block_size - 1) / bm->block_size;
-    if (need > static_cast<int64_t>(bm->free_list.size()))
+    if (need > bm->available())
         return pkv::fail(PKV_ERR_NO_SPACE, "pkv_bm_add_sequence: not enough free blocks");
     Sequence s;
     s.len = num_tokens;
@@ -107,8 +185,8 @@ int pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n, in
     int64_t need = 0;
     for (int i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seq_ids[i]);
-        if (it == bm->seqs.end() || !seen.insert(seq_ids[i]).second)
-            return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_append_slots: unknown or repeated sequence id");
+        if (it == bm->seqs.end() || !seen.insert(seq_ids[i]).second || it->second.swapped)
+            return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_append_slots: unknown, repeated or swapped-out sequence id");
         const Sequence& s = it->second;
         if (s.len % bs == 0) {
             ++need;
@@ -120,7 +198,7 @@ int pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n, in
             }
         }
     }
-    if (need > static_cast<int64_t>(bm->free_list.size()))
+    if (need > bm->available())
         return pkv::fail(PKV_ERR_NO_SPACE, "pkv_bm_append_slots: not enough free blocks for the batch");
     // Pass 2: apply.
     int pairs = 0;
@@ -151,8 +229,8 @@ int pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n, in
 int pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_id) {
     if (!bm) return pkv::fail(PKV_ERR_INVALID, "pkv_bm_fork: null manager");
     auto it = bm->seqs.find(parent_id);
-    if (it == bm->seqs.end() || bm->seqs.count(child_id))
-        return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_fork: unknown parent or child id in use");
+    if (it == bm->seqs.end() || bm->seqs.count(child_id) || it->second.swapped)
+        return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_fork: unknown or swapped-out parent, or child id in use");
     Sequence child = it->second;
     for (int32_t b : child.blocks) ++bm->ref[b];
     bm->seqs.emplace(child_id, std::move(child));
@@ -163,7 +241,7 @@ int pkv_bm_free_sequence(pkv_block_manager* bm, int64_t seq_id) {
     if (!bm) return pkv::fail(PKV_ERR_INVALID, "pkv_bm_free_sequence: null manager");
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_free_sequence: unknown id");
-    for (int32_t b : it->second.blocks) bm->release(b);
+    for (int32_t b : it->second.blocks) bm->release(b);  // a swapped-out sequence holds none
     bm->seqs.erase(it);
     return PKV_OK;
 }
@@ -174,7 +252,8 @@ int pkv_bm_get_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n
         return pkv::fail(PKV_ERR_INVALID, "pkv_bm_get_tables: bad arguments");
     for (int i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seq_ids[i]);
-        if (it == bm->seqs.end()) return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_get_tables: unknown id");
+        if (it == bm->seqs.end() || it->second.swapped)
+            return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_get_tables: unknown or swapped-out id");
         const Sequence& s = it->second;
         if (static_cast<int64_t>(s.blocks.size()) > max_blocks_per_seq)
             return pkv::fail(PKV_ERR_SHAPE, "pkv_bm_get_tables: a table is longer than max_blocks_per_seq");
@@ -186,7 +265,92 @@ int pkv_bm_get_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n
     return PKV_OK;
 }
 
-int pkv_bm_num_free(const pkv_block_manager* bm) { return bm ? static_cast<int>(bm->free_list.size()) : -1; }
+int pkv_bm_add_sequence_cached(pkv_block_manager* bm, int64_t seq_id, const int32_t* tokens, int num_tokens,
+                               int* num_cached_tokens) {
+    if (!bm || num_tokens < 0 || (num_tokens > 0 && !tokens) || !num_cached_tokens)
+        return pkv::fail(PKV_ERR_INVALID, "pkv_bm_add_sequence_cached: bad arguments");
+    if (bm->seqs.count(seq_id))
+        return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_add_sequence_cached: sequence id already in use");
+    const int bs = bm->block_size;
+    const int n_full = num_tokens / bs;
+    const int n_blocks = (num_tokens + bs - 1) / bs;
+    // longest registered prefix of full blocks
+    std::vector<uint64_t> hashes(n_full);
+    uint64_t h = 0;
+    for (int i = 0; i < n_full; ++i) {
+        h = block_hash(h, tokens + static_cast<size_t>(i) * bs, bs);
+        hashes[i] = h;
+    }
+    int reused = 0;
+    int revived_from_lru = 0;
+    while (reused < n_full) {
+        auto it = bm->cached.find(hashes[reused]);
+        if (it == bm->cached.end()) break;
+        if (bm->ref[it->second] == 0) ++revived_from_lru;
+        ++reused;
+    }
+    const int fresh = n_blocks - reused;
+    if (fresh > bm->available() - revived_from_lru)
+        return pkv::fail(PKV_ERR_NO_SPACE, "pkv_bm_add_sequence_cached: not enough free blocks");
+    Sequence s;
+    s.len = num_tokens;
+    for (int i = 0; i < reused; ++i) {
+        const int32_t b = bm->cached[hashes[i]];
+        bm->revive(b);
+        s.blocks.push_back(b);
+    }
+    for (int i = reused; i < n_blocks; ++i) {
+        const int32_t b = bm->take();
+        if (i < n_full) {
+            bm->hash_of[b] = hashes[i];
+            bm->registered[b] = 1;
+            bm->cached[hashes[i]] = b;
+        }
+        s.blocks.push_back(b);
+    }
+    bm->seqs.emplace(seq_id, std::move(s));
+    *num_cached_tokens = reused * bs;
+    return PKV_OK;
+}
+
+int pkv_bm_swap_out(pkv_block_manager* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n) {
+    if (!bm || !n || cap < 0) return pkv::fail(PKV_ERR_INVALID, "pkv_bm_swap_out: bad arguments");
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end() || it->second.swapped)
+        return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_swap_out: unknown or already swapped-out id");
+    Sequence& s = it->second;
+    const int nb = static_cast<int>(s.blocks.size());
+    if (nb > cap || (nb > 0 && !blocks_out)) return pkv::fail(PKV_ERR_SHAPE, "pkv_bm_swap_out: output too small");
+    for (int i = 0; i < nb; ++i) blocks_out[i] = s.blocks[i];
+    for (int32_t b : s.blocks) bm->release(b);
+    s.blocks.clear();
+    s.swapped = true;
+    *n = nb;
+    return PKV_OK;
+}
+
+int pkv_bm_swap_in(pkv_block_manager* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n) {
+    if (!bm || !n || cap < 0) return pkv::fail(PKV_ERR_INVALID, "pkv_bm_swap_in: bad arguments");
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end() || !it->second.swapped)
+        return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_swap_in: unknown or resident id");
+    Sequence& s = it->second;
+    const int nb = static_cast<int>((s.len + bm->block_size - 1) / bm->block_size);
+    if (nb > cap || (nb > 0 && !blocks_out)) return pkv::fail(PKV_ERR_SHAPE, "pkv_bm_swap_in: output too small");
+    if (nb > bm->available()) return pkv::fail(PKV_ERR_NO_SPACE, "pkv_bm_swap_in: not enough free blocks");
+    for (int i = 0; i < nb; ++i) {
+        const int32_t b = bm->take();
+        s.blocks.push_back(b);
+        blocks_out[i] = b;
+    }
+    s.swapped = false;
+    *n = nb;
+    return PKV_OK;
+}
+
+int pkv_bm_num_cached_blocks(const pkv_block_manager* bm) { return bm ? static_cast<int>(bm->cached.size()) : -1; }
+
+int pkv_bm_num_free(const pkv_block_manager* bm) { return bm ? bm->available() : -1; }
 
 int pkv_bm_ref_count(const pkv_block_manager* bm, int block) {
     if (!bm || block < 0 || block >= bm->num_blocks) return -1;

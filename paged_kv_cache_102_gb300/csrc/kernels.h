@@ -34,6 +34,17 @@ struct CopyParams {
     int num_blocks;
 };
 
+struct SwapParams {
+    void* k_cache;
+    void* v_cache;
+    const int32_t* block_ids;
+    void* staging;  // [n][2][block_bytes]: K then V of each listed block
+    int* err;
+    size_t block_bytes;
+    int num_blocks;
+    int to_staging;  // 1: pools -> staging (swap out), 0: staging -> pools (swap in)
+};
+
 struct DecodeParams {
     const void* q;
     const void* k_cache;
@@ -71,6 +82,7 @@ struct MergeParams {
 
 cudaError_t launch_append(const AppendParams& p, int act, int cache, cudaStream_t stream);
 cudaError_t launch_block_copy(const CopyParams& p, int num_pairs, cudaStream_t stream);
+cudaError_t launch_block_swap(const SwapParams& p, int n, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int act, int num_seqs, cudaStream_t stream);
 
 // Partition kernel for one (act, cache) pair; returns cudaErrorInvalidValue

@@ -117,6 +117,50 @@ cudaError_t launch_block_copy(const CopyParams& p, int num_pairs, cudaStream_t s
 }
 
 // ---------------------------------------------------------------------------
+// Block swap (PagedAttention notes, section "Preemption": swapping moves the
+// KV cache of a sequence that is not running to CPU DRAM and brings it back
+// later).  One launch gathers (out) or scatters (in) whole physical blocks,
+// K and V, between the pools and a staging buffer [n][K block, V block]
+// that may live in pinned host memory: the kernel reads or writes it
+// directly, so scattered small blocks cost no per-copy overhead.
+// grid.x = block i of the list, grid.y = 16 KB chunk of the block.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) paged_block_swap_kernel(SwapParams p) {
+    const int i = blockIdx.x;
+    const int b = p.block_ids[i];
+    if (b < 0 || b >= p.num_blocks) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(p.err, kErrBadPair);
+        return;
+    }
+    const size_t begin = static_cast<size_t>(blockIdx.y) * kCopyChunkBytes;
+    const size_t end = min(begin + kCopyChunkBytes, p.block_bytes);
+    unsigned char* kd = static_cast<unsigned char*>(p.k_cache) + static_cast<size_t>(b) * p.block_bytes;
+    unsigned char* vd = static_cast<unsigned char*>(p.v_cache) + static_cast<size_t>(b) * p.block_bytes;
+    unsigned char* ks = static_cast<unsigned char*>(p.staging) + static_cast<size_t>(i) * 2 * p.block_bytes;
+    unsigned char* vs = ks + p.block_bytes;
+    for (size_t o = begin + threadIdx.x * 16; o < end; o += blockDim.x * 16) {
+        if (p.to_staging) {
+            const uint4 a = *reinterpret_cast<const uint4*>(kd + o);
+            const uint4 c = *reinterpret_cast<const uint4*>(vd + o);
+            *reinterpret_cast<uint4*>(ks + o) = a;
+            *reinterpret_cast<uint4*>(vs + o) = c;
+        } else {
+            const uint4 a = *reinterpret_cast<const uint4*>(ks + o);
+            const uint4 c = *reinterpret_cast<const uint4*>(vs + o);
+            *reinterpret_cast<uint4*>(kd + o) = a;
+            *reinterpret_cast<uint4*>(vd + o) = c;
+        }
+    }
+}
+
+cudaError_t launch_block_swap(const SwapParams& p, int n, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    const unsigned chunks = static_cast<unsigned>((p.block_bytes + kCopyChunkBytes - 1) / kCopyChunkBytes);
+    paged_block_swap_kernel<<<dim3(n, chunks), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Split-K merge.  Each partition p of a sequence left (m_p, l_p, o_p) with
 // o_p already divided by l_p and m_p in log2 units; the full softmax is
 //   out = sum_p w_p o_p / sum_p w_p,  w_p = l_p * 2^(m_p - max_p m_p).

@@ -126,3 +126,64 @@ def test_errors(pkv_lib):
         pkv_lib.BlockManager(4, 16, free_list=[0, 0])
     t, lens = bm.tables([1], max_blocks_per_seq=3, pad=-1)
     assert list(t[0]) == [0, -1, -1] and lens[0] == 10
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_swap_out_in_matches_oracle(pkv_lib, seed):
+    rng = np.random.default_rng(100 + seed)
+    NB, bs = int(rng.integers(10, 40)), int(rng.choice([4, 16]))
+    fl = rng.permutation(NB).astype(np.int32)
+    bm = pkv_lib.BlockManager(NB, bs, free_list=fl)
+    ref = RefBlockManager(NB, bs, free_list=fl)
+    live, out, nid = [], [], 0
+    for _ in range(250):
+        op = int(rng.integers(0, 6))
+        if op == 0 or not (live or out):
+            n = int(rng.integers(1, 3 * bs))
+            try:
+                ref.add_sequence(nid, n)
+                bm.add_sequence(nid, n)
+                live.append(nid)
+            except RefOutOfBlocks:
+                with pytest.raises(pkv_lib.OutOfBlocks):
+                    bm.add_sequence(nid, n)
+            nid += 1
+        elif op == 1 and live:
+            s = int(rng.choice(live))
+            try:
+                want = ref.append_slot(s)
+            except RefOutOfBlocks:
+                continue  # (state unchanged on both sides only if the product also refuses)
+            slots, _ = bm.append_slots([s])
+            assert slots[0] == want[0]
+        elif op == 2 and live:
+            parent = int(rng.choice(live))
+            ref.fork(parent, nid)
+            bm.fork(parent, nid)
+            live.append(nid)
+            nid += 1
+        elif op == 3 and live:
+            s = live.pop(int(rng.integers(0, len(live))))
+            assert list(bm.swap_out(s)) == ref.swap_out(s)
+            out.append(s)
+            with pytest.raises(pkv_lib.PagedKVError):
+                bm.append_slots([s])
+        elif op == 4 and out:
+            s = out[int(rng.integers(0, len(out)))]
+            try:
+                want = ref.swap_in(s)
+            except RefOutOfBlocks:
+                with pytest.raises(pkv_lib.OutOfBlocks):
+                    bm.swap_in(s, 64)
+                continue
+            assert list(bm.swap_in(s, 64)) == want
+            out.remove(s)
+            live.append(s)
+        elif op == 5 and (live or out):
+            pool = live + out
+            s = pool[int(rng.integers(0, len(pool)))]
+            bm.free_sequence(s)
+            ref.free_sequence(s)
+            (live if s in live else out).remove(s)
+        assert list(bm.free_list()) == ref.free
+        assert [bm.ref_count(b) for b in range(NB)] == ref.ref

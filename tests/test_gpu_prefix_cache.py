@@ -1,0 +1,79 @@
+"""Prefix caching end to end on the GPU: requests that share a system prompt
+reuse its full blocks (their K/V are written once, by the first request), and
+decode over the shared blocks matches the float64 oracle computed with the
+oracle's own allocator, append and tables."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.block_manager_ref import RefBlockManager
+from tests.parity import TOL, assert_attention_close, bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _kv_for_prefix(tokens, pos, Hkv, D):
+    """K/V of token `pos`: a deterministic function of tokens[: pos + 1], as in a model."""
+    seed = zlib.crc32(np.asarray(tokens[: pos + 1], dtype=np.int32).tobytes())
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((2, Hkv, D)).astype(np.float32)
+
+
+def test_prefix_cached_decode_matches_oracle(pkv_lib, cuda_device):
+    pkv = pkv_lib
+    pkv.device_error(reset=True)
+    bs, Hq, Hkv, D, NB = 16, 8, 4, 64, 64
+    rng = np.random.default_rng(3)
+    system = list(rng.integers(0, 30000, size=50))  # 3 full blocks + 2 tokens
+    prompts = [system + list(rng.integers(0, 30000, size=int(n))) for n in (9, 30, 0, 61)]
+    prompts.append(list(rng.integers(0, 30000, size=20)))  # unrelated request
+    bm = pkv.BlockManager(NB, bs)
+    ref = RefBlockManager(NB, bs)
+    kc = torch.zeros(NB, Hkv, bs, D, dtype=torch.float16, device=cuda_device)
+    vc = torch.zeros_like(kc)
+    rk, rv = bits(kc).copy(), bits(vc).copy()
+    cached_counts = []
+    for sid, toks in enumerate(prompts):
+        cached = bm.add_sequence_cached(sid, toks)
+        assert cached == ref.add_sequence_cached(sid, toks)
+        cached_counts.append(cached)
+        t, _ = bm.tables([sid])
+        assert list(t[0][: len(ref.tables[sid])]) == ref.tables[sid]
+        # write K/V only for the tokens that are not already in the pool
+        pos = np.arange(cached, len(toks))
+        if len(pos) == 0:
+            continue
+        kv = np.stack([_kv_for_prefix(toks, int(p), Hkv, D) for p in pos])  # [n, 2, Hkv, D]
+        k_new = torch.from_numpy(kv[:, 0]).half()
+        v_new = torch.from_numpy(kv[:, 1]).half()
+        slots = np.array([oracle.slot_of(ref.tables[sid], int(p), bs) for p in pos], np.int64)
+        pkv.paged_kv_append(k_new.to(cuda_device), v_new.to(cuda_device), torch.from_numpy(slots).to(cuda_device),
+                            kc, vc)
+        oracle.append(bits(k_new), bits(v_new), oracle.F16, slots, rk, rv, oracle.F16)
+    assert cached_counts == [0, 48, 48, 48, 0]
+    t_first, _ = bm.tables([0])
+    for sid in (1, 2, 3):
+        t, _ = bm.tables([sid])
+        assert list(t[0][:3]) == list(t_first[0][:3])  # the system prompt's full blocks are shared
+    ids = np.arange(len(prompts))
+    tables, lens = bm.tables(ids)
+    q = torch.randn(len(prompts), Hq, D, generator=torch.Generator().manual_seed(5)).half()
+    out = pkv.paged_attention_decode(q.to(cuda_device), kc, vc, torch.from_numpy(tables).to(cuda_device),
+                                     torch.from_numpy(lens).to(cuda_device), 0.125)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(kc), rk) and np.array_equal(bits(vc), rv)
+    want = oracle.paged_decode(bits(q), oracle.F16, rk, rv, oracle.F16, tables, lens, 0.125)
+    assert_attention_close(out, want, TOL["f16"], rounding_slack=True)
+    # and each request's attention equals attention over its own, unshared K/V
+    for sid, toks in enumerate(prompts):
+        kv = np.stack([_kv_for_prefix(toks, p, Hkv, D) for p in range(len(toks))])
+        K = torch.from_numpy(kv[:, 0]).half().double().permute(1, 0, 2)  # [Hkv, L, D]
+        V = torch.from_numpy(kv[:, 1]).half().double().permute(1, 0, 2)
+        qq = q[sid].double().view(Hkv, Hq // Hkv, 1, D)
+        o = torch.nn.functional.scaled_dot_product_attention(qq, K[:, None].expand(Hkv, Hq // Hkv, -1, D),
+                                                             V[:, None].expand(Hkv, Hq // Hkv, -1, D), scale=0.125)
+        assert np.abs(o.reshape(Hq, D).numpy() - want[sid]).max() < 1e-9
+    assert pkv.device_error(reset=True) == 0
