@@ -220,13 +220,20 @@ def run_native(args):
     def step(ev_mid=None):
         if npairs:
             pkv.paged_block_copy(vals["k_cache"], vals["v_cache"], st["pairs"])
+        if args.fused:
+            if ev_mid is not None:
+                ev_mid.record(stream)
+            pkv.paged_attention_decode_append(vals["q"], vals["k_new"], vals["v_new"], st["slots"], vals["k_cache"],
+                                              vals["v_cache"], st["tables"], st["lens"], wl.scale, out=st["out"],
+                                              k_scale=ks, v_scale=vs, partition_size=ps, workspace=ws)
+            return
         pkv.paged_kv_append(vals["k_new"], vals["v_new"], st["slots"], vals["k_cache"], vals["v_cache"], ks, vs)
         if ev_mid is not None:
             ev_mid.record(stream)
         pkv.paged_attention_decode(vals["q"], vals["k_cache"], vals["v_cache"], st["tables"], st["lens"], wl.scale,
                                    out=st["out"], k_scale=ks, v_scale=vs, partition_size=ps, workspace=ws)
 
-    launches_per_step = (1 if npairs else 0) + 1 + 1 + (1 if max_parts > 1 else 0)
+    launches_per_step = (1 if npairs else 0) + (0 if args.fused else 1) + 1 + (1 if max_parts > 1 else 0)
     dec_bytes, app_bytes = algorithmic_bytes(wl, st["lens_h"])
     step_bytes = dec_bytes + app_bytes
 
@@ -297,9 +304,14 @@ def run_native(args):
             dslots.copy_(host["slots"], non_blocking=True)
             dtab.copy_(t_pin, non_blocking=True)
             dlens.copy_(l_pin, non_blocking=True)
-            pkv.paged_kv_append(dk, dv, dslots, vals["k_cache"], vals["v_cache"], ks, vs)
-            pkv.paged_attention_decode(dq, vals["k_cache"], vals["v_cache"], dtab, dlens, wl.scale, out=st["out"],
-                                       k_scale=ks, v_scale=vs, partition_size=ps, workspace=ws)
+            if args.fused:
+                pkv.paged_attention_decode_append(dq, dk, dv, dslots, vals["k_cache"], vals["v_cache"], dtab, dlens,
+                                                  wl.scale, out=st["out"], k_scale=ks, v_scale=vs,
+                                                  partition_size=ps, workspace=ws)
+            else:
+                pkv.paged_kv_append(dk, dv, dslots, vals["k_cache"], vals["v_cache"], ks, vs)
+                pkv.paged_attention_decode(dq, vals["k_cache"], vals["v_cache"], dtab, dlens, wl.scale,
+                                           out=st["out"], k_scale=ks, v_scale=vs, partition_size=ps, workspace=ws)
             out_h.copy_(st["out"], non_blocking=True)
             torch.cuda.current_stream(dev).synchronize()
 
@@ -346,7 +358,7 @@ def run_native(args):
                                                                 st["tables_h"].shape[1], wl.block_size, ps),
                    "l2": "inputs larger than L2 (K/V read per step %.2f GB vs 129 MB L2)" % (dec_bytes / 1e9),
                    "parallelism": f"replicas x{world} (sequences sharded, no collective)",
-                   "kernel_path": args.kernel_path},
+                   "kernel_path": args.kernel_path, "fused_append": bool(args.fused)},
         "pct_of_peak": round(100 * value / peak, 2),
         "seq_steps_per_s": round(B * world / (ms_step * 1e-3), 1),
         "bytes_per_step": {"decode": dec_bytes, "append": app_bytes},
@@ -467,6 +479,53 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_swap(args):
+    """Swap bandwidth between the pools and pinned host memory, by block size:
+    one gather/scatter launch for all blocks vs one cudaMemcpyAsync per block."""
+    import paged_kv_cache_102_gb300 as pkv
+    dev = torch.device("cuda", 0)
+    pkv.load()
+    Hkv, D = 32, 128
+    total = 1 << 30  # bytes of K+V moved per direction
+    for bs in (1, 4, 16, 32, 64):
+        block_bytes = Hkv * bs * D * 2
+        n = total // (2 * block_bytes)
+        NB = 2 * n
+        kc = torch.empty(NB, Hkv, bs, D, dtype=torch.bfloat16, device=dev).normal_()
+        vc = torch.empty_like(kc).normal_()
+        ids = torch.randperm(NB, device=dev)[:n].to(torch.int32)
+        staging = torch.empty(n, 2, block_bytes, dtype=torch.uint8).pin_memory()
+        res = {}
+        for name, direction in (("out", pkv.SWAP_OUT), ("in", pkv.SWAP_IN)):
+            for _ in range(2):
+                pkv.paged_block_swap(kc, vc, ids, staging, direction)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                pkv.paged_block_swap(kc, vc, ids, staging, direction)
+            e1.record()
+            torch.cuda.synchronize()
+            res[f"kernel_{name}_gbs"] = round(total * args.steps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+        # per-block copies (what a loop of cudaMemcpyAsync calls would do), swap-out direction
+        ids_h = ids.cpu().numpy()
+        kflat, vflat = kc.view(NB, -1).view(torch.uint8), vc.view(NB, -1).view(torch.uint8)
+        m = min(n, 4096)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for j in range(m):
+            staging[j, 0].copy_(kflat[int(ids_h[j])], non_blocking=True)
+            staging[j, 1].copy_(vflat[int(ids_h[j])], non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        res["per_block_memcpy_out_gbs"] = round(2 * block_bytes * m / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+        print(json.dumps({"measure": "block swap, pools <-> pinned host memory", "block_size_tokens": bs,
+                          "block_bytes_per_cache": block_bytes, "blocks": int(n), "bytes_per_direction": total,
+                          **res}), flush=True)
+        del kc, vc, staging
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,6 +536,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--partition-size", type=int, default=-1)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling only)")
+    ap.add_argument("--swap", action="store_true", help="measure block swap bandwidth instead")
+    ap.add_argument("--fused", type=int, default=0, help="1: append fused into the decode launch")
     ap.add_argument("--kernel-path", type=int, default=0,
                     help="decode kernel: 0 library choice, 1 CUDA-core, 2/3 tensor-core (1 or 2 CTAs per SM)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -487,7 +548,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.swap:
+        run_swap(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_native(args)

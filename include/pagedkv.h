@@ -137,6 +137,32 @@ int paged_attention_decode(const void* q, const void* k_cache, const void* v_cac
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * paged_attention_decode_append -- paged_kv_append of one new token per
+ * sequence fused into paged_attention_decode, in one launch: the composition
+ * of the append (Ultralytics glossary "PagedAttention", section "How paging
+ * works": each new key goes to its slot) and the attention kernel that reads
+ * the keys back block by block.
+ *  k_new, v_new  [num_seqs][num_kv_heads][head_dim] of act_dtype (device):
+ *                the K/V of each sequence's newest token.
+ *  slot_mapping  int64 [num_seqs] (device): the slot of that token, which
+ *                must be position context_lens[b] - 1 of sequence b (the
+ *                slot the block manager returns for it); < 0: sequence b has
+ *                no new token this step.
+ * Everything else as paged_attention_decode: context_lens count the new
+ * token.  Result and cache contents are those of paged_kv_append followed by
+ * paged_attention_decode; the new token's row is written by the CTA whose
+ * partition ends the context, before that CTA's TMA reads of its block.
+ */
+int paged_attention_decode_append(const void* q, const void* k_new, const void* v_new,
+                                  const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int block_size, int head_dim, int num_blocks,
+                                  float scale, void* out, int act_dtype, int cache_dtype,
+                                  const float* k_scale, const float* v_scale, int partition_size,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pkv_workspace_size -- bytes of workspace paged_attention_decode needs for
  * these sizes and partition_size: a 256-byte header (the work counter of the
  * tensor-core kernel's dynamic scheduling) and, when more than one partition

@@ -34,7 +34,8 @@ DEV_BAD_BLOCK, DEV_BAD_CONTEXT_LEN, DEV_BAD_SLOT, DEV_BAD_PAIR, DEV_WAIT_TIMEOUT
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR, PATH_TENSOR_2CTA = 0, 1, 2, 3
 SWAP_OUT, SWAP_IN = 0, 1
 
-__all__ = ["paged_kv_append", "paged_attention_decode", "paged_block_copy", "paged_block_swap", "workspace_size",
+__all__ = ["paged_kv_append", "paged_attention_decode", "paged_attention_decode_append", "paged_block_copy",
+           "paged_block_swap", "workspace_size",
            "resolve_partition_size", "device_error", "set_kernel_path", "BlockManager", "OutOfBlocks", "PagedKVError",
            "F16", "BF16", "E4M3", "PARTITION_SINGLE", "PARTITION_AUTO", "load"]
 
@@ -154,6 +155,37 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
     _native.call("paged_attention_decode", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks,
                  _ptr(context_lens), B, Hq, Hkv, bs, D, NB, float(scale), _ptr(out), _code(q), _code(k_cache),
                  _ptr(k_scale), _ptr(v_scale), int(partition_size), _ptr(workspace), ws_bytes, s)
+    return out
+
+
+def paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, context_lens, scale,
+                                  out=None, k_scale=None, v_scale=None, partition_size=PARTITION_AUTO, workspace=None,
+                                  stream=None):
+    """Append each sequence's new K/V row (k_new, v_new [B, Hkv, D] at slot_mapping int64 [B]) and decode, in one
+    launch; context_lens count the new token.  Returns out [B, Hq, D]."""
+    B, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("paged_attention_decode_append: shape mismatch")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.shape != (B,):
+        raise ValueError("paged_attention_decode_append: slot_mapping must be int64 [num_seqs]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("paged_attention_decode_append: block_tables and context_lens must be int32")
+    if out is None:
+        out = torch.empty_like(q)
+    _require_cuda(q.device, q=q, k_new=k_new, v_new=v_new, slot_mapping=slot_mapping, k_cache=k_cache,
+                  v_cache=v_cache, block_tables=block_tables, context_lens=context_lens, out=out, k_scale=k_scale,
+                  v_scale=v_scale, workspace=workspace)
+    max_blocks = block_tables.shape[1]
+    s = _stream(stream, q.device)
+    need = workspace_size(B, Hq, Hkv, D, max_blocks, bs, partition_size)
+    if need and workspace is None:
+        workspace = _workspace(q.device, s.value or 0, need)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _native.call("paged_attention_decode_append", _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                 _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), B, Hq, Hkv, bs, D,
+                 NB, float(scale), _ptr(out), _code(q), _code(k_cache), _ptr(k_scale), _ptr(v_scale),
+                 int(partition_size), _ptr(workspace), ws_bytes, s)
     return out
 
 

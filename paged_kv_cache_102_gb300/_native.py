@@ -26,6 +26,8 @@ SIGNATURES = {
     "paged_kv_append": (I32, [P, P, P, I32, P, P, I32, I32, I32, I32, I32, I32, P, P, P]),
     "paged_attention_decode": (I32, [P, P, P, P, I32, P, I32, I32, I32, I32, I32, I32, F32, P, I32, I32, P, P,
                                      I32, P, SZ, P]),
+    "paged_attention_decode_append": (I32, [P, P, P, P, P, P, P, I32, P, I32, I32, I32, I32, I32, I32, F32, P,
+                                            I32, I32, P, P, I32, P, SZ, P]),
     "paged_attention_decode_noalloc": (I32, [P, P, P, P, I32, P, I32, I32, I32, I32, I32, I32, F32, P, I32, I32,
                                              P, P, I32, P]),
     "pkv_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32, I32]),

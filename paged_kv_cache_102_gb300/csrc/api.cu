@@ -190,51 +190,55 @@ int paged_block_swap(void* k_cache, void* v_cache, const int32_t* block_ids, int
     return PKV_OK;
 }
 
-int paged_attention_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                           int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
-                           int num_kv_heads, int block_size, int head_dim, int num_blocks, float scale, void* out,
-                           int act_dtype, int cache_dtype, const float* k_scale, const float* v_scale,
-                           int partition_size, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+static int decode_impl(const char* fn, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                       int num_q_heads, int num_kv_heads, int block_size, int head_dim, int num_blocks, float scale,
+                       void* out, int act_dtype, int cache_dtype, const float* k_scale, const float* v_scale,
+                       int partition_size, void* workspace, size_t workspace_bytes, void* stream, const void* k_new,
+                       const void* v_new, const int64_t* new_slots) {
+    const std::string F(fn);
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: sizes must be positive");
+        return fail(PKV_ERR_INVALID, F + ": " + "sizes must be positive");
     if (num_q_heads % num_kv_heads != 0)
-        return fail(PKV_ERR_SHAPE, "paged_attention_decode: num_q_heads must be a multiple of num_kv_heads");
+        return fail(PKV_ERR_SHAPE, F + ": " + "num_q_heads must be a multiple of num_kv_heads");
     const int G = num_q_heads / num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: query heads per kv head must be 1, 2, 4 or 8");
+        return fail(PKV_ERR_INVALID, F + ": " + "query heads per kv head must be 1, 2, 4 or 8");
     if (head_dim != 64 && head_dim != 128)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: head_dim must be 64 or 128");
+        return fail(PKV_ERR_INVALID, F + ": " + "head_dim must be 64 or 128");
     if (block_size != 16 && block_size != 32)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: block_size must be 16 or 32");
+        return fail(PKV_ERR_INVALID, F + ": " + "block_size must be 16 or 32");
     if (act_dtype != PKV_F16 && act_dtype != PKV_BF16)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: act_dtype must be PKV_F16 or PKV_BF16");
+        return fail(PKV_ERR_INVALID, F + ": " + "act_dtype must be PKV_F16 or PKV_BF16");
     if (cache_dtype != act_dtype && cache_dtype != PKV_E4M3)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: cache_dtype must equal act_dtype or be PKV_E4M3");
-    if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID, "paged_attention_decode: scale must be finite");
+        return fail(PKV_ERR_INVALID, F + ": " + "cache_dtype must equal act_dtype or be PKV_E4M3");
+    if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID, F + ": " + "scale must be finite");
     if (num_seqs == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: null pointer");
+        return fail(PKV_ERR_INVALID, F + ": " + "null pointer");
     if (cache_dtype == PKV_E4M3 && (!k_scale || !v_scale))
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: an E4M3 cache needs k_scale and v_scale");
+        return fail(PKV_ERR_INVALID, F + ": " + "an E4M3 cache needs k_scale and v_scale");
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(workspace, 16))
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: q, caches, out, workspace must be 16-byte aligned");
+        return fail(PKV_ERR_INVALID, F + ": " + "q, caches, out, workspace must be 16-byte aligned");
     const int P = pkv_resolve_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                              block_size, partition_size);
     if (P <= 0)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: partition_size must be 0, -1 or a positive multiple of 32 and of block_size");
+        return fail(PKV_ERR_INVALID, F + ": " + "partition_size must be 0, -1 or a positive multiple of 32 and of block_size");
     const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
-    if (max_ctx > 0x7fffffffLL) return fail(PKV_ERR_INVALID, "paged_attention_decode: table too long");
+    if (max_ctx > 0x7fffffffLL) return fail(PKV_ERR_INVALID, F + ": " + "table too long");
     const int max_parts = static_cast<int>((max_ctx + P - 1) / P);
     if (max_parts > 65535 || num_kv_heads > 65535 || num_seqs > 65535)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: grid too large (partitions, kv heads or sequences > 65535)");
+        return fail(PKV_ERR_INVALID, F + ": " + "grid too large (partitions, kv heads or sequences > 65535)");
     const size_t need = pkv_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                            block_size, partition_size);
     if (!workspace || workspace_bytes < need)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: workspace of " + std::to_string(need) +
+        return fail(PKV_ERR_INVALID, F + ": " + "workspace of " + std::to_string(need) +
                                          " bytes required (pkv_workspace_size)");
     int* err = device_error_word();
-    if (!err) return fail(PKV_ERR_CUDA, "paged_attention_decode: cannot resolve the device error word");
+    if (!err) return fail(PKV_ERR_CUDA, F + ": " + "cannot resolve the device error word");
 
     DecodeParams p{};
     p.q = q;
@@ -260,13 +264,16 @@ int paged_attention_decode(const void* q, const void* k_cache, const void* v_cac
     p.partition_size = P;
     p.max_parts = max_parts;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.new_slots = new_slots;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     const int path = g_kernel_path.load();
     const bool tc_ok = decode_tc_supported(num_seqs, head_dim, block_size, G, act_dtype, cache_dtype, P);
     if ((path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA) && !tc_ok)
-        return fail(PKV_ERR_INVALID, "paged_attention_decode: the tensor-core path needs head_dim 128, a 16-bit "
+        return fail(PKV_ERR_INVALID, F + ": " + "the tensor-core path needs head_dim 128, a 16-bit "
                                      "cache, 2/4/8 query heads per kv head and partitions of at most 512 tokens");
     const bool use_tc = path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA ||
                         (path == PKV_PATH_AUTO && tc_ok && G >= 4);
@@ -278,14 +285,43 @@ int paged_attention_decode(const void* q, const void* k_cache, const void* v_cac
     else
         e = cache_dtype == PKV_E4M3 ? launch_decode_bf16_e4m3(p, head_dim, block_size, G, s)
                                     : launch_decode_bf16_bf16(p, head_dim, block_size, G, s);
-    if (e != cudaSuccess) return cuda_fail("paged_attention_decode: partition kernel launch", e);
+    if (e != cudaSuccess) return cuda_fail((F + ": partition kernel launch").c_str(), e);
     if (max_parts > 1) {
         MergeParams m{context_lens, p.ws_ml, p.ws_o, out, num_q_heads, head_dim, P, max_parts,
                       static_cast<int>(max_ctx)};
         e = launch_merge(m, act_dtype, num_seqs, s);
-        if (e != cudaSuccess) return cuda_fail("paged_attention_decode: merge kernel launch", e);
+        if (e != cudaSuccess) return cuda_fail((F + ": merge kernel launch").c_str(), e);
     }
     return PKV_OK;
+}
+
+extern "C" {
+
+int paged_attention_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int block_size, int head_dim, int num_blocks, float scale, void* out,
+                           int act_dtype, int cache_dtype, const float* k_scale, const float* v_scale,
+                           int partition_size, void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_impl("paged_attention_decode", q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       num_seqs, num_q_heads, num_kv_heads, block_size, head_dim, num_blocks, scale, out, act_dtype,
+                       cache_dtype, k_scale, v_scale, partition_size, workspace, workspace_bytes, stream, nullptr,
+                       nullptr, nullptr);
+}
+
+int paged_attention_decode_append(const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                  void* k_cache, void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                                  int block_size, int head_dim, int num_blocks, float scale, void* out, int act_dtype,
+                                  int cache_dtype, const float* k_scale, const float* v_scale, int partition_size,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping))
+        return fail(PKV_ERR_INVALID, "paged_attention_decode_append: null pointer");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8))
+        return fail(PKV_ERR_INVALID, "paged_attention_decode_append: k_new, v_new must be 16-byte aligned");
+    return decode_impl("paged_attention_decode_append", q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_q_heads, num_kv_heads, block_size, head_dim, num_blocks, scale, out,
+                       act_dtype, cache_dtype, k_scale, v_scale, partition_size, workspace, workspace_bytes, stream,
+                       k_new, v_new, slot_mapping);
 }
 
 }  // extern "C"

@@ -103,6 +103,13 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
         // ------------------------------ producer ------------------------------
         const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks_per_seq + blk_begin;
         const uint64_t policy = l2_policy_evict_first();
+        if (p.new_slots != nullptr && tok_end == L) {
+            // fused append: this CTA's partition holds the new (last) token; write it
+            // before any TMA read of its block
+            append_row_warp<ACT, CACHE>(p.k_new, p.v_new, p.new_slots[seq], seq, kvh, p.num_kv_heads, BS, D,
+                                        p.num_blocks, const_cast<void*>(p.k_cache), const_cast<void*>(p.v_cache),
+                                        p.k_scale, p.v_scale, p.err, lane);
+        }
         const unsigned char* kc = static_cast<const unsigned char*>(p.k_cache);
         const unsigned char* vc = static_cast<const unsigned char*>(p.v_cache);
         bool ok = true;

@@ -318,6 +318,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         auto issue_q_and_k = [&](const TcItem& it, int phys, int k) {
             bool good = true;
+            if (p.new_slots != nullptr && it.tok_begin + it.n_tok == s_lens[it.seq]) {
+                // fused append: this item holds the new (last) token; write it before
+                // the TMA reads of its block
+                append_row_warp<ACT, ACT>(p.k_new, p.v_new, p.new_slots[it.seq], it.seq, it.kvh, p.num_kv_heads,
+                                          BS, kTcD, p.num_blocks, const_cast<void*>(p.k_cache),
+                                          const_cast<void*>(p.v_cache), nullptr, nullptr, p.err, lane);
+            }
             if (lane == 0) {
                 const int b = k & 1;
                 if (k >= 2) good = tc_wait(&q_empty[b], ((k >> 1) - 1) & 1, abort_flag, p.err);

@@ -55,6 +55,11 @@ struct DecodeParams {
     float* ws_ml;  // [num_seqs][num_q_heads][max_parts][2]: (max in log2 units, sum)
     float* ws_o;   // [num_seqs][num_q_heads][max_parts][head_dim]: normalised partial outputs
     int* work_counter;  // workspace header: next item to claim (tensor-core path), zero at launch
+    // fused append (optional): new K/V row of each sequence ([num_seqs][Hkv][D], act dtype) and its
+    // slot; the row is the sequence's last context token
+    const void* k_new;
+    const void* v_new;
+    const int64_t* new_slots;
     const float* k_scale;
     const float* v_scale;
     int* err;

@@ -166,4 +166,46 @@ __device__ __forceinline__ uint16_t float_to_act<kF16>(float x) {
     return __half_as_ushort(__float2half_rn(x));
 }
 
+// Fused append: one warp writes row (seq, kvh) of the new K and V into slot
+// `slot` of the caches (16-bit copy, or E4M3 codes of x / scale), then fences
+// the generic-proxy writes against later TMA (async-proxy) reads of the same
+// block issued by this warp.  A slot outside the pool is skipped and flagged
+// (kErrBadSlot); a negative slot means no new token.
+template <int ACT, int CACHE>
+__device__ __forceinline__ void append_row_warp(const void* k_new, const void* v_new, int64_t slot, int seq, int kvh,
+                                                int num_kv_heads, int block_size, int head_dim, int num_blocks,
+                                                void* k_cache, void* v_cache, const float* k_scale,
+                                                const float* v_scale, int* err, int lane) {
+    if (slot < 0) return;
+    if (slot >= static_cast<int64_t>(num_blocks) * block_size) {
+        if (lane == 0) atomicOr(err, kErrBadSlot);
+        return;
+    }
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    const int64_t dst = ((blk * num_kv_heads + kvh) * block_size + off) * head_dim;
+    const int64_t src = (static_cast<int64_t>(seq) * num_kv_heads + kvh) * head_dim;
+    for (int c = lane; c < head_dim / 8; c += 32) {
+        const uint4 kin = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(k_new) + src + c * 8);
+        const uint4 vin = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(v_new) + src + c * 8);
+        if (CACHE == ACT) {
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(k_cache) + dst + c * 8) = kin;
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(v_cache) + dst + c * 8) = vin;
+        } else {
+            const float ks = *k_scale, vs = *v_scale;
+            const uint16_t* ke = reinterpret_cast<const uint16_t*>(&kin);
+            const uint16_t* ve = reinterpret_cast<const uint16_t*>(&vin);
+            uint8_t kq[8], vq[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                kq[j] = __nv_cvt_float_to_fp8(__fdiv_rn(act_to_float<ACT>(ke[j]), ks), __NV_SATFINITE, __NV_E4M3);
+                vq[j] = __nv_cvt_float_to_fp8(__fdiv_rn(act_to_float<ACT>(ve[j]), vs), __NV_SATFINITE, __NV_E4M3);
+            }
+            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(k_cache) + dst + c * 8) = *reinterpret_cast<const uint2*>(kq);
+            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(v_cache) + dst + c * 8) = *reinterpret_cast<const uint2*>(vq);
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+}
+
 }  // namespace pkv
