@@ -278,7 +278,8 @@ def run_native(args):
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
     peak, peak_src = _peaks()
     dec_avg_ms = statistics.mean(dec_ms)
-    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
+    kernel_bytes = dec_bytes + (app_bytes if args.fused else 0)  # the fused launch also does the append
+    achieved = kernel_bytes / (dec_avg_ms * 1e-3) / 1e9
     traffic = _traffic(args.workload)
 
     # end to end through the public API: pinned host inputs -> device, step, output -> host
@@ -362,11 +363,13 @@ def run_native(args):
         "pct_of_peak": round(100 * value / peak, 2),
         "seq_steps_per_s": round(B * world / (ms_step * 1e-3), 1),
         "bytes_per_step": {"decode": dec_bytes, "append": app_bytes},
-        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (partition + merge kernels)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("paged_attention_decode_append" if args.fused else "paged_attention_decode")
+                               + " (partition + merge kernels)",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "avg_launch_us": round(dec_avg_ms * 1e3, 3),
-                     "algorithmic_bytes_per_launch": dec_bytes},
+                     "algorithmic_bytes_per_launch": kernel_bytes},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
@@ -537,7 +540,7 @@ def main():
     ap.add_argument("--partition-size", type=int, default=-1)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling only)")
     ap.add_argument("--swap", action="store_true", help="measure block swap bandwidth instead")
-    ap.add_argument("--fused", type=int, default=0, help="1: append fused into the decode launch")
+    ap.add_argument("--fused", type=int, default=1, help="1: append fused into the decode launch (default), 0: two launches")
     ap.add_argument("--kernel-path", type=int, default=0,
                     help="decode kernel: 0 library choice, 1 CUDA-core, 2/3 tensor-core (1 or 2 CTAs per SM)")
     ap.add_argument("--no-e2e", action="store_true")
