@@ -60,6 +60,12 @@ def _load():
             lib.oracle_decode_array.restype = None
             lib.oracle_e4m3_encode_array.argtypes = [P, sz, P]
             lib.oracle_e4m3_encode_array.restype = None
+            lib.oracle_quest_select.argtypes = [P, i32, P, i32, f64, P, i32, P, i32, i32, i32, i32, i32, i32, i32,
+                                                P, P, P]
+            lib.oracle_quest_select.restype = i32
+            lib.oracle_sparse_decode.argtypes = [P, i32, P, P, i32, f64, f64, P, i32, P, i32, i32, i32, i32, i32,
+                                                 i32, f64, P]
+            lib.oracle_sparse_decode.restype = i32
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
             del i64
@@ -151,6 +157,45 @@ def block_copy(k_cache, v_cache, src_dst_pairs):
     rc = _load().oracle_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0], NB, block_bytes)
     if rc != 0:
         raise ValueError("oracle_block_copy: block id outside the pool")
+
+
+def quest_select(q, q_dtype, k_cache, cache_dtype, block_tables, context_lens, budget_blocks, k_scale=1.0):
+    """QUEST top-K block selection per (sequence, kv head) (see oracle.c).
+    Returns (sel_tables int32 [B, Hkv, budget], sel_lens int32 [B, Hkv],
+    bounds float64 [B, Hkv, max_blocks])."""
+    q = _bits(q, q_dtype)
+    k_cache = _bits(k_cache, cache_dtype)
+    block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    context_lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    sel = np.zeros((B, Hkv, budget_blocks), np.int32)
+    lens = np.zeros((B, Hkv), np.int32)
+    bounds = np.full((B, Hkv, block_tables.shape[1]), np.nan)
+    rc = _load().oracle_quest_select(_ptr(q), q_dtype, _ptr(k_cache), cache_dtype, float(k_scale),
+                                     _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, bs,
+                                     D, NB, int(budget_blocks), _ptr(sel), _ptr(lens), _ptr(bounds))
+    if rc != 0:
+        raise ValueError(f"oracle_quest_select rejected its arguments (rc={rc})")
+    return sel, lens, bounds
+
+
+def sparse_decode(q, q_dtype, k_cache, v_cache, cache_dtype, tables, lens, scale, k_scale=1.0, v_scale=1.0):
+    """Attention over per-(sequence, kv head) block lists: tables [B, Hkv, max_blocks], lens [B, Hkv]."""
+    q = _bits(q, q_dtype)
+    k_cache = _bits(k_cache, cache_dtype)
+    v_cache = _bits(v_cache, cache_dtype)
+    tables = np.ascontiguousarray(tables, dtype=np.int32)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    out = np.empty((B, Hq, D), np.float64)
+    rc = _load().oracle_sparse_decode(_ptr(q), q_dtype, _ptr(k_cache), _ptr(v_cache), cache_dtype, float(k_scale),
+                                      float(v_scale), _ptr(tables), tables.shape[2], _ptr(lens), B, Hq, Hkv, bs, D,
+                                      NB, float(scale), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_sparse_decode rejected its arguments (rc={rc})")
+    return out
 
 
 def slot_of(block_table, pos: int, block_size: int) -> int:

@@ -288,3 +288,145 @@ void oracle_decode_array(const void* src, int dtype, size_t n, double* out) {
 void oracle_e4m3_encode_array(const float* x, size_t n, uint8_t* out) {
     for (size_t i = 0; i < n; ++i) out[i] = oracle_e4m3_from_float(x[i]);
 }
+
+/*
+ * QUEST query-aware block selection (Tencent Cloud "LLMs serving challenges",
+ * section "Query-sparsity attention / QUEST"):
+ *  1. for every block, the channel-wise minimum and maximum of its keys;
+ *  2. for the query, an upper bound of q.k over the block's keys:
+ *     U = sum_c max(q_c * min_c, q_c * max_c)  (a negative q_c pairs with the
+ *     minimum, a positive one with the maximum);
+ *  3. keep the K blocks with the largest bounds and attend only to them.
+ * Readings: the keys are the stored (dequantised) cache values of the block's
+ * filled slots; for grouped heads one selection serves the kv head, ranked by
+ * the largest bound over its query heads; ties go to the lower logical block;
+ * no block is forced in; with K >= the number of blocks every block is kept.
+ * Output, per (sequence, kv head): the selected physical blocks in logical
+ * order (sel_tables [B][Hkv][budget_blocks]) and their token count (sel_lens
+ * [B][Hkv]: full blocks plus the filled part of the sequence's last block if
+ * selected).  bounds [B][Hkv][max_blocks] (may be NULL) receives U.
+ */
+int oracle_quest_select(const void* q, int q_dtype, const void* k_cache, int cache_dtype, double k_scale,
+                        const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                        int B, int Hq, int Hkv, int bs, int D, int num_blocks, int budget_blocks,
+                        int32_t* sel_tables, int32_t* sel_lens, double* bounds) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || budget_blocks < 1) return -1;
+    int G = Hq / Hkv;
+    double kmul = cache_dtype == ORC_E4M3 ? k_scale : 1.0;
+    for (int b = 0; b < B; ++b) {
+        int L = context_lens[b];
+        if (L < 1 || L > max_blocks_per_seq * bs) return -1;
+        int nblk = (L + bs - 1) / bs;
+        const int32_t* table = block_tables + (size_t)b * max_blocks_per_seq;
+        for (int j = 0; j < nblk; ++j)
+            if (table[j] < 0 || table[j] >= num_blocks) return -1;
+        for (int kvh = 0; kvh < Hkv; ++kvh) {
+            double* U = (double*)malloc(sizeof(double) * (size_t)nblk);
+            char* taken = (char*)calloc((size_t)nblk, 1);
+            double* mn = (double*)malloc(sizeof(double) * (size_t)D);
+            double* mx = (double*)malloc(sizeof(double) * (size_t)D);
+            if (!U || !taken || !mn || !mx) {
+                free(U); free(taken); free(mn); free(mx);
+                return -2;
+            }
+            for (int j = 0; j < nblk; ++j) {
+                int filled = (j == nblk - 1) ? L - j * bs : bs;
+                for (int d = 0; d < D; ++d) {
+                    mn[d] = INFINITY;
+                    mx[d] = -INFINITY;
+                }
+                for (int t = 0; t < filled; ++t) {
+                    size_t row = (((size_t)table[j] * Hkv + kvh) * bs + t) * D;
+                    for (int d = 0; d < D; ++d) {
+                        double x = load_elem(k_cache, cache_dtype, row + d) * kmul;
+                        if (x < mn[d]) mn[d] = x;
+                        if (x > mx[d]) mx[d] = x;
+                    }
+                }
+                double best = -INFINITY;
+                for (int g = 0; g < G; ++g) {
+                    double u = 0.0;
+                    for (int d = 0; d < D; ++d) {
+                        double qd = load_elem(q, q_dtype, ((size_t)b * Hq + kvh * G + g) * D + d);
+                        double a = qd * mn[d], c = qd * mx[d];
+                        u += a > c ? a : c;
+                    }
+                    if (u > best) best = u;
+                }
+                U[j] = best;
+                if (bounds) bounds[((size_t)b * Hkv + kvh) * max_blocks_per_seq + j] = best;
+            }
+            int keep = nblk < budget_blocks ? nblk : budget_blocks;
+            for (int r = 0; r < keep; ++r) {  /* repeated arg-max; the first maximum wins ties */
+                int arg = -1;
+                for (int j = 0; j < nblk; ++j)
+                    if (!taken[j] && (arg < 0 || U[j] > U[arg])) arg = j;
+                taken[arg] = 1;
+            }
+            int32_t* out_row = sel_tables + ((size_t)b * Hkv + kvh) * budget_blocks;
+            int n = 0, tokens = 0;
+            for (int j = 0; j < nblk; ++j) {
+                if (!taken[j]) continue;
+                out_row[n++] = table[j];
+                tokens += (j == nblk - 1) ? L - j * bs : bs;
+            }
+            for (int i = n; i < budget_blocks; ++i) out_row[i] = 0;
+            sel_lens[(size_t)b * Hkv + kvh] = tokens;
+            free(U); free(taken); free(mn); free(mx);
+        }
+    }
+    return 0;
+}
+
+/*
+ * Attention over per-(sequence, kv head) block lists: the same definition as
+ * oracle_paged_decode, with the keys and values of kv head kvh of sequence b
+ * gathered through tables[b][kvh][.] over lens[b][kvh] tokens.
+ */
+int oracle_sparse_decode(const void* q, int q_dtype, const void* k_cache, const void* v_cache, int cache_dtype,
+                         double k_scale, double v_scale, const int32_t* tables, int max_blocks, const int32_t* lens,
+                         int B, int Hq, int Hkv, int bs, int D, int num_blocks, double scale, double* out) {
+    if (Hkv <= 0 || Hq % Hkv != 0) return -1;
+    int G = Hq / Hkv;
+    double kmul = cache_dtype == ORC_E4M3 ? k_scale : 1.0;
+    double vmul = cache_dtype == ORC_E4M3 ? v_scale : 1.0;
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < Hq; ++h) {
+            int kvh = h / G;
+            int L = lens[(size_t)b * Hkv + kvh];
+            const int32_t* table = tables + ((size_t)b * Hkv + kvh) * max_blocks;
+            if (L < 1 || L > max_blocks * bs) return -1;
+            double* s = (double*)malloc(sizeof(double) * (size_t)L);
+            if (!s) return -2;
+            double m = -INFINITY;
+            for (int j = 0; j < L; ++j) {
+                int blk = table[j / bs];
+                if (blk < 0 || blk >= num_blocks) {
+                    free(s);
+                    return -1;
+                }
+                size_t row = (((size_t)blk * Hkv + kvh) * bs + (j % bs)) * D;
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d)
+                    dot += load_elem(q, q_dtype, ((size_t)b * Hq + h) * D + d) *
+                           (load_elem(k_cache, cache_dtype, row + d) * kmul);
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            double z = 0.0;
+            for (int j = 0; j < L; ++j) {
+                s[j] = exp(s[j] - m);
+                z += s[j];
+            }
+            double* o = out + ((size_t)b * Hq + h) * D;
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            for (int j = 0; j < L; ++j) {
+                size_t row = (((size_t)table[j / bs] * Hkv + kvh) * bs + (j % bs)) * D;
+                double p = s[j] / z;
+                for (int d = 0; d < D; ++d) o[d] += p * (load_elem(v_cache, cache_dtype, row + d) * vmul);
+            }
+            free(s);
+        }
+    }
+    return 0;
+}
