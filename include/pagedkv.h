@@ -289,6 +289,56 @@ int paged_block_swap(void* k_cache, void* v_cache, const int32_t* block_ids, int
                      int num_blocks, size_t block_bytes, void* staging, int direction,
                      void* stream);
 
+/* ------------------------------------------------------------------------
+ * QUEST query-aware block selection (Tencent Cloud "LLMs serving
+ * challenges", section "Query-sparsity attention / QUEST"): per block the
+ * channel-wise minimum and maximum key; for a query the upper bound
+ * U = sum_c max(q_c * min_c, q_c * max_c) of q.k over the block's keys;
+ * attention reads only the K blocks with the largest bounds.
+ * kmeta: [num_blocks][num_kv_heads][2][head_dim] of the cache's 16-bit type
+ * (min row, then max row, over the block's filled slots).  16-bit caches only.
+ * ---------------------------------------------------------------------- */
+
+/* Recompute kmeta for every block the given sequences use (their filled
+ * slots).  Shared blocks get the same values from each sharer. */
+int quest_block_minmax(const void* k_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int num_seqs, int num_kv_heads, int block_size,
+                       int head_dim, int num_blocks, int cache_dtype, void* kmeta, void* stream);
+
+/* Update kmeta with newly appended keys k_new [num_tokens][num_kv_heads][head_dim]
+ * at slot_mapping (as given to paged_kv_append): a token at offset 0 of its
+ * block starts the block's metadata, later offsets widen it.  At most one
+ * token per block per call (one decode step); slots < 0 are skipped.
+ * Copy-on-write copies do not carry metadata: recompute it for the copies. */
+int quest_append_minmax(const void* k_new, const int64_t* slot_mapping, int num_tokens,
+                        int num_kv_heads, int block_size, int head_dim, int num_blocks,
+                        int cache_dtype, void* kmeta, void* stream);
+
+/* Select, per (sequence, kv head), the budget_blocks blocks with the largest
+ * bounds (the bound of a kv head is the largest over its query heads; equal
+ * bounds prefer the lower logical block), in logical order:
+ * sel_tables int32 [num_seqs][num_kv_heads][budget_blocks] (unused entries 0)
+ * and sel_lens int32 [num_seqs][num_kv_heads] (their token count; the
+ * sequence's last block counts its filled slots).  A sequence with at most
+ * budget_blocks blocks keeps them all.  Bounds are computed in float32.
+ * head_dim 64 or 128; group 1, 2, 4 or 8; at most 16384 blocks per sequence. */
+int quest_select(const void* q, const void* kmeta, const int32_t* block_tables,
+                 int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
+                 int num_kv_heads, int block_size, int head_dim, int num_blocks, int act_dtype,
+                 int budget_blocks, int32_t* sel_tables, int32_t* sel_lens, void* stream);
+
+/* paged_attention_decode over per-(sequence, kv head) block lists, such as
+ * quest_select's: tables [num_seqs][num_kv_heads][max_sel_blocks], lengths
+ * [num_seqs][num_kv_heads].  Runs on the CUDA-core kernel; the workspace is
+ * pkv_workspace_size(..., max_sel_blocks, ...). */
+int paged_attention_decode_sparse(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* sel_tables, int max_sel_blocks,
+                                  const int32_t* sel_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int block_size, int head_dim, int num_blocks,
+                                  float scale, void* out, int act_dtype, int cache_dtype,
+                                  const float* k_scale, const float* v_scale, int partition_size,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char* pkv_last_error(void);
 

@@ -66,6 +66,8 @@ def _load():
             lib.oracle_sparse_decode.argtypes = [P, i32, P, P, i32, f64, f64, P, i32, P, i32, i32, i32, i32, i32,
                                                  i32, f64, P]
             lib.oracle_sparse_decode.restype = i32
+            lib.oracle_quest_block_minmax.argtypes = [P, i32, P, i32, P, i32, i32, i32, i32, i32, P, P]
+            lib.oracle_quest_block_minmax.restype = i32
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
             del i64
@@ -178,6 +180,23 @@ def quest_select(q, q_dtype, k_cache, cache_dtype, block_tables, context_lens, b
     if rc != 0:
         raise ValueError(f"oracle_quest_select rejected its arguments (rc={rc})")
     return sel, lens, bounds
+
+
+def quest_block_minmax(k_cache, cache_dtype, block_tables, context_lens):
+    """Channel-wise min and max of each (sequence, logical block, kv head)'s filled keys:
+    two float64 arrays [B, max_blocks, Hkv, D] (NaN past the context)."""
+    k_cache = _bits(k_cache, cache_dtype)
+    block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    context_lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    NB, Hkv, bs, D = k_cache.shape
+    B, maxb = block_tables.shape
+    mn = np.empty((B, maxb, Hkv, D))
+    mx = np.empty((B, maxb, Hkv, D))
+    rc = _load().oracle_quest_block_minmax(_ptr(k_cache), cache_dtype, _ptr(block_tables), maxb, _ptr(context_lens),
+                                           B, Hkv, bs, D, NB, _ptr(mn), _ptr(mx))
+    if rc != 0:
+        raise ValueError("oracle_quest_block_minmax rejected its arguments")
+    return mn, mx
 
 
 def sparse_decode(q, q_dtype, k_cache, v_cache, cache_dtype, tables, lens, scale, k_scale=1.0, v_scale=1.0):

@@ -430,3 +430,41 @@ int oracle_sparse_decode(const void* q, int q_dtype, const void* k_cache, const 
     }
     return 0;
 }
+
+/* QUEST metadata alone: channel-wise minimum and maximum of the keys of each
+ * (sequence, logical block, kv head) over the block's filled slots, float64
+ * [B][max_blocks][Hkv][D] (entries of blocks past the context are NaN). */
+int oracle_quest_block_minmax(const void* k_cache, int cache_dtype, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* context_lens, int B, int Hkv, int bs, int D,
+                              int num_blocks, double* out_min, double* out_max) {
+    for (int b = 0; b < B; ++b) {
+        int L = context_lens[b];
+        if (L < 1 || L > max_blocks_per_seq * bs) return -1;
+        for (int j = 0; j < max_blocks_per_seq; ++j) {
+            for (int h = 0; h < Hkv; ++h) {
+                double* mn = out_min + (((size_t)b * max_blocks_per_seq + j) * Hkv + h) * D;
+                double* mx = out_max + (((size_t)b * max_blocks_per_seq + j) * Hkv + h) * D;
+                if (j * bs >= L) {
+                    for (int d = 0; d < D; ++d) mn[d] = mx[d] = NAN;
+                    continue;
+                }
+                int blk = block_tables[(size_t)b * max_blocks_per_seq + j];
+                if (blk < 0 || blk >= num_blocks) return -1;
+                int filled = L - j * bs < bs ? L - j * bs : bs;
+                for (int d = 0; d < D; ++d) {
+                    mn[d] = INFINITY;
+                    mx[d] = -INFINITY;
+                }
+                for (int t = 0; t < filled; ++t) {
+                    size_t row = (((size_t)blk * Hkv + h) * bs + t) * D;
+                    for (int d = 0; d < D; ++d) {
+                        double x = load_elem(k_cache, cache_dtype, row + d);
+                        if (x < mn[d]) mn[d] = x;
+                        if (x > mx[d]) mx[d] = x;
+                    }
+                }
+            }
+        }
+    }
+    return 0;
+}

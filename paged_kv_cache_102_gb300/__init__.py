@@ -35,7 +35,8 @@ PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR, PATH_TENSOR_2CTA = 0, 1, 2, 3
 SWAP_OUT, SWAP_IN = 0, 1
 
 __all__ = ["paged_kv_append", "paged_attention_decode", "paged_attention_decode_append", "paged_block_copy",
-           "paged_block_swap", "workspace_size",
+           "paged_block_swap", "paged_attention_decode_sparse", "quest_block_minmax", "quest_append_minmax",
+           "quest_select", "workspace_size",
            "resolve_partition_size", "device_error", "set_kernel_path", "BlockManager", "OutOfBlocks", "PagedKVError",
            "F16", "BF16", "E4M3", "PARTITION_SINGLE", "PARTITION_AUTO", "load"]
 
@@ -186,6 +187,64 @@ def paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cach
                  _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), B, Hq, Hkv, bs, D,
                  NB, float(scale), _ptr(out), _code(q), _code(k_cache), _ptr(k_scale), _ptr(v_scale),
                  int(partition_size), _ptr(workspace), ws_bytes, s)
+    return out
+
+
+def quest_block_minmax(k_cache, block_tables, context_lens, kmeta=None, stream=None):
+    """Per-block channel min/max of the keys (QUEST metadata) for every block the sequences use;
+    returns kmeta [num_blocks, Hkv, 2, D] of the cache type."""
+    NB, Hkv, bs, D = k_cache.shape
+    if kmeta is None:
+        kmeta = torch.zeros(NB, Hkv, 2, D, dtype=k_cache.dtype, device=k_cache.device)
+    _require_cuda(k_cache.device, k_cache=k_cache, block_tables=block_tables, context_lens=context_lens, kmeta=kmeta)
+    _native.call("quest_block_minmax", _ptr(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                 block_tables.shape[0], Hkv, bs, D, NB, _code(k_cache), _ptr(kmeta), _stream(stream, k_cache.device))
+    return kmeta
+
+
+def quest_append_minmax(k_new, slot_mapping, kmeta, block_size, stream=None):
+    """Widen QUEST metadata with newly appended keys k_new [T, Hkv, D] at slot_mapping (int64 [T])."""
+    T, Hkv, D = k_new.shape
+    _require_cuda(k_new.device, k_new=k_new, slot_mapping=slot_mapping, kmeta=kmeta)
+    _native.call("quest_append_minmax", _ptr(k_new), _ptr(slot_mapping), T, Hkv, block_size, D, kmeta.shape[0],
+                 _code(k_new), _ptr(kmeta), _stream(stream, k_new.device))
+
+
+def quest_select(q, kmeta, block_tables, context_lens, block_size, budget_blocks, sel_tables=None, sel_lens=None,
+                 stream=None):
+    """QUEST top-K blocks per (sequence, kv head); returns (sel_tables [B, Hkv, budget], sel_lens [B, Hkv])."""
+    B, Hq, D = q.shape
+    NB, Hkv = kmeta.shape[0], kmeta.shape[1]
+    if sel_tables is None:
+        sel_tables = torch.empty(B, Hkv, budget_blocks, dtype=torch.int32, device=q.device)
+    if sel_lens is None:
+        sel_lens = torch.empty(B, Hkv, dtype=torch.int32, device=q.device)
+    _require_cuda(q.device, q=q, kmeta=kmeta, block_tables=block_tables, context_lens=context_lens,
+                  sel_tables=sel_tables, sel_lens=sel_lens)
+    _native.call("quest_select", _ptr(q), _ptr(kmeta), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                 B, Hq, Hkv, block_size, D, NB, _code(q), int(budget_blocks), _ptr(sel_tables), _ptr(sel_lens),
+                 _stream(stream, q.device))
+    return sel_tables, sel_lens
+
+
+def paged_attention_decode_sparse(q, k_cache, v_cache, sel_tables, sel_lens, scale, out=None, k_scale=None,
+                                  v_scale=None, partition_size=PARTITION_AUTO, workspace=None, stream=None):
+    """Decode over per-(sequence, kv head) block lists sel_tables [B, Hkv, max_sel], sel_lens [B, Hkv]."""
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _require_cuda(q.device, q=q, k_cache=k_cache, v_cache=v_cache, sel_tables=sel_tables, sel_lens=sel_lens,
+                  out=out, k_scale=k_scale, v_scale=v_scale, workspace=workspace)
+    max_sel = sel_tables.shape[2]
+    s = _stream(stream, q.device)
+    need = workspace_size(B, Hq, Hkv, D, max_sel, bs, partition_size)
+    if need and workspace is None:
+        workspace = _workspace(q.device, s.value or 0, need)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _native.call("paged_attention_decode_sparse", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(sel_tables), max_sel,
+                 _ptr(sel_lens), B, Hq, Hkv, bs, D, NB, float(scale), _ptr(out), _code(q), _code(k_cache),
+                 _ptr(k_scale), _ptr(v_scale), int(partition_size), _ptr(workspace), ws_bytes, s)
     return out
 
 

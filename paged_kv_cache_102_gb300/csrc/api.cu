@@ -197,7 +197,7 @@ static int decode_impl(const char* fn, const void* q, const void* k_cache, const
                        int num_q_heads, int num_kv_heads, int block_size, int head_dim, int num_blocks, float scale,
                        void* out, int act_dtype, int cache_dtype, const float* k_scale, const float* v_scale,
                        int partition_size, void* workspace, size_t workspace_bytes, void* stream, const void* k_new,
-                       const void* v_new, const int64_t* new_slots) {
+                       const void* v_new, const int64_t* new_slots, bool per_kvh_tables = false) {
     const std::string F(fn);
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
         return fail(PKV_ERR_INVALID, F + ": " + "sizes must be positive");
@@ -267,11 +267,23 @@ static int decode_impl(const char* fn, const void* q, const void* k_cache, const
     p.k_new = k_new;
     p.v_new = v_new;
     p.new_slots = new_slots;
+    if (per_kvh_tables) {  // tables [B][Hkv][max_blocks], lengths [B][Hkv]
+        p.table_seq_stride = static_cast<int64_t>(num_kv_heads) * max_blocks_per_seq;
+        p.table_kvh_stride = max_blocks_per_seq;
+        p.lens_seq_stride = num_kv_heads;
+        p.lens_kvh_stride = 1;
+    } else {
+        p.table_seq_stride = max_blocks_per_seq;
+        p.table_kvh_stride = 0;
+        p.lens_seq_stride = 1;
+        p.lens_kvh_stride = 0;
+    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     const int path = g_kernel_path.load();
-    const bool tc_ok = decode_tc_supported(num_seqs, head_dim, block_size, G, act_dtype, cache_dtype, P);
+    const bool tc_ok =
+        !per_kvh_tables && decode_tc_supported(num_seqs, head_dim, block_size, G, act_dtype, cache_dtype, P);
     if ((path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA) && !tc_ok)
         return fail(PKV_ERR_INVALID, F + ": " + "the tensor-core path needs head_dim 128, a 16-bit "
                                      "cache, 2/4/8 query heads per kv head and partitions of at most 512 tokens");
@@ -287,8 +299,19 @@ static int decode_impl(const char* fn, const void* q, const void* k_cache, const
                                     : launch_decode_bf16_bf16(p, head_dim, block_size, G, s);
     if (e != cudaSuccess) return cuda_fail((F + ": partition kernel launch").c_str(), e);
     if (max_parts > 1) {
-        MergeParams m{context_lens, p.ws_ml, p.ws_o, out, num_q_heads, head_dim, P, max_parts,
-                      static_cast<int>(max_ctx)};
+        MergeParams m{};
+        m.context_lens = context_lens;
+        m.lens_seq_stride = p.lens_seq_stride;
+        m.lens_kvh_stride = p.lens_kvh_stride;
+        m.group = G;
+        m.ws_ml = p.ws_ml;
+        m.ws_o = p.ws_o;
+        m.out = out;
+        m.num_q_heads = num_q_heads;
+        m.head_dim = head_dim;
+        m.partition_size = P;
+        m.max_parts = max_parts;
+        m.max_context = static_cast<int>(max_ctx);
         e = launch_merge(m, act_dtype, num_seqs, s);
         if (e != cudaSuccess) return cuda_fail((F + ": merge kernel launch").c_str(), e);
     }
@@ -322,6 +345,82 @@ int paged_attention_decode_append(const void* q, const void* k_new, const void* 
                        context_lens, num_seqs, num_q_heads, num_kv_heads, block_size, head_dim, num_blocks, scale, out,
                        act_dtype, cache_dtype, k_scale, v_scale, partition_size, workspace, workspace_bytes, stream,
                        k_new, v_new, slot_mapping);
+}
+
+
+int paged_attention_decode_sparse(const void* q, const void* k_cache, const void* v_cache, const int32_t* sel_tables,
+                                  int max_sel_blocks, const int32_t* sel_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int block_size, int head_dim, int num_blocks, float scale,
+                                  void* out, int act_dtype, int cache_dtype, const float* k_scale,
+                                  const float* v_scale, int partition_size, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    return decode_impl("paged_attention_decode_sparse", q, k_cache, v_cache, sel_tables, max_sel_blocks, sel_lens,
+                       num_seqs, num_q_heads, num_kv_heads, block_size, head_dim, num_blocks, scale, out, act_dtype,
+                       cache_dtype, k_scale, v_scale, partition_size, workspace, workspace_bytes, stream, nullptr,
+                       nullptr, nullptr, true);
+}
+
+int quest_block_minmax(const void* k_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int num_seqs, int num_kv_heads, int block_size, int head_dim,
+                       int num_blocks, int cache_dtype, void* kmeta, void* stream) {
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0 ||
+        head_dim <= 0 || head_dim % 8 != 0)
+        return fail(PKV_ERR_INVALID, "quest_block_minmax: sizes must be positive, head_dim a multiple of 8");
+    if (cache_dtype != PKV_F16 && cache_dtype != PKV_BF16)
+        return fail(PKV_ERR_INVALID, "quest_block_minmax: the cache must be PKV_F16 or PKV_BF16");
+    if (num_seqs == 0) return PKV_OK;
+    if (!k_cache || !block_tables || !context_lens || !kmeta) return fail(PKV_ERR_INVALID, "quest_block_minmax: null pointer");
+    if (!aligned(k_cache, 16) || !aligned(kmeta, 16)) return fail(PKV_ERR_INVALID, "quest_block_minmax: misaligned");
+    int* err = device_error_word();
+    if (!err) return fail(PKV_ERR_CUDA, "quest_block_minmax: cannot resolve the device error word");
+    QuestMetaParams p{k_cache, block_tables, context_lens, kmeta, err, num_seqs, max_blocks_per_seq, num_kv_heads,
+                      block_size, head_dim, num_blocks};
+    cudaError_t e = launch_quest_minmax(p, cache_dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail("quest_block_minmax: launch", e);
+}
+
+int quest_append_minmax(const void* k_new, const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                        int block_size, int head_dim, int num_blocks, int cache_dtype, void* kmeta, void* stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0 || head_dim <= 0 || head_dim % 8 != 0)
+        return fail(PKV_ERR_INVALID, "quest_append_minmax: sizes must be positive, head_dim a multiple of 8");
+    if (cache_dtype != PKV_F16 && cache_dtype != PKV_BF16)
+        return fail(PKV_ERR_INVALID, "quest_append_minmax: the cache must be PKV_F16 or PKV_BF16");
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !slot_mapping || !kmeta) return fail(PKV_ERR_INVALID, "quest_append_minmax: null pointer");
+    if (!aligned(k_new, 16) || !aligned(kmeta, 16) || !aligned(slot_mapping, 8))
+        return fail(PKV_ERR_INVALID, "quest_append_minmax: misaligned");
+    int* err = device_error_word();
+    if (!err) return fail(PKV_ERR_CUDA, "quest_append_minmax: cannot resolve the device error word");
+    QuestAppendParams p{k_new, slot_mapping, kmeta, err, num_tokens, num_kv_heads, block_size, head_dim, num_blocks};
+    cudaError_t e = launch_quest_append_minmax(p, cache_dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail("quest_append_minmax: launch", e);
+}
+
+int quest_select(const void* q, const void* kmeta, const int32_t* block_tables, int max_blocks_per_seq,
+                 const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
+                 int head_dim, int num_blocks, int act_dtype, int budget_blocks, int32_t* sel_tables, int32_t* sel_lens,
+                 void* stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0 || budget_blocks <= 0)
+        return fail(PKV_ERR_INVALID, "quest_select: sizes must be positive, num_q_heads a multiple of num_kv_heads");
+    const int G = num_q_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return fail(PKV_ERR_INVALID, "quest_select: group must be 1, 2, 4 or 8");
+    if (head_dim != 64 && head_dim != 128) return fail(PKV_ERR_INVALID, "quest_select: head_dim must be 64 or 128");
+    if (act_dtype != PKV_F16 && act_dtype != PKV_BF16)
+        return fail(PKV_ERR_INVALID, "quest_select: act_dtype must be PKV_F16 or PKV_BF16");
+    int sort_size = 1;
+    while (sort_size < max_blocks_per_seq) sort_size <<= 1;
+    if (sort_size > 16384) return fail(PKV_ERR_INVALID, "quest_select: at most 16384 blocks per sequence");
+    if (num_seqs == 0) return PKV_OK;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return fail(PKV_ERR_INVALID, "quest_select: grid too large");
+    if (!q || !kmeta || !block_tables || !context_lens || !sel_tables || !sel_lens)
+        return fail(PKV_ERR_INVALID, "quest_select: null pointer");
+    int* err = device_error_word();
+    if (!err) return fail(PKV_ERR_CUDA, "quest_select: cannot resolve the device error word");
+    QuestSelectParams p{q, kmeta, block_tables, context_lens, sel_tables, sel_lens, err, num_seqs, num_q_heads,
+                        num_kv_heads, block_size, head_dim, num_blocks, max_blocks_per_seq, budget_blocks, sort_size};
+    cudaError_t e = launch_quest_select(p, act_dtype, G, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail("quest_select: launch", e);
 }
 
 }  // extern "C"

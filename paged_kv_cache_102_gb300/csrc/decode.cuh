@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const int L = p.context_lens[seq];
+    const int L = p.context_lens[static_cast<int64_t>(seq) * p.lens_seq_stride + kvh * p.lens_kvh_stride];
     if (L < 1 || L > p.max_blocks_per_seq * BS) {
         if (part == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.err, kErrBadLen);
         return;
@@ -101,7 +101,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
-        const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks_per_seq + blk_begin;
+        const int32_t* table =
+            p.block_tables + seq * p.table_seq_stride + kvh * p.table_kvh_stride + blk_begin;
         const uint64_t policy = l2_policy_evict_first();
         if (p.new_slots != nullptr && tok_end == L) {
             // fused append: this CTA's partition holds the new (last) token; write it
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
 
     const float vmul = CACHE == kE4M3 ? *p.v_scale : 1.0f;
     const int tid = threadIdx.x;
-    const bool single = p.max_parts == 1 || L <= p.partition_size;
+    const bool single = p.max_parts == 1 || L <= p.partition_size;  // per (seq, kvh) length
     for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
         const int g = idx / D;
         const int d = idx % D;

@@ -60,6 +60,13 @@ struct DecodeParams {
     const void* k_new;
     const void* v_new;
     const int64_t* new_slots;
+    // table row of (seq, kvh) = block_tables + seq*table_seq_stride + kvh*table_kvh_stride;
+    // its length = context_lens[seq*lens_seq_stride + kvh*lens_kvh_stride]
+    // (per-sequence tables: max_blocks_per_seq, 0, 1, 0)
+    int64_t table_seq_stride;
+    int64_t table_kvh_stride;
+    int lens_seq_stride;
+    int lens_kvh_stride;
     const float* k_scale;
     const float* v_scale;
     int* err;
@@ -75,6 +82,9 @@ struct DecodeParams {
 
 struct MergeParams {
     const int32_t* context_lens;
+    int lens_seq_stride;
+    int lens_kvh_stride;
+    int group;  // query heads per kv head
     const float* ws_ml;
     const float* ws_o;
     void* out;
@@ -84,6 +94,55 @@ struct MergeParams {
     int max_parts;
     int max_context;
 };
+
+struct QuestMetaParams {
+    const void* k_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    void* kmeta;
+    int* err;
+    int num_seqs;
+    int max_blocks_per_seq;
+    int num_kv_heads;
+    int block_size;
+    int head_dim;
+    int num_blocks;
+};
+
+struct QuestAppendParams {
+    const void* k_new;
+    const int64_t* slot_mapping;
+    void* kmeta;
+    int* err;
+    int num_tokens;
+    int num_kv_heads;
+    int block_size;
+    int head_dim;
+    int num_blocks;
+};
+
+struct QuestSelectParams {
+    const void* q;
+    const void* kmeta;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int32_t* sel_tables;
+    int32_t* sel_lens;
+    int* err;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int block_size;
+    int head_dim;
+    int num_blocks;
+    int max_blocks_per_seq;
+    int budget_blocks;
+    int sort_size;  // power of two >= max_blocks_per_seq
+};
+
+cudaError_t launch_quest_minmax(const QuestMetaParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_quest_append_minmax(const QuestAppendParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_quest_select(const QuestSelectParams& p, int dtype, int G, cudaStream_t s);
 
 cudaError_t launch_append(const AppendParams& p, int act, int cache, cudaStream_t stream);
 cudaError_t launch_block_copy(const CopyParams& p, int num_pairs, cudaStream_t stream);

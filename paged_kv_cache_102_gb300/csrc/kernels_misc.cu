@@ -172,7 +172,7 @@ __global__ void paged_decode_merge_kernel(MergeParams p) {
     const int h = blockIdx.x;
     const int seq = blockIdx.y;
     const int d = threadIdx.x;
-    const int L = p.context_lens[seq];
+    const int L = p.context_lens[static_cast<int64_t>(seq) * p.lens_seq_stride + (h / p.group) * p.lens_kvh_stride];
     if (L < 1 || L > p.max_context) return;  // flagged by the partition kernel
     const int n_parts = (L + p.partition_size - 1) / p.partition_size;
     if (n_parts <= 1) return;

@@ -1,0 +1,120 @@
+"""QUEST on the GPU: block min/max metadata (full and incremental) exact
+against the oracle; top-K selection equal to the oracle's where the bounds
+have a margin at the cut and a valid top-K everywhere; sparse decode within
+tolerance of the oracle; a budget covering every block reproduces full
+decode."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.block_manager_ref import RefBlockManager
+from tests.parity import ACT_CODE, TOL, assert_attention_close, bits
+
+pytestmark = pytest.mark.gpu
+DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.fixture
+def pkv(pkv_lib, cuda_device):
+    pkv_lib.device_error(reset=True)
+    prev = pkv_lib.set_kernel_path(pkv_lib.PATH_AUTO)
+    yield pkv_lib
+    pkv_lib.set_kernel_path(prev)
+    assert pkv_lib.device_error(reset=True) == 0
+
+
+def _setup(act, Hq, Hkv, D, bs, ctx, seed):
+    g = torch.Generator().manual_seed(seed)
+    B = len(ctx)
+    NB = sum(-(-(c + 1) // bs) for c in ctx) + 3
+    ref = RefBlockManager(NB, bs, free_list=torch.randperm(NB, generator=g).numpy())
+    for i, c in enumerate(ctx):
+        ref.add_sequence(i, c)
+    slots = np.array([ref.append_slot(i)[0] for i in range(B)], np.int64)
+    maxb = max(len(t) for t in ref.tables.values())
+    tables = np.zeros((B, maxb), np.int32)
+    for i in range(B):
+        tables[i, : len(ref.tables[i])] = ref.tables[i]
+    kc = torch.randn(NB, Hkv, bs, D, generator=g).to(DT[act])
+    vc = torch.randn(NB, Hkv, bs, D, generator=g).to(DT[act])
+    q = torch.randn(B, Hq, D, generator=g).to(DT[act])
+    k_new = torch.randn(B, Hkv, D, generator=g).to(DT[act])
+    v_new = torch.randn(B, Hkv, D, generator=g).to(DT[act])
+    return q, kc, vc, k_new, v_new, tables, slots, np.array([c + 1 for c in ctx], np.int32)
+
+
+CASES = [("bf16", 8, 8, 128, 16), ("f16", 16, 4, 64, 32), ("bf16", 32, 4, 128, 16)]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_quest_metadata_selection_and_sparse_decode(pkv, case):
+    act, Hq, Hkv, D, bs = case
+    ctx = [0, 9, 100, 511, 1500, 3000]
+    q, kc, vc, k_new, v_new, tables, slots, lens = _setup(act, Hq, Hkv, D, bs, ctx, zlib.crc32(repr(case).encode()))
+    dev = torch.device("cuda")
+    dk, dv = kc.to(dev), vc.to(dev)
+    t_d, l_d = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
+    # metadata of the cache before the step, then widened by the step's appended keys
+    l0 = torch.from_numpy(np.maximum(lens - 1, 1)).to(dev)
+    kmeta = pkv.quest_block_minmax(dk, t_d, l0)
+    has_prev = lens > 1  # sequence 0 had no tokens before this step
+    pkv.paged_kv_append(k_new.to(dev), v_new.to(dev), torch.from_numpy(slots).to(dev), dk, dv)
+    pkv.quest_append_minmax(k_new.to(dev), torch.from_numpy(slots).to(dev), kmeta, bs)
+    full = pkv.quest_block_minmax(dk, t_d, l_d)
+    torch.cuda.synchronize()
+    kbits = bits(dk)
+    mn, mx = oracle.quest_block_minmax(kbits, ACT_CODE[DT[act]], tables, lens)
+    meta = kmeta.float().cpu().numpy().astype(np.float64)
+    meta_full = full.float().cpu().numpy().astype(np.float64)
+    for b in range(len(ctx)):
+        for j in range(-(-int(lens[b]) // bs)):
+            blk = tables[b, j]
+            np.testing.assert_array_equal(meta_full[blk, :, 0], mn[b, j])
+            np.testing.assert_array_equal(meta_full[blk, :, 1], mx[b, j])
+            if has_prev[b] or j > 0:
+                np.testing.assert_array_equal(meta[blk], meta_full[blk])  # incremental == recompute
+    for budget in (1, 8, 40):
+        sel, slen = pkv.quest_select(q.to(dev), full, t_d, l_d, bs, budget)
+        torch.cuda.synchronize()
+        sel_h, slen_h = sel.cpu().numpy(), slen.cpu().numpy()
+        want_sel, want_len, bounds = oracle.quest_select(bits(q), ACT_CODE[DT[act]], kbits, ACT_CODE[DT[act]],
+                                                         tables, lens, budget)
+        for b in range(len(ctx)):
+            n = -(-int(lens[b]) // bs)
+            for h in range(Hkv):
+                got = [int(x) for x in sel_h[b, h, : min(budget, n)]]
+                logical = [int(np.where(tables[b, :n] == x)[0][0]) for x in got]
+                assert logical == sorted(logical) and len(set(logical)) == len(logical)
+                toks = sum(int(lens[b]) - j * bs if j == n - 1 else bs for j in logical)
+                assert slen_h[b, h] == toks
+                if n <= budget:
+                    assert logical == list(range(n))
+                    continue
+                u = bounds[b, h, :n]
+                order = np.sort(u)[::-1]
+                cut, nxt = order[budget - 1], order[budget]
+                if cut - nxt > 1e-3 * max(1.0, abs(cut)):
+                    assert got == [int(x) for x in want_sel[b, h, :budget]]
+                else:  # a near tie at the cut: any valid top-K
+                    assert min(u[logical]) >= nxt - 1e-3 * max(1.0, abs(nxt))
+        out = pkv.paged_attention_decode_sparse(q.to(dev), dk, dv, sel, slen, 0.09)
+        torch.cuda.synchronize()
+        want = oracle.sparse_decode(bits(q), ACT_CODE[DT[act]], kbits, bits(dv), ACT_CODE[DT[act]], sel_h, slen_h,
+                                    0.09)
+        assert_attention_close(out, want, TOL[act], rounding_slack=True)
+
+
+def test_full_budget_reproduces_full_decode(pkv):
+    q, kc, vc, _, _, tables, _, lens = _setup("bf16", 8, 8, 128, 16, [50, 700, 2000], 3)
+    dev = torch.device("cuda")
+    dk, dv = kc.to(dev), vc.to(dev)
+    t_d, l_d = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
+    kmeta = pkv.quest_block_minmax(dk, t_d, l_d)
+    sel, slen = pkv.quest_select(q.to(dev), kmeta, t_d, l_d, 16, tables.shape[1])
+    sparse = pkv.paged_attention_decode_sparse(q.to(dev), dk, dv, sel, slen, 0.09)
+    full = pkv.paged_attention_decode(q.to(dev), dk, dv, t_d, l_d, 0.09)
+    torch.cuda.synchronize()
+    assert torch.equal(sparse, full)

@@ -98,3 +98,15 @@ def test_sparse_decode_matches_sdpa_on_selected_tokens(oracle_mod):
             qq = q[b, h * G:(h + 1) * G].double()[:, None]
             want = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, scale=0.2)[:, 0].numpy()
             np.testing.assert_allclose(got[b, h * G:(h + 1) * G], want, rtol=0, atol=1e-12)
+
+
+def test_minmax_matches_hand_example(oracle_mod):
+    g = golden("t7_quest_hand_example.json")
+    bs, D = g["block_size"], g["head_dim"]
+    keys = torch.tensor(g["keys"]).half()
+    kc = torch.zeros(6, 1, bs, D).half()
+    for pos in range(g["context_len"]):
+        kc[g["block_table"][pos // bs], 0, pos % bs] = keys[pos]
+    mn, mx = oracle_mod.quest_block_minmax(_bits(kc), 0, np.array([g["block_table"]], np.int32),
+                                           np.array([g["context_len"]], np.int32))
+    assert mn[0, :, 0].tolist() == g["expected_min"] and mx[0, :, 0].tolist() == g["expected_max"]
