@@ -529,6 +529,72 @@ def run_swap(args):
         del kc, vc, staging
 
 
+def run_quest(args):
+    """QUEST step (append, metadata update, top-K selection, sparse decode) vs full decode."""
+    import paged_kv_cache_102_gb300 as pkv
+    from paged_kv_cache_102_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    pkv.load()
+    st = setup(pkv, W, args.workload, args.seed, dev, args.batch)
+    wl, vals = st["wl"], st["vals"]
+    bs = wl.block_size
+    budget = max(1, args.quest // bs)
+    kc, vc = vals["k_cache"], vals["v_cache"]
+    kmeta = pkv.quest_block_minmax(kc, st["tables"], st["lens"])
+    B = len(st["ids"])
+    sel = torch.empty(B, wl.num_kv_heads, budget, dtype=torch.int32, device=dev)
+    slen = torch.empty(B, wl.num_kv_heads, dtype=torch.int32, device=dev)
+    out = torch.empty_like(vals["q"])
+
+    def quest_step():
+        pkv.paged_kv_append(vals["k_new"], vals["v_new"], st["slots"], kc, vc)
+        pkv.quest_append_minmax(vals["k_new"], st["slots"], kmeta, bs)
+        pkv.quest_select(vals["q"], kmeta, st["tables"], st["lens"], bs, budget, sel, slen)
+        pkv.paged_attention_decode_sparse(vals["q"], kc, vc, sel, slen, wl.scale, out=out)
+
+    def full_step():
+        pkv.paged_attention_decode_append(vals["q"], vals["k_new"], vals["v_new"], st["slots"], kc, vc, st["tables"],
+                                          st["lens"], wl.scale, out=out)
+
+    res = {}
+    phases = {"append": lambda: pkv.paged_kv_append(vals["k_new"], vals["v_new"], st["slots"], kc, vc),
+              "metadata": lambda: pkv.quest_append_minmax(vals["k_new"], st["slots"], kmeta, bs),
+              "select": lambda: pkv.quest_select(vals["q"], kmeta, st["tables"], st["lens"], bs, budget, sel, slen),
+              "sparse_decode": lambda: pkv.paged_attention_decode_sparse(vals["q"], kc, vc, sel, slen, wl.scale,
+                                                                         out=out)}
+    for name, fn in phases.items():
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[f"{name}_us"] = round(e0.elapsed_time(e1) * 1e3 / args.steps, 2)
+    for name, fn in (("full", full_step), ("quest", quest_step)):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[f"{name}_us_per_step"] = round(e0.elapsed_time(e1) * 1e3 / args.steps, 2)
+    e = ELEM[wl.cache_dtype]
+    sel_tokens = int(slen.sum().item())
+    full_tokens = int(st["lens_h"].sum()) * wl.num_kv_heads
+    meta_bytes = sum(-(-int(L) // bs) for L in st["lens_h"]) * wl.num_kv_heads * 2 * wl.head_dim * e
+    print(json.dumps({"measure": "QUEST top-K blocks vs full decode", "workload": wl.name,
+                      "budget_tokens": budget * bs, "selected_kv_tokens": sel_tokens, "full_kv_tokens": full_tokens,
+                      "kv_bytes_full": full_tokens * 2 * wl.head_dim * e,
+                      "kv_bytes_selected": sel_tokens * 2 * wl.head_dim * e, "metadata_bytes": meta_bytes,
+                      **res, "speedup": round(res["full_us_per_step"] / res["quest_us_per_step"], 2)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -540,6 +606,7 @@ def main():
     ap.add_argument("--partition-size", type=int, default=-1)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling only)")
     ap.add_argument("--swap", action="store_true", help="measure block swap bandwidth instead")
+    ap.add_argument("--quest", type=int, default=0, help="measure QUEST with this token budget instead")
     ap.add_argument("--fused", type=int, default=1, help="1: append fused into the decode launch (default), 0: two launches")
     ap.add_argument("--kernel-path", type=int, default=0,
                     help="decode kernel: 0 library choice, 1 CUDA-core, 2/3 tensor-core (1 or 2 CTAs per SM)")
@@ -553,6 +620,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.swap:
         run_swap(args)
+    elif args.quest:
+        run_quest(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

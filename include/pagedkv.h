@@ -329,8 +329,9 @@ int quest_select(const void* q, const void* kmeta, const int32_t* block_tables,
 
 /* paged_attention_decode over per-(sequence, kv head) block lists, such as
  * quest_select's: tables [num_seqs][num_kv_heads][max_sel_blocks], lengths
- * [num_seqs][num_kv_heads].  Runs on the CUDA-core kernel; the workspace is
- * pkv_workspace_size(..., max_sel_blocks, ...). */
+ * [num_seqs][num_kv_heads].  Same kernels as paged_attention_decode (the
+ * tensor-core kernel serves num_seqs * num_kv_heads <= 2048); the workspace
+ * is pkv_workspace_size(..., max_sel_blocks, ...). */
 int paged_attention_decode_sparse(const void* q, const void* k_cache, const void* v_cache,
                                   const int32_t* sel_tables, int max_sel_blocks,
                                   const int32_t* sel_lens, int num_seqs, int num_q_heads,

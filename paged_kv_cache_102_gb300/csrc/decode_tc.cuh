@@ -79,15 +79,23 @@ struct TcSmem {
 };
 
 struct TcItem {
-    int seq, kvh, part, tok_begin, n_tok, n_tiles;
+    int seq, kvh, row, part, tok_begin, n_tok, n_tiles;
 };
 
-// Item number ci (0 <= ci < prefix[B]) -> (sequence, kv head, partition).
-// prefix[s] = number of items of sequences before s; a sequence of L tokens
-// has num_kv_heads * ceil(L / partition_size) items, kv head major.
+// Rows: a sequence (tables shared by its kv heads) or, with per-(sequence,
+// kv head) tables, one (sequence, kv head) pair; row r has length
+// context_lens[r] either way.
+__device__ __forceinline__ bool tc_per_kvh(const DecodeParams& p) { return p.table_kvh_stride != 0; }
+__device__ __forceinline__ int tc_rows(const DecodeParams& p) {
+    return tc_per_kvh(p) ? p.num_seqs * p.num_kv_heads : p.num_seqs;
+}
+
+// Item number ci (0 <= ci < prefix[rows]) -> (sequence, kv head, partition).
+// prefix[r] = number of items of rows before r; a row of L tokens has
+// ceil(L / partition_size) items per kv head it covers, kv head major.
 __device__ __forceinline__ void tc_decode_item(int ci, const DecodeParams& p, const int* lens, const int* prefix,
                                                TcItem& it) {
-    int lo = 0, hi = p.num_seqs;  // find the last s with prefix[s] <= ci
+    int lo = 0, hi = tc_rows(p);  // find the last r with prefix[r] <= ci
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (prefix[mid] <= ci) lo = mid;
@@ -96,9 +104,16 @@ __device__ __forceinline__ void tc_decode_item(int ci, const DecodeParams& p, co
     const int L = lens[lo];
     const int parts = (L + p.partition_size - 1) / p.partition_size;
     const int r = ci - prefix[lo];
-    it.seq = lo;
-    it.kvh = r / parts;
-    it.part = r - it.kvh * parts;
+    it.row = lo;
+    if (tc_per_kvh(p)) {
+        it.seq = lo / p.num_kv_heads;
+        it.kvh = lo - it.seq * p.num_kv_heads;
+        it.part = r;
+    } else {
+        it.seq = lo;
+        it.kvh = r / parts;
+        it.part = r - it.kvh * parts;
+    }
     it.tok_begin = it.part * p.partition_size;
     it.n_tok = min(p.partition_size, L - it.tok_begin);
     it.n_tiles = (it.n_tok + kTcTile - 1) / kTcTile;
@@ -173,10 +188,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int B = p.num_seqs;  // <= kTcMaxSeqs (checked on the host)
+    const int B = tc_rows(p);  // rows: <= kTcMaxSeqs (checked on the host)
+    const int heads_per_row = tc_per_kvh(p) ? 1 : p.num_kv_heads;
 
-    // Lengths and the exclusive prefix of items per sequence (a sequence with a
-    // length outside 1..max_blocks*BS has no items).
+    // Lengths and the exclusive prefix of items per row (a row with a length
+    // outside 1..max_blocks*BS has no items).
     {
         const int chunk = (B + kTcThreads - 1) / kTcThreads;
         const int s0 = min(B, threadIdx.x * chunk), s1 = min(B, s0 + chunk);
@@ -185,7 +201,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int L = p.context_lens[s];
             s_lens[s] = L;
             if (L >= 1 && L <= p.max_blocks_per_seq * BS)
-                local += p.num_kv_heads * ((L + p.partition_size - 1) / p.partition_size);
+                local += heads_per_row * ((L + p.partition_size - 1) / p.partition_size);
         }
         int incl = local;
 #pragma unroll
@@ -203,7 +219,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             s_prefix[s] = run;
             const int L = s_lens[s];
             if (L >= 1 && L <= p.max_blocks_per_seq * BS)
-                run += p.num_kv_heads * ((L + p.partition_size - 1) / p.partition_size);
+                run += heads_per_row * ((L + p.partition_size - 1) / p.partition_size);
         }
         if (threadIdx.x == kTcThreads - 1) s_prefix[B] = base + incl;
     }
@@ -277,7 +293,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int n_blk = (it.n_tok + BS - 1) / BS;
             int phys = -1;
             if (lane < n_blk) {
-                phys = p.block_tables[static_cast<size_t>(it.seq) * p.max_blocks_per_seq + it.tok_begin / BS + lane];
+                phys = p.block_tables[it.seq * p.table_seq_stride + it.kvh * p.table_kvh_stride + it.tok_begin / BS +
+                                      lane];
                 if (phys < 0 || phys >= p.num_blocks) {
                     atomicOr(p.err, kErrBadBlock);
                     phys = -1;
@@ -318,7 +335,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         auto issue_q_and_k = [&](const TcItem& it, int phys, int k) {
             bool good = true;
-            if (p.new_slots != nullptr && it.tok_begin + it.n_tok == s_lens[it.seq]) {
+            if (p.new_slots != nullptr && it.tok_begin + it.n_tok == s_lens[it.row]) {
                 // fused append: this item holds the new (last) token; write it before
                 // the TMA reads of its block
                 append_row_warp<ACT, ACT>(p.k_new, p.v_new, p.new_slots[it.seq], it.seq, it.kvh, p.num_kv_heads,
@@ -611,7 +628,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (named_bar_or(1, 128, !good)) return false;
             if (tid == 0) mbar_arrive(&o_free[b]);
             const int d = row;
-            const bool single = p.max_parts == 1 || s_lens[it.seq] <= p.partition_size;
+            const bool single = p.max_parts == 1 || s_lens[it.row] <= p.partition_size;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float Mg = stats[b * 16 + g];

@@ -126,16 +126,17 @@ __global__ void __launch_bounds__(256) quest_append_minmax_kernel(QuestAppendPar
     }
 }
 
-// Selection: one CTA of 256 threads per (kv head, sequence).  Warp w scores
-// logical blocks w, w + 8, ... (lanes over head_dim, coalesced metadata
-// rows; the bound of a kv head is the largest over its G query heads); then
-// a bitonic sort of (bound desc, logical index asc) in shared memory keeps
-// the first budget_blocks, which are written in logical order.
-constexpr int kQuestThreads = 256;
+// Selection: one CTA of 1024 threads per (kv head, sequence).  The group's
+// queries are staged in shared memory; thread j scores logical blocks j,
+// j + 1024, ... from 16-byte loads of the block's min and max rows (the
+// bound of a kv head is the largest over its G query heads); a bitonic sort
+// of (bound desc, logical index asc) in shared memory keeps the first
+// budget_blocks, which are written in logical order.
+constexpr int kQuestThreads = 1024;
 
 template <int T, int D, int G>
 __global__ void __launch_bounds__(kQuestThreads) quest_select_kernel(QuestSelectParams p) {
-    extern __shared__ unsigned char smem[];
+    extern __shared__ __align__(16) unsigned char smem[];
     const int kvh = blockIdx.x;
     const int seq = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -157,50 +158,48 @@ __global__ void __launch_bounds__(kQuestThreads) quest_select_kernel(QuestSelect
         return;
     }
     const int n2 = p.sort_size;  // power of two >= nblk, sized by the host
-    float* U = reinterpret_cast<float*>(smem);
-    int* idx = reinterpret_cast<int*>(U + n2);
+    float* qs = reinterpret_cast<float*>(smem);          // [G][D]
+    float* U = qs + G * D;                               // [n2]
+    int* idx = reinterpret_cast<int*>(U + n2);           // [n2]
     unsigned char* chosen = reinterpret_cast<unsigned char*>(idx + n2);
 
-    constexpr int CH = D / 32;  // channels per lane
-    float qv[G][CH];
     const uint16_t* qrow = static_cast<const uint16_t*>(p.q) + (static_cast<int64_t>(seq) * p.num_q_heads + kvh * G) * D;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int e = 0; e < CH; ++e) qv[g][e] = act_to_float<T>(qrow[g * D + lane * CH + e]);
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) qs[i] = act_to_float<T>(qrow[i]);
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x) chosen[j] = 0;
+    __syncthreads();
 
-    for (int j = warp; j < n2; j += kQuestThreads / 32) {
+    for (int j = threadIdx.x; j < n2; j += blockDim.x) {
         float best = -INFINITY;
         if (j < nblk) {
             const int blk = table[j];
             if (blk < 0 || blk >= p.num_blocks) {
-                if (lane == 0) atomicOr(p.err, kErrBadBlock);
+                atomicOr(p.err, kErrBadBlock);
             } else {
                 const uint16_t* meta =
                     static_cast<const uint16_t*>(p.kmeta) + ((static_cast<int64_t>(blk) * p.num_kv_heads + kvh) * 2) * D;
-                float mn[CH], mx[CH];
+                float u[G];
 #pragma unroll
-                for (int e = 0; e < CH; ++e) {
-                    mn[e] = act_to_float<T>(meta[lane * CH + e]);
-                    mx[e] = act_to_float<T>(meta[D + lane * CH + e]);
+                for (int g = 0; g < G; ++g) u[g] = 0.f;
+#pragma unroll 4
+                for (int c = 0; c < D; c += 8) {
+                    float mn[8], mx[8];
+                    unpack8<T>(*reinterpret_cast<const uint4*>(meta + c), mn);
+                    unpack8<T>(*reinterpret_cast<const uint4*>(meta + D + c), mx);
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float qv = qs[g * D + c + e];
+                            u[g] += fmaxf(qv * mn[e], qv * mx[e]);
+                        }
                 }
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float u = 0.f;
-#pragma unroll
-                    for (int e = 0; e < CH; ++e) u += fmaxf(qv[g][e] * mn[e], qv[g][e] * mx[e]);
-#pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) u += __shfl_xor_sync(0xffffffffu, u, off);
-                    best = fmaxf(best, u);
-                }
+                for (int g = 0; g < G; ++g) best = fmaxf(best, u[g]);
             }
         }
-        if (lane == 0) {
-            U[j] = j < nblk ? best : -INFINITY;
-            idx[j] = j < nblk ? j : 0x7fffffff;
-        }
+        U[j] = j < nblk ? best : -INFINITY;
+        idx[j] = j < nblk ? j : 0x7fffffff;
     }
-    for (int j = threadIdx.x; j < nblk; j += blockDim.x) chosen[j] = 0;
     __syncthreads();
     // bitonic sort: descending bound, ascending logical index on equal bounds
     for (int k = 2; k <= n2; k <<= 1) {
@@ -271,7 +270,7 @@ cudaError_t launch_quest_append_minmax(const QuestAppendParams& p, int dtype, cu
 namespace {
 template <int T, int D, int G>
 cudaError_t select_one(const QuestSelectParams& p, cudaStream_t s) {
-    const size_t smem = static_cast<size_t>(p.sort_size) * 9;  // bound, index, chosen flag
+    const size_t smem = static_cast<size_t>(G) * D * 4 + static_cast<size_t>(p.sort_size) * 9;  // q, bound, index, flag
     auto kern = quest_select_kernel<T, D, G>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -118,3 +118,20 @@ def test_full_budget_reproduces_full_decode(pkv):
     full = pkv.paged_attention_decode(q.to(dev), dk, dv, t_d, l_d, 0.09)
     torch.cuda.synchronize()
     assert torch.equal(sparse, full)
+
+
+@pytest.mark.parametrize("path", [1, 3])
+def test_sparse_decode_paths_agree_with_oracle(pkv, path):
+    """Per-(sequence, kv head) tables on the CUDA-core and tensor-core kernels."""
+    q, kc, vc, _, _, tables, _, lens = _setup("bf16", 32, 4, 128, 16, [100, 900, 2500, 4000], 21)
+    dev = torch.device("cuda")
+    dk, dv = kc.to(dev), vc.to(dev)
+    t_d, l_d = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
+    kmeta = pkv.quest_block_minmax(dk, t_d, l_d)
+    sel, slen = pkv.quest_select(q.to(dev), kmeta, t_d, l_d, 16, 64)
+    pkv.set_kernel_path(path)
+    out = pkv.paged_attention_decode_sparse(q.to(dev), dk, dv, sel, slen, 0.088, partition_size=512)
+    torch.cuda.synchronize()
+    want = oracle.sparse_decode(bits(q), oracle.BF16, bits(dk), bits(dv), oracle.BF16, sel.cpu().numpy(),
+                                slen.cpu().numpy(), 0.088)
+    assert_attention_close(out, want, TOL["bf16"], rounding_slack=True)
