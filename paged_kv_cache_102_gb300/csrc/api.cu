@@ -282,8 +282,8 @@ static int decode_impl(const char* fn, const void* q, const void* k_cache, const
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     const int path = g_kernel_path.load();
-    const int rows = per_kvh_tables ? num_seqs * num_kv_heads : num_seqs;
-    const bool tc_ok = decode_tc_supported(rows, head_dim, block_size, G, act_dtype, cache_dtype, P);
+    const int table_rows = per_kvh_tables ? num_seqs * num_kv_heads : num_seqs;
+    const bool tc_ok = decode_tc_supported(table_rows, head_dim, block_size, G, act_dtype, cache_dtype, P);
     if ((path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA) && !tc_ok)
         return fail(PKV_ERR_INVALID, F + ": " + "the tensor-core path needs head_dim 128, a 16-bit "
                                      "cache, 2/4/8 query heads per kv head and partitions of at most 512 tokens");
