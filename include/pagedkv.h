@@ -320,12 +320,20 @@ int quest_append_minmax(const void* k_new, const int64_t* slot_mapping, int num_
  * sel_tables int32 [num_seqs][num_kv_heads][budget_blocks] (unused entries 0)
  * and sel_lens int32 [num_seqs][num_kv_heads] (their token count; the
  * sequence's last block counts its filled slots).  A sequence with at most
- * budget_blocks blocks keeps them all.  Bounds are computed in float32.
+ * budget_blocks blocks keeps them all.  Bounds are computed in float32 by
+ * one kernel over every block and kept in `workspace` (device, at least
+ * quest_workspace_size bytes, no initialisation needed); a second kernel
+ * sorts each (sequence, kv head)'s bounds in shared memory.
  * head_dim 64 or 128; group 1, 2, 4 or 8; at most 16384 blocks per sequence. */
 int quest_select(const void* q, const void* kmeta, const int32_t* block_tables,
                  int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
                  int num_kv_heads, int block_size, int head_dim, int num_blocks, int act_dtype,
-                 int budget_blocks, int32_t* sel_tables, int32_t* sel_lens, void* stream);
+                 int budget_blocks, int32_t* sel_tables, int32_t* sel_lens, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* Device workspace quest_select needs: one float32 bound per (sequence, kv
+ * head, table entry).  Host only. */
+size_t quest_workspace_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq);
 
 /* paged_attention_decode over per-(sequence, kv head) block lists, such as
  * quest_select's: tables [num_seqs][num_kv_heads][max_sel_blocks], lengths

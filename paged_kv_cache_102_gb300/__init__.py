@@ -211,7 +211,7 @@ def quest_append_minmax(k_new, slot_mapping, kmeta, block_size, stream=None):
 
 
 def quest_select(q, kmeta, block_tables, context_lens, block_size, budget_blocks, sel_tables=None, sel_lens=None,
-                 stream=None):
+                 workspace=None, stream=None):
     """QUEST top-K blocks per (sequence, kv head); returns (sel_tables [B, Hkv, budget], sel_lens [B, Hkv])."""
     B, Hq, D = q.shape
     NB, Hkv = kmeta.shape[0], kmeta.shape[1]
@@ -220,10 +220,14 @@ def quest_select(q, kmeta, block_tables, context_lens, block_size, budget_blocks
     if sel_lens is None:
         sel_lens = torch.empty(B, Hkv, dtype=torch.int32, device=q.device)
     _require_cuda(q.device, q=q, kmeta=kmeta, block_tables=block_tables, context_lens=context_lens,
-                  sel_tables=sel_tables, sel_lens=sel_lens)
+                  sel_tables=sel_tables, sel_lens=sel_lens, workspace=workspace)
+    s = _stream(stream, q.device)
+    need = int(_native.lib().quest_workspace_size(B, Hkv, block_tables.shape[1]))
+    if workspace is None:
+        workspace = _workspace(q.device, -(s.value or 0) - 1, need)  # separate from the decode workspace
     _native.call("quest_select", _ptr(q), _ptr(kmeta), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
                  B, Hq, Hkv, block_size, D, NB, _code(q), int(budget_blocks), _ptr(sel_tables), _ptr(sel_lens),
-                 _stream(stream, q.device))
+                 _ptr(workspace), workspace.numel() * workspace.element_size(), s)
     return sel_tables, sel_lens
 
 

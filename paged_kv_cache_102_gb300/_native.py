@@ -34,7 +34,8 @@ SIGNATURES = {
                                             P, I32, P, SZ, P]),
     "quest_block_minmax": (I32, [P, P, I32, P, I32, I32, I32, I32, I32, I32, P, P]),
     "quest_append_minmax": (I32, [P, P, I32, I32, I32, I32, I32, I32, P, P]),
-    "quest_select": (I32, [P, P, P, I32, P, I32, I32, I32, I32, I32, I32, I32, I32, P, P, P]),
+    "quest_select": (I32, [P, P, P, I32, P, I32, I32, I32, I32, I32, I32, I32, I32, P, P, P, SZ, P]),
+    "quest_workspace_size": (SZ, [I32, I32, I32]),
     "pkv_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
     "pkv_resolve_partition_size": (I32, [I32, I32, I32, I32, I32, I32, I32]),
     "paged_block_copy": (I32, [P, P, P, I32, I32, SZ, P]),

@@ -396,10 +396,15 @@ int quest_append_minmax(const void* k_new, const int64_t* slot_mapping, int num_
     return e == cudaSuccess ? PKV_OK : cuda_fail("quest_append_minmax: launch", e);
 }
 
+size_t quest_workspace_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq) {
+    if (num_seqs <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0) return 0;
+    return static_cast<size_t>(num_seqs) * num_kv_heads * max_blocks_per_seq * sizeof(float);
+}
+
 int quest_select(const void* q, const void* kmeta, const int32_t* block_tables, int max_blocks_per_seq,
                  const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
                  int head_dim, int num_blocks, int act_dtype, int budget_blocks, int32_t* sel_tables, int32_t* sel_lens,
-                 void* stream) {
+                 void* workspace, size_t workspace_bytes, void* stream) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
         max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0 || budget_blocks <= 0)
         return fail(PKV_ERR_INVALID, "quest_select: sizes must be positive, num_q_heads a multiple of num_kv_heads");
@@ -408,17 +413,22 @@ int quest_select(const void* q, const void* kmeta, const int32_t* block_tables, 
     if (head_dim != 64 && head_dim != 128) return fail(PKV_ERR_INVALID, "quest_select: head_dim must be 64 or 128");
     if (act_dtype != PKV_F16 && act_dtype != PKV_BF16)
         return fail(PKV_ERR_INVALID, "quest_select: act_dtype must be PKV_F16 or PKV_BF16");
-    int sort_size = 1;
+    int sort_size = 32;  // the sort kernel works on at least 32 entries
     while (sort_size < max_blocks_per_seq) sort_size <<= 1;
     if (sort_size > 16384) return fail(PKV_ERR_INVALID, "quest_select: at most 16384 blocks per sequence");
     if (num_seqs == 0) return PKV_OK;
     if (num_seqs > 65535 || num_kv_heads > 65535) return fail(PKV_ERR_INVALID, "quest_select: grid too large");
     if (!q || !kmeta || !block_tables || !context_lens || !sel_tables || !sel_lens)
         return fail(PKV_ERR_INVALID, "quest_select: null pointer");
+    const size_t need = quest_workspace_size(num_seqs, num_kv_heads, max_blocks_per_seq);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
+        return fail(PKV_ERR_INVALID, "quest_select: workspace of " + std::to_string(need) +
+                                         " bytes (16-byte aligned) required (quest_workspace_size)");
     int* err = device_error_word();
     if (!err) return fail(PKV_ERR_CUDA, "quest_select: cannot resolve the device error word");
-    QuestSelectParams p{q, kmeta, block_tables, context_lens, sel_tables, sel_lens, err, num_seqs, num_q_heads,
-                        num_kv_heads, block_size, head_dim, num_blocks, max_blocks_per_seq, budget_blocks, sort_size};
+    QuestSelectParams p{q, kmeta, block_tables, context_lens, sel_tables, sel_lens, static_cast<float*>(workspace),
+                        err, num_seqs, num_q_heads, num_kv_heads, block_size, head_dim, num_blocks,
+                        max_blocks_per_seq, budget_blocks, sort_size};
     cudaError_t e = launch_quest_select(p, act_dtype, G, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail("quest_select: launch", e);
 }

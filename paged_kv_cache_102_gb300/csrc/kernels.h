@@ -128,6 +128,7 @@ struct QuestSelectParams {
     const int32_t* context_lens;
     int32_t* sel_tables;
     int32_t* sel_lens;
+    float* bounds;  // workspace [num_seqs][num_kv_heads][max_blocks_per_seq]
     int* err;
     int num_seqs;
     int num_q_heads;

@@ -126,16 +126,61 @@ __global__ void __launch_bounds__(256) quest_append_minmax_kernel(QuestAppendPar
     }
 }
 
-// Selection: one CTA of 1024 threads per (kv head, sequence).  The group's
-// queries are staged in shared memory; thread j scores logical blocks j,
-// j + 1024, ... from 16-byte loads of the block's min and max rows (the
-// bound of a kv head is the largest over its G query heads); a bitonic sort
-// of (bound desc, logical index asc) in shared memory keeps the first
-// budget_blocks, which are written in logical order.
-constexpr int kQuestThreads = 1024;
-
+// Selection, step 1: the bound of every (sequence, kv head, logical block),
+// one thread per block over all SMs (the bound of a kv head is the largest
+// over its G query heads).  Consecutive threads share (sequence, kv head), so
+// their query loads are warp-uniform; each reads its block's min and max rows
+// with 16-byte loads.  Bounds go to the workspace [B][Hkv][max_blocks].
 template <int T, int D, int G>
-__global__ void __launch_bounds__(kQuestThreads) quest_select_kernel(QuestSelectParams p) {
+__global__ void __launch_bounds__(256) quest_bounds_kernel(QuestSelectParams p) {
+    const int64_t per_row = p.max_blocks_per_seq;
+    const int64_t total = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * per_row;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int j = static_cast<int>(i % per_row);
+        const int64_t r = i / per_row;
+        const int kvh = static_cast<int>(r % p.num_kv_heads);
+        const int seq = static_cast<int>(r / p.num_kv_heads);
+        const int L = p.context_lens[seq];
+        if (L < 1 || L > p.max_blocks_per_seq * p.block_size || j * p.block_size >= L) continue;
+        const int blk = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks_per_seq + j];
+        float best = -INFINITY;
+        if (blk < 0 || blk >= p.num_blocks) {
+            atomicOr(p.err, kErrBadBlock);
+        } else {
+            const uint16_t* meta =
+                static_cast<const uint16_t*>(p.kmeta) + ((static_cast<int64_t>(blk) * p.num_kv_heads + kvh) * 2) * D;
+            const uint16_t* qrow =
+                static_cast<const uint16_t*>(p.q) + (static_cast<int64_t>(seq) * p.num_q_heads + kvh * G) * D;
+            float u[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) u[g] = 0.f;
+#pragma unroll 4
+            for (int c = 0; c < D; c += 8) {
+                float mn[8], mx[8];
+                unpack8<T>(*reinterpret_cast<const uint4*>(meta + c), mn);
+                unpack8<T>(*reinterpret_cast<const uint4*>(meta + D + c), mx);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float qv[8];
+                    unpack8<T>(*reinterpret_cast<const uint4*>(qrow + g * D + c), qv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) u[g] += fmaxf(qv[e] * mn[e], qv[e] * mx[e]);
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) best = fmaxf(best, u[g]);
+        }
+        p.bounds[i] = best;
+    }
+}
+
+// Selection, step 2: one CTA per (kv head, sequence) sorts the row's bounds
+// (descending bound, ascending logical index on equal bounds) with a bitonic
+// network in shared memory, keeps the first budget_blocks and writes them in
+// logical order.
+template <int NT>
+__global__ void __launch_bounds__(NT) quest_topk_kernel(QuestSelectParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int kvh = blockIdx.x;
     const int seq = blockIdx.y;
@@ -146,7 +191,7 @@ __global__ void __launch_bounds__(kQuestThreads) quest_select_kernel(QuestSelect
     int32_t* out_len = p.sel_lens + static_cast<int64_t>(seq) * p.num_kv_heads + kvh;
     if (L < 1 || L > p.max_blocks_per_seq * p.block_size) {
         if (threadIdx.x == 0) {
-            atomicOr(p.err, kErrBadLen);
+            if (kvh == 0) atomicOr(p.err, kErrBadLen);
             *out_len = 0;
         }
         return;
@@ -157,54 +202,21 @@ __global__ void __launch_bounds__(kQuestThreads) quest_select_kernel(QuestSelect
         if (threadIdx.x == 0) *out_len = L;
         return;
     }
-    const int n2 = p.sort_size;  // power of two >= nblk, sized by the host
-    float* qs = reinterpret_cast<float*>(smem);          // [G][D]
-    float* U = qs + G * D;                               // [n2]
-    int* idx = reinterpret_cast<int*>(U + n2);           // [n2]
+    int n2 = 32;  // power of two >= nblk
+    while (n2 < nblk) n2 <<= 1;
+    float* U = reinterpret_cast<float*>(smem);
+    int* idx = reinterpret_cast<int*>(U + n2);
     unsigned char* chosen = reinterpret_cast<unsigned char*>(idx + n2);
-
-    const uint16_t* qrow = static_cast<const uint16_t*>(p.q) + (static_cast<int64_t>(seq) * p.num_q_heads + kvh * G) * D;
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) qs[i] = act_to_float<T>(qrow[i]);
-    for (int j = threadIdx.x; j < nblk; j += blockDim.x) chosen[j] = 0;
-    __syncthreads();
-
-    for (int j = threadIdx.x; j < n2; j += blockDim.x) {
-        float best = -INFINITY;
-        if (j < nblk) {
-            const int blk = table[j];
-            if (blk < 0 || blk >= p.num_blocks) {
-                atomicOr(p.err, kErrBadBlock);
-            } else {
-                const uint16_t* meta =
-                    static_cast<const uint16_t*>(p.kmeta) + ((static_cast<int64_t>(blk) * p.num_kv_heads + kvh) * 2) * D;
-                float u[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) u[g] = 0.f;
-#pragma unroll 4
-                for (int c = 0; c < D; c += 8) {
-                    float mn[8], mx[8];
-                    unpack8<T>(*reinterpret_cast<const uint4*>(meta + c), mn);
-                    unpack8<T>(*reinterpret_cast<const uint4*>(meta + D + c), mx);
-#pragma unroll
-                    for (int g = 0; g < G; ++g)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float qv = qs[g * D + c + e];
-                            u[g] += fmaxf(qv * mn[e], qv * mx[e]);
-                        }
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) best = fmaxf(best, u[g]);
-            }
-        }
-        U[j] = j < nblk ? best : -INFINITY;
+    const float* row = p.bounds + (static_cast<int64_t>(seq) * p.num_kv_heads + kvh) * p.max_blocks_per_seq;
+    for (int j = threadIdx.x; j < n2; j += NT) {
+        U[j] = j < nblk ? row[j] : -INFINITY;
         idx[j] = j < nblk ? j : 0x7fffffff;
+        if (j < nblk) chosen[j] = 0;
     }
     __syncthreads();
-    // bitonic sort: descending bound, ascending logical index on equal bounds
     for (int k = 2; k <= n2; k <<= 1) {
         for (int jj = k >> 1; jj > 0; jj >>= 1) {
-            for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+            for (int i = threadIdx.x; i < n2; i += NT) {
                 const int partner = i ^ jj;
                 if (partner > i) {
                     const bool desc = (i & k) == 0;
@@ -222,10 +234,9 @@ __global__ void __launch_bounds__(kQuestThreads) quest_select_kernel(QuestSelect
             __syncthreads();
         }
     }
-    for (int r = threadIdx.x; r < p.budget_blocks; r += blockDim.x)
+    for (int r = threadIdx.x; r < p.budget_blocks; r += NT)
         if (idx[r] >= 0 && idx[r] < nblk) chosen[idx[r]] = 1;  // (NaN bounds could misorder the padding)
     __syncthreads();
-    // write the chosen blocks in logical order (one warp; nblk is small)
     if (warp == 0) {
         int base = 0, tokens = 0;
         for (int j0 = 0; j0 < nblk; j0 += 32) {
@@ -269,32 +280,48 @@ cudaError_t launch_quest_append_minmax(const QuestAppendParams& p, int dtype, cu
 
 namespace {
 template <int T, int D, int G>
-cudaError_t select_one(const QuestSelectParams& p, cudaStream_t s) {
-    const size_t smem = static_cast<size_t>(G) * D * 4 + static_cast<size_t>(p.sort_size) * 9;  // q, bound, index, flag
-    auto kern = quest_select_kernel<T, D, G>;
+cudaError_t bounds_one(const QuestSelectParams& p, cudaStream_t s) {
+    const int64_t total = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * p.max_blocks_per_seq;
+    const int blocks = static_cast<int>(total / 256 + 1 < 152 * 64 ? total / 256 + 1 : 152 * 64);
+    quest_bounds_kernel<T, D, G><<<blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+template <int T, int D>
+cudaError_t bounds_g(const QuestSelectParams& p, int G, cudaStream_t s) {
+    switch (G) {
+        case 1: return bounds_one<T, D, 1>(p, s);
+        case 2: return bounds_one<T, D, 2>(p, s);
+        case 4: return bounds_one<T, D, 4>(p, s);
+        case 8: return bounds_one<T, D, 8>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+template <int NT>
+cudaError_t topk(const QuestSelectParams& p, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(p.sort_size) * 9;  // bound, index, chosen flag
+    auto kern = quest_topk_kernel<NT>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    kern<<<dim3(p.num_kv_heads, p.num_seqs), kQuestThreads, smem, s>>>(p);
+    kern<<<dim3(p.num_kv_heads, p.num_seqs), NT, smem, s>>>(p);
     return cudaGetLastError();
-}
-template <int T, int D>
-cudaError_t select_g(const QuestSelectParams& p, int G, cudaStream_t s) {
-    switch (G) {
-        case 1: return select_one<T, D, 1>(p, s);
-        case 2: return select_one<T, D, 2>(p, s);
-        case 4: return select_one<T, D, 4>(p, s);
-        case 8: return select_one<T, D, 8>(p, s);
-        default: return cudaErrorInvalidValue;
-    }
 }
 }  // namespace
 
 cudaError_t launch_quest_select(const QuestSelectParams& p, int dtype, int G, cudaStream_t s) {
     if (p.num_seqs == 0) return cudaSuccess;
-    if (dtype == kBF16) return p.head_dim == 128 ? select_g<kBF16, 128>(p, G, s) : select_g<kBF16, 64>(p, G, s);
-    return p.head_dim == 128 ? select_g<kF16, 128>(p, G, s) : select_g<kF16, 64>(p, G, s);
+    cudaError_t e;
+    if (dtype == kBF16)
+        e = p.head_dim == 128 ? bounds_g<kBF16, 128>(p, G, s) : bounds_g<kBF16, 64>(p, G, s);
+    else
+        e = p.head_dim == 128 ? bounds_g<kF16, 128>(p, G, s) : bounds_g<kF16, 64>(p, G, s);
+    if (e != cudaSuccess) return e;
+    // threads: half the sort size (one compare-exchange each per stage), 32..1024
+    if (p.sort_size <= 64) return topk<32>(p, s);
+    if (p.sort_size <= 256) return topk<128>(p, s);
+    if (p.sort_size <= 1024) return topk<512>(p, s);
+    return topk<1024>(p, s);
 }
 
 }  // namespace pkv
