@@ -323,7 +323,8 @@ int quest_append_minmax(const void* k_new, const int64_t* slot_mapping, int num_
  * budget_blocks blocks keeps them all.  Bounds are computed in float32 by
  * one kernel over every block and kept in `workspace` (device, at least
  * quest_workspace_size bytes, no initialisation needed); a second kernel
- * sorts each (sequence, kv head)'s bounds in shared memory.
+ * finds each (sequence, kv head)'s K-th largest bound by radix selection
+ * over the bounds' order-preserving 32-bit keys in shared memory.
  * head_dim 64 or 128; group 1, 2, 4 or 8; at most 16384 blocks per sequence. */
 int quest_select(const void* q, const void* kmeta, const int32_t* block_tables,
                  int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,

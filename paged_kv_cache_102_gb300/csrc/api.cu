@@ -413,13 +413,12 @@ int quest_select(const void* q, const void* kmeta, const int32_t* block_tables, 
     if (head_dim != 64 && head_dim != 128) return fail(PKV_ERR_INVALID, "quest_select: head_dim must be 64 or 128");
     if (act_dtype != PKV_F16 && act_dtype != PKV_BF16)
         return fail(PKV_ERR_INVALID, "quest_select: act_dtype must be PKV_F16 or PKV_BF16");
-    int sort_size = 32;  // the sort kernel works on at least 32 entries
-    while (sort_size < max_blocks_per_seq) sort_size <<= 1;
-    if (sort_size > 16384) return fail(PKV_ERR_INVALID, "quest_select: at most 16384 blocks per sequence");
+    if (max_blocks_per_seq > 16384) return fail(PKV_ERR_INVALID, "quest_select: at most 16384 blocks per sequence");
     if (num_seqs == 0) return PKV_OK;
     if (num_seqs > 65535 || num_kv_heads > 65535) return fail(PKV_ERR_INVALID, "quest_select: grid too large");
     if (!q || !kmeta || !block_tables || !context_lens || !sel_tables || !sel_lens)
         return fail(PKV_ERR_INVALID, "quest_select: null pointer");
+    if (!aligned(q, 16) || !aligned(kmeta, 16)) return fail(PKV_ERR_INVALID, "quest_select: q and kmeta must be 16-byte aligned");
     const size_t need = quest_workspace_size(num_seqs, num_kv_heads, max_blocks_per_seq);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
         return fail(PKV_ERR_INVALID, "quest_select: workspace of " + std::to_string(need) +
@@ -428,7 +427,7 @@ int quest_select(const void* q, const void* kmeta, const int32_t* block_tables, 
     if (!err) return fail(PKV_ERR_CUDA, "quest_select: cannot resolve the device error word");
     QuestSelectParams p{q, kmeta, block_tables, context_lens, sel_tables, sel_lens, static_cast<float*>(workspace),
                         err, num_seqs, num_q_heads, num_kv_heads, block_size, head_dim, num_blocks,
-                        max_blocks_per_seq, budget_blocks, sort_size};
+                        max_blocks_per_seq, budget_blocks};
     cudaError_t e = launch_quest_select(p, act_dtype, G, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail("quest_select: launch", e);
 }

@@ -138,7 +138,6 @@ struct QuestSelectParams {
     int num_blocks;
     int max_blocks_per_seq;
     int budget_blocks;
-    int sort_size;  // power of two >= max_blocks_per_seq
 };
 
 cudaError_t launch_quest_minmax(const QuestMetaParams& p, int dtype, cudaStream_t s);

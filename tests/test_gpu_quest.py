@@ -46,7 +46,35 @@ def _setup(act, Hq, Hkv, D, bs, ctx, seed):
     return q, kc, vc, k_new, v_new, tables, slots, np.array([c + 1 for c in ctx], np.int32)
 
 
-CASES = [("bf16", 8, 8, 128, 16), ("f16", 16, 4, 64, 32), ("bf16", 32, 4, 128, 16)]
+CASES = [("bf16", 8, 8, 128, 16), ("f16", 16, 4, 64, 32), ("bf16", 32, 4, 128, 16), ("bf16", 16, 8, 64, 16),
+         ("f16", 32, 4, 64, 16)]
+
+
+def _check_selection(sel_h, slen_h, q, kbits, act, tables, lens, bs, budget):
+    """Selected blocks equal the oracle's where its bounds have a margin at the
+    cut, and form a valid top-K (ascending, distinct, token count right) everywhere."""
+    want_sel, want_len, bounds = oracle.quest_select(bits(q), ACT_CODE[DT[act]], kbits, ACT_CODE[DT[act]],
+                                                     tables, lens, budget)
+    B, Hkv = slen_h.shape
+    for b in range(B):
+        n = -(-int(lens[b]) // bs)
+        pos = {int(x): j for j, x in enumerate(tables[b, :n])}
+        for h in range(Hkv):
+            got = [int(x) for x in sel_h[b, h, : min(budget, n)]]
+            logical = [pos[x] for x in got]
+            assert logical == sorted(logical) and len(set(logical)) == len(logical)
+            toks = sum(int(lens[b]) - j * bs if j == n - 1 else bs for j in logical)
+            assert slen_h[b, h] == toks
+            if n <= budget:
+                assert logical == list(range(n))
+                continue
+            u = bounds[b, h, :n]
+            order = np.sort(u)[::-1]
+            cut, nxt = order[budget - 1], order[budget]
+            if cut - nxt > 1e-3 * max(1.0, abs(cut)):
+                assert got == [int(x) for x in want_sel[b, h, :budget]]
+            else:  # a near tie at the cut: any valid top-K
+                assert min(u[logical]) >= nxt - 1e-3 * max(1.0, abs(nxt))
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
@@ -80,26 +108,7 @@ def test_quest_metadata_selection_and_sparse_decode(pkv, case):
         sel, slen = pkv.quest_select(q.to(dev), full, t_d, l_d, bs, budget)
         torch.cuda.synchronize()
         sel_h, slen_h = sel.cpu().numpy(), slen.cpu().numpy()
-        want_sel, want_len, bounds = oracle.quest_select(bits(q), ACT_CODE[DT[act]], kbits, ACT_CODE[DT[act]],
-                                                         tables, lens, budget)
-        for b in range(len(ctx)):
-            n = -(-int(lens[b]) // bs)
-            for h in range(Hkv):
-                got = [int(x) for x in sel_h[b, h, : min(budget, n)]]
-                logical = [int(np.where(tables[b, :n] == x)[0][0]) for x in got]
-                assert logical == sorted(logical) and len(set(logical)) == len(logical)
-                toks = sum(int(lens[b]) - j * bs if j == n - 1 else bs for j in logical)
-                assert slen_h[b, h] == toks
-                if n <= budget:
-                    assert logical == list(range(n))
-                    continue
-                u = bounds[b, h, :n]
-                order = np.sort(u)[::-1]
-                cut, nxt = order[budget - 1], order[budget]
-                if cut - nxt > 1e-3 * max(1.0, abs(cut)):
-                    assert got == [int(x) for x in want_sel[b, h, :budget]]
-                else:  # a near tie at the cut: any valid top-K
-                    assert min(u[logical]) >= nxt - 1e-3 * max(1.0, abs(nxt))
+        _check_selection(sel_h, slen_h, q, kbits, act, tables, lens, bs, budget)
         out = pkv.paged_attention_decode_sparse(q.to(dev), dk, dv, sel, slen, 0.09)
         torch.cuda.synchronize()
         want = oracle.sparse_decode(bits(q), ACT_CODE[DT[act]], kbits, bits(dv), ACT_CODE[DT[act]], sel_h, slen_h,
@@ -135,3 +144,20 @@ def test_sparse_decode_paths_agree_with_oracle(pkv, path):
     want = oracle.sparse_decode(bits(q), oracle.BF16, bits(dk), bits(dv), oracle.BF16, sel.cpu().numpy(),
                                 slen.cpu().numpy(), 0.088)
     assert_attention_close(out, want, TOL["bf16"], rounding_slack=True)
+
+
+@pytest.mark.parametrize("group", [4, 8])
+def test_quest_select_many_items_per_cta(pkv, group):
+    """Enough (sequence, kv head, 32-block chunk) items that every persistent
+    CTA of the bounds kernel cycles its shared-memory ring several times."""
+    Hkv, D, bs = 2, 64, 16
+    ctx = [9000 + 37 * i for i in range(96)]  # 96 x 2 x 23 items over at most 3 CTAs per SM
+    q, kc, _, _, _, tables, _, lens = _setup("bf16", Hkv * group, Hkv, D, bs, ctx, 77 + group)
+    dev = torch.device("cuda")
+    dk = kc.to(dev)
+    t_d, l_d = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
+    kmeta = pkv.quest_block_minmax(dk, t_d, l_d)
+    for budget in (3, 100):
+        sel, slen = pkv.quest_select(q.to(dev), kmeta, t_d, l_d, bs, budget)
+        torch.cuda.synchronize()
+        _check_selection(sel.cpu().numpy(), slen.cpu().numpy(), q, bits(kc), "bf16", tables, lens, bs, budget)
