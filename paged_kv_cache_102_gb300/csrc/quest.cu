@@ -204,11 +204,12 @@ struct SplitSum {
 //
 // Persistent CTAs walk a contiguous range of items; an item is 32 logical
 // blocks of one (sequence, kv head) row, items ordered (sequence, kv head,
-// chunk) so a CTA mostly stays on one row and keeps its query registers.  Warp 0 reads
-// the item's block ids and bulk-copies each block's min and max rows (4*D
-// contiguous bytes) into a ring of shared-memory stages; warps 1..4 compute
-// from shared memory, D/8 lanes per block (D/4 for a group of 8), lane c
-// holding q+ and q- of its 8 (or 4) channels of the group's query heads.  Bounds go to the workspace
+// chunk) so a CTA mostly stays on one row and keeps its query registers.
+// Warp 0 reads the item's block ids and bulk-copies each block's min and max
+// rows (4*D contiguous bytes) into a ring of shared-memory stages; warps 1..4
+// compute from shared memory, D/8 lanes per block (D/4 for a group of 8),
+// lane c holding q+ and q- of its 8 (or 4) channels of the group's query
+// heads.  Bounds go to the workspace
 // [B][Hkv][max_blocks] (-inf past the context).
 constexpr int kBItem = 32;
 constexpr int kBConsumerWarps = 4;
