@@ -301,6 +301,7 @@ static int decode_impl(const char* fn, const void* q, const void* k_cache, const
     if (max_parts > 1) {
         MergeParams m{};
         m.context_lens = context_lens;
+        m.num_seqs = num_seqs;
         m.lens_seq_stride = p.lens_seq_stride;
         m.lens_kvh_stride = p.lens_kvh_stride;
         m.group = G;
@@ -312,7 +313,7 @@ static int decode_impl(const char* fn, const void* q, const void* k_cache, const
         m.partition_size = P;
         m.max_parts = max_parts;
         m.max_context = static_cast<int>(max_ctx);
-        e = launch_merge(m, act_dtype, num_seqs, s);
+        e = launch_merge(m, act_dtype, s);
         if (e != cudaSuccess) return cuda_fail((F + ": merge kernel launch").c_str(), e);
     }
     return PKV_OK;

@@ -71,6 +71,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
     float* red_l = red + kConsumerWarps * G;                // [NW][G]
     float* red_acc = red + 2 * kConsumerWarps * G;          // [NW][G][D]
 
+    // the merge kernel may be scheduled once every CTA got here; it waits for
+    // this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;");
     const int part = blockIdx.x;
     const int kvh = blockIdx.y;
     const int seq = blockIdx.z;

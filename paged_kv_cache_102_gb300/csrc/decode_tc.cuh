@@ -11,7 +11,10 @@
 // read once for all G heads.
 //
 // Work item: (sequence, kv head, partition of up to 512 tokens).  Only
-// non-empty items are numbered (a per-sequence prefix sum in shared memory).
+// non-empty items are numbered, in an order that keeps the tail short: every
+// row's full partitions first, then each row's last, partly filled partition,
+// longest first (8 length buckets; a stable counting sort in shared memory
+// that every CTA computes alike).
 // The kernel is persistent and balances ragged lengths dynamically: the
 // producer of each CTA claims the next item number from a counter in the
 // workspace (zeroed before the launch) and passes it to the other roles
@@ -58,6 +61,7 @@ constexpr int kTcSlotCols = kTcMaxTiles * kTcN + kTcN;  // S (4 x 16) + O (16) p
 constexpr int kTcTmemCols = 256;              // two buffers of 80 columns, rounded to a power of 2
 constexpr int kTcMaxSeqs = 2048;              // sequences served (lengths and item prefix in shared memory)
 constexpr int kTcQueue = 4;                   // claimed items in flight between the roles
+constexpr int kTcLenBuckets = 8;              // length buckets of the partly filled partitions
 
 template <int NS>
 struct TcSmem {
@@ -65,8 +69,9 @@ struct TcSmem {
     static constexpr int Q = NS * kTcStage;
     static constexpr int P = Q + 2 * kTcQBuf;
     static constexpr int LENS = P + 2 * kTcPBuf;
-    static constexpr int PREFIX = LENS + kTcMaxSeqs * 4;      // items before each sequence, [B + 1]
-    static constexpr int QUEUE = PREFIX + (kTcMaxSeqs + 1) * 4;
+    static constexpr int PREFIX = LENS + kTcMaxSeqs * 4;      // full-partition items before each row, [B + 2]
+    static constexpr int ORDER = PREFIX + (kTcMaxSeqs + 2) * 4;  // rows with a partly filled partition, longest first
+    static constexpr int QUEUE = ORDER + kTcMaxSeqs * 2;
     static constexpr int BARS = (QUEUE + kTcQueue * 4 + 7) / 8 * 8;
     // full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_free[2], final,
     // item_full[4], item_empty[4]
@@ -90,31 +95,48 @@ __device__ __forceinline__ int tc_rows(const DecodeParams& p) {
     return tc_per_kvh(p) ? p.num_seqs * p.num_kv_heads : p.num_seqs;
 }
 
-// Item number ci (0 <= ci < prefix[rows]) -> (sequence, kv head, partition).
-// prefix[r] = number of items of rows before r; a row of L tokens has
-// ceil(L / partition_size) items per kv head it covers, kv head major.
+// Item number ci -> (sequence, kv head, partition).  Items [0, F), F =
+// prefix[rows], are full partitions: prefix[r] counts those of the rows
+// before r, a row of L tokens has floor(L / partition_size) of them per kv
+// head it covers, kv head major.  Items [F, F + H * prefix[rows + 1]) are the
+// partly filled last partitions of the rows listed in `order`, H per row
+// (H = the kv heads a row covers).
 __device__ __forceinline__ void tc_decode_item(int ci, const DecodeParams& p, const int* lens, const int* prefix,
-                                               TcItem& it) {
-    int lo = 0, hi = tc_rows(p);  // find the last r with prefix[r] <= ci
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= ci) lo = mid;
-        else hi = mid;
-    }
-    const int L = lens[lo];
-    const int parts = (L + p.partition_size - 1) / p.partition_size;
-    const int r = ci - prefix[lo];
-    it.row = lo;
-    if (tc_per_kvh(p)) {
-        it.seq = lo / p.num_kv_heads;
-        it.kvh = lo - it.seq * p.num_kv_heads;
-        it.part = r;
+                                               const uint16_t* order, TcItem& it) {
+    const int rows = tc_rows(p);
+    const int F = prefix[rows];
+    const int H = tc_per_kvh(p) ? 1 : p.num_kv_heads;
+    int row, part, h;
+    if (ci < F) {
+        int lo = 0, hi = rows;  // the last r with prefix[r] <= ci
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= ci) lo = mid;
+            else hi = mid;
+        }
+        row = lo;
+        const int nfull = lens[row] / p.partition_size;
+        const int r = ci - prefix[row];
+        h = r / nfull;
+        part = r - h * nfull;
     } else {
-        it.seq = lo;
-        it.kvh = r / parts;
-        it.part = r - it.kvh * parts;
+        const int j = ci - F;
+        const int idx = j / H;
+        row = order[idx];
+        h = j - idx * H;
+        part = lens[row] / p.partition_size;
     }
-    it.tok_begin = it.part * p.partition_size;
+    const int L = lens[row];
+    it.row = row;
+    if (tc_per_kvh(p)) {
+        it.seq = row / p.num_kv_heads;
+        it.kvh = row - it.seq * p.num_kv_heads;
+    } else {
+        it.seq = row;
+        it.kvh = h;
+    }
+    it.part = part;
+    it.tok_begin = part * p.partition_size;
     it.n_tok = min(p.partition_size, L - it.tok_begin);
     it.n_tiles = (it.n_tok + kTcTile - 1) / kTcTile;
 }
@@ -159,6 +181,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     static_assert(G == 2 || G == 4 || G == 8, "query heads per kv head");
     static_assert(kTcMaxTiles * kTcTile / BS <= 32, "one warp holds the table entries of an item");
 
+    // the merge kernel may be scheduled now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -167,6 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* pbuf = sm + S::P;
     int* s_lens = reinterpret_cast<int*>(sm + S::LENS);
     int* s_prefix = reinterpret_cast<int*>(sm + S::PREFIX);
+    uint16_t* s_order = reinterpret_cast<uint16_t*>(sm + S::ORDER);
     volatile int* item_q = reinterpret_cast<volatile int*>(sm + S::QUEUE);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BARS);
     uint64_t* full = bars;
@@ -191,37 +216,85 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int B = tc_rows(p);  // rows: <= kTcMaxSeqs (checked on the host)
     const int heads_per_row = tc_per_kvh(p) ? 1 : p.num_kv_heads;
 
-    // Lengths and the exclusive prefix of items per row (a row with a length
-    // outside 1..max_blocks*BS has no items).
+    // Lengths, the exclusive prefix of full-partition items per row and the
+    // rows with a partly filled partition sorted by its length, longest first
+    // (a row with a length outside 1..max_blocks*BS has no items).  Each
+    // thread owns a contiguous chunk of rows; one block-wide scan gives the
+    // full-item prefix and every bucket's offsets, so the order is the same in
+    // every CTA.
     {
+        constexpr int NBK = kTcLenBuckets;
         const int chunk = (B + kTcThreads - 1) / kTcThreads;
         const int s0 = min(B, threadIdx.x * chunk), s1 = min(B, s0 + chunk);
-        int local = 0;
+        auto bucket_of = [&](int L) { return (L % p.partition_size) * NBK / p.partition_size; };
+        auto valid_len = [&](int L) { return L >= 1 && L <= p.max_blocks_per_seq * BS; };
+        int cnt[NBK + 1] = {};  // [0]: full items, [1 + k]: rows in length bucket k
         for (int s = s0; s < s1; ++s) {
             const int L = p.context_lens[s];
             s_lens[s] = L;
-            if (L >= 1 && L <= p.max_blocks_per_seq * BS)
-                local += heads_per_row * ((L + p.partition_size - 1) / p.partition_size);
-        }
-        int incl = local;
+            if (!valid_len(L)) continue;
+            cnt[0] += heads_per_row * (L / p.partition_size);
+            if (L % p.partition_size != 0) {
+                const int k = bucket_of(L);
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
+                for (int kk = 0; kk < NBK; ++kk) cnt[1 + kk] += kk == k;
+            }
         }
-        int* warp_tot = reinterpret_cast<int*>(red_max);
-        if (lane == 31) warp_tot[warp] = incl;
+        int incl[NBK + 1];
+#pragma unroll
+        for (int k = 0; k <= NBK; ++k) {
+            incl[k] = cnt[k];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl[k], off);
+                if (lane >= off) incl[k] += v;
+            }
+        }
+        int* warp_tot = reinterpret_cast<int*>(red_max);  // [warps][NBK + 1]
+        if (lane == 31) {
+#pragma unroll
+            for (int k = 0; k <= NBK; ++k) warp_tot[warp * (NBK + 1) + k] = incl[k];
+        }
         __syncthreads();
-        int base = 0;
-        for (int w = 0; w < warp; ++w) base += warp_tot[w];
-        int run = base + incl - local;
-        for (int s = s0; s < s1; ++s) {
-            s_prefix[s] = run;
-            const int L = s_lens[s];
-            if (L >= 1 && L <= p.max_blocks_per_seq * BS)
-                run += heads_per_row * ((L + p.partition_size - 1) / p.partition_size);
+        int run[NBK + 1], total[NBK + 1];
+#pragma unroll
+        for (int k = 0; k <= NBK; ++k) {
+            int before = 0, all = 0;
+            for (int w = 0; w < kTcThreads / 32; ++w) {
+                const int t = warp_tot[w * (NBK + 1) + k];
+                if (w < warp) before += t;
+                all += t;
+            }
+            run[k] = before + incl[k] - cnt[k];
+            total[k] = all;
         }
-        if (threadIdx.x == kTcThreads - 1) s_prefix[B] = base + incl;
+        // bucket k starts after the rows of the longer buckets k+1 .. NBK-1
+#pragma unroll
+        for (int k = 0; k < NBK; ++k) {
+            int start = 0;
+#pragma unroll
+            for (int k2 = k + 1; k2 < NBK; ++k2) start += total[1 + k2];
+            run[1 + k] += start;
+        }
+        for (int s = s0; s < s1; ++s) {
+            s_prefix[s] = run[0];
+            const int L = s_lens[s];
+            if (!valid_len(L)) continue;
+            run[0] += heads_per_row * (L / p.partition_size);
+            if (L % p.partition_size != 0) {
+                const int k = bucket_of(L);
+#pragma unroll
+                for (int kk = 0; kk < NBK; ++kk)
+                    if (kk == k) s_order[run[1 + kk]++] = static_cast<uint16_t>(s);
+            }
+        }
+        if (threadIdx.x == 0) {
+            int partial = 0;
+#pragma unroll
+            for (int k = 0; k < NBK; ++k) partial += total[1 + k];
+            s_prefix[B] = total[0];
+            s_prefix[B + 1] = partial;
+        }
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
@@ -247,7 +320,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_base_smem;
-    const int total = s_prefix[B];
+    const int total = s_prefix[B] + heads_per_row * s_prefix[B + 1];
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
@@ -286,7 +359,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             ++nclaim;
             if (ci < 0) return false;
-            tc_decode_item(ci, p, s_lens, s_prefix, it);
+            tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
             return true;
         };
         auto table_entry = [&](const TcItem& it) {
@@ -408,7 +481,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ++nread;
             if (!good) return -1;
             if (ci < 0) return 0;
-            tc_decode_item(ci, p, s_lens, s_prefix, it);
+            tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
             return 1;
         };
         auto mma_s = [&](const TcItem& it, int k) {
@@ -534,7 +607,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (named_bar_or(3, 128, !good)) return -1;
             if (tid == 0) mbar_arrive(&item_empty[slot]);
             if (ci < 0) return 0;
-            tc_decode_item(ci, p, s_lens, s_prefix, it);
+            tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
             return 1;
         };
         auto softmax = [&](const TcItem& it, int k) {

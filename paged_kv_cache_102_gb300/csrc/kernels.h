@@ -82,6 +82,7 @@ struct DecodeParams {
 
 struct MergeParams {
     const int32_t* context_lens;
+    int num_seqs;
     int lens_seq_stride;
     int lens_kvh_stride;
     int group;  // query heads per kv head
@@ -147,7 +148,7 @@ cudaError_t launch_quest_select(const QuestSelectParams& p, int dtype, int G, cu
 cudaError_t launch_append(const AppendParams& p, int act, int cache, cudaStream_t stream);
 cudaError_t launch_block_copy(const CopyParams& p, int num_pairs, cudaStream_t stream);
 cudaError_t launch_block_swap(const SwapParams& p, int n, cudaStream_t stream);
-cudaError_t launch_merge(const MergeParams& p, int act, int num_seqs, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, int act, cudaStream_t stream);
 
 // Partition kernel for one (act, cache) pair; returns cudaErrorInvalidValue
 // for a (head_dim, block_size, group) it was not built for.

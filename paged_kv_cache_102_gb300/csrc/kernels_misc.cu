@@ -164,39 +164,123 @@ cudaError_t launch_block_swap(const SwapParams& p, int n, cudaStream_t stream) {
 // Split-K merge.  Each partition p of a sequence left (m_p, l_p, o_p) with
 // o_p already divided by l_p and m_p in log2 units; the full softmax is
 //   out = sum_p w_p o_p / sum_p w_p,  w_p = l_p * 2^(m_p - max_p m_p).
-// One CTA of head_dim threads per (query head, sequence); sequences that fit
-// one partition were written directly by the partition kernel.
+// W warps per (sequence, query head) row (1 when there are enough rows to fill
+// the GPU, else 2, 4 or 8 from the largest partition count), 8 warps per CTA.  Every warp of a row reads the
+// partitions' (m, l) pairs with its lanes in parallel and reduces their max
+// with shuffles; warp j then sums partitions j, j+W, ... over its lane's D/32
+// output channels with independent vector loads, and the row's warps combine
+// their sums through shared memory.  Rows that fit one partition were written
+// directly by the partition kernel.  The kernel is launched as a programmatic
+// dependent of the partition kernel: griddepcontrol.wait returns once that
+// grid has completed and its writes are visible.
 // ---------------------------------------------------------------------------
-template <int ACT>
-__global__ void paged_decode_merge_kernel(MergeParams p) {
-    const int h = blockIdx.x;
-    const int seq = blockIdx.y;
-    const int d = threadIdx.x;
-    const int L = p.context_lens[static_cast<int64_t>(seq) * p.lens_seq_stride + (h / p.group) * p.lens_kvh_stride];
-    if (L < 1 || L > p.max_context) return;  // flagged by the partition kernel
-    const int n_parts = (L + p.partition_size - 1) / p.partition_size;
-    if (n_parts <= 1) return;
-    const size_t row = static_cast<size_t>(seq) * p.num_q_heads + h;
-    const float* ml = p.ws_ml + row * p.max_parts * 2;
-    const float* o = p.ws_o + row * p.max_parts * p.head_dim;
-    float M = -INFINITY;
-    for (int i = 0; i < n_parts; ++i) M = fmaxf(M, ml[2 * i]);
-    float num = 0.f, den = 0.f;
-    for (int i = 0; i < n_parts; ++i) {
-        const float w = ml[2 * i + 1] * exp2f(ml[2 * i] - M);
-        num = fmaf(w, o[static_cast<size_t>(i) * p.head_dim + d], num);
-        den += w;
+constexpr int kMergeWarps = 8;
+
+template <int ACT, int D, int W>
+__global__ void __launch_bounds__(32 * kMergeWarps) paged_decode_merge_kernel(MergeParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    constexpr int V = D / 32;  // channels per lane
+    constexpr int ROWS = kMergeWarps / W;
+    __shared__ float s_acc[W > 1 ? kMergeWarps : 1][D];
+    __shared__ float s_den[kMergeWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = warp % W;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * ROWS + warp / W;
+    bool active = row < static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
+    int n_parts = 0;
+    if (active) {
+        const int seq = static_cast<int>(row / p.num_q_heads), h = static_cast<int>(row % p.num_q_heads);
+        const int L =
+            p.context_lens[static_cast<int64_t>(seq) * p.lens_seq_stride + (h / p.group) * p.lens_kvh_stride];
+        // a bad length was flagged by the partition kernel; one partition was written directly
+        active = L >= 1 && L <= p.max_context;
+        n_parts = active ? (L + p.partition_size - 1) / p.partition_size : 0;
+        active = n_parts > 1;
     }
-    static_cast<uint16_t*>(p.out)[row * p.head_dim + d] = float_to_act<ACT>(num / den);
+    float acc[V] = {};
+    float den = 0.f;
+    if (active) {
+        const float* ml = p.ws_ml + row * p.max_parts * 2;
+        const float* o = p.ws_o + row * p.max_parts * D + lane * V;
+        float M = -INFINITY;
+        for (int i = lane; i < n_parts; i += 32) M = fmaxf(M, ml[2 * i]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        for (int base = 0; base < n_parts; base += 32) {
+            const int i = base + lane;
+            const float w = i < n_parts ? ml[2 * i + 1] * exp2f(ml[2 * i] - M) : 0.f;
+            if (lane % W == sub) den += w;  // base is a multiple of W
+            const int cnt = min(32, n_parts - base);
+#pragma unroll 4
+            for (int k = sub; k < cnt; k += W) {
+                const float wk = __shfl_sync(0xffffffffu, w, k);
+                const float* src = o + static_cast<int64_t>(base + k) * D;
+                if constexpr (V == 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(src);
+                    acc[0] = fmaf(wk, x.x, acc[0]);
+                    acc[1] = fmaf(wk, x.y, acc[1]);
+                    acc[2] = fmaf(wk, x.z, acc[2]);
+                    acc[3] = fmaf(wk, x.w, acc[3]);
+                } else {
+                    const float2 x = *reinterpret_cast<const float2*>(src);
+                    acc[0] = fmaf(wk, x.x, acc[0]);
+                    acc[1] = fmaf(wk, x.y, acc[1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    }
+    if constexpr (W > 1) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) s_acc[warp][lane * V + v] = acc[v];
+        if (lane == 0) s_den[warp] = den;
+        __syncthreads();
+        if (!active || sub != 0) return;
+#pragma unroll
+        for (int j = 1; j < W; ++j) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] += s_acc[warp + j][lane * V + v];
+            den += s_den[warp + j];
+        }
+    }
+    if (!active) return;
+    uint16_t* dst = static_cast<uint16_t*>(p.out) + row * D + lane * V;
+#pragma unroll
+    for (int v = 0; v < V; ++v) dst[v] = float_to_act<ACT>(acc[v] / den);
 }
 
-cudaError_t launch_merge(const MergeParams& p, int act, int num_seqs, cudaStream_t stream) {
-    dim3 grid(p.num_q_heads, num_seqs);
-    if (act == kF16)
-        paged_decode_merge_kernel<kF16><<<grid, p.head_dim, 0, stream>>>(p);
-    else
-        paged_decode_merge_kernel<kBF16><<<grid, p.head_dim, 0, stream>>>(p);
-    return cudaGetLastError();
+template <int ACT, int D, int W>
+cudaError_t merge_one(const MergeParams& p, cudaStream_t stream) {
+    constexpr int ROWS = kMergeWarps / W;
+    const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + ROWS - 1) / ROWS));
+    cfg.blockDim = dim3(32 * kMergeWarps);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, paged_decode_merge_kernel<ACT, D, W>, p);
+}
+
+template <int ACT, int D>
+cudaError_t merge_w(const MergeParams& p, cudaStream_t stream) {
+    // enough rows to fill the GPU with one warp each: no cross-warp combine
+    if (static_cast<int64_t>(p.num_seqs) * p.num_q_heads >= 4096) return merge_one<ACT, D, 1>(p, stream);
+    if (p.max_parts >= 32) return merge_one<ACT, D, 8>(p, stream);
+    if (p.max_parts >= 8) return merge_one<ACT, D, 4>(p, stream);
+    if (p.max_parts >= 4) return merge_one<ACT, D, 2>(p, stream);
+    return merge_one<ACT, D, 1>(p, stream);
+}
+
+cudaError_t launch_merge(const MergeParams& p, int act, cudaStream_t stream) {
+    if (p.num_seqs == 0) return cudaSuccess;
+    if (p.head_dim == 128) return act == kF16 ? merge_w<kF16, 128>(p, stream) : merge_w<kBF16, 128>(p, stream);
+    return act == kF16 ? merge_w<kF16, 64>(p, stream) : merge_w<kBF16, 64>(p, stream);
 }
 
 }  // namespace pkv
