@@ -26,6 +26,8 @@
 // (m, l, o = acc/l) for the split-K merge kernel.
 #pragma once
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "pkv_device.cuh"
 
@@ -180,20 +182,29 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
     const int c = lane % C::LPR;  // 16-byte chunk within the row
     const int h0 = kvh * G;
 
-    float qf[G][C::VEC];
-    {
-        const float kmul = CACHE == kE4M3 ? *p.k_scale : 1.0f;
-        const uint16_t* q = static_cast<const uint16_t*>(p.q) + (static_cast<size_t>(seq) * p.num_q_heads + h0) * D;
+    const float kmul = CACHE == kE4M3 ? *p.k_scale : 1.0f;
+    const float qscale = p.scale_log2 * kmul;
+    const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) + (static_cast<size_t>(seq) * p.num_q_heads + h0) * D;
+
+    // An E4M3 cache takes the mixed-precision path: K and V pairs become
+    // binary16 pairs (exact), q is held in binary16 (exact for a 16-bit value
+    // of magnitude <= 65504, checked per warp), products accumulate in
+    // binary32 with fma.rn.f32.f16, and the scale multiplies the reduced dot
+    // product.  P·V takes the probability rounded to binary16.
+    bool mixed = false;
+    if constexpr (CACHE == kE4M3) {
+        bool fits = true;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
 #pragma unroll
             for (int v = 0; v < C::VEC; v += 8) {
-                const uint4 u = *reinterpret_cast<const uint4*>(q + g * D + c * C::VEC + v);
+                const uint4 u = *reinterpret_cast<const uint4*>(qsrc + g * D + c * C::VEC + v);
                 const uint16_t* e = reinterpret_cast<const uint16_t*>(&u);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) qf[g][v + i] = act_to_float<ACT>(e[i]) * p.scale_log2 * kmul;
+                for (int i = 0; i < 8; ++i) fits = fits && fabsf(act_to_float<ACT>(e[i])) <= 65504.f;
             }
         }
+        mixed = __all_sync(0xffffffffu, fits);
     }
 
     float m[G], l[G], acc[G][C::VEC];
@@ -205,74 +216,137 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
         for (int v = 0; v < C::VEC; ++v) acc[g][v] = 0.f;
     }
 
-    for (int st = 0; st < n_stage; ++st) {
-        const int s = st % C::STAGES;
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (st / C::STAGES) & 1))) {
-            if (lane == 0) {
-                atomicOr(p.err, kErrTimeout);
-                s_failed = 1;
-            }
-            break;
-        }
-        const unsigned char* kb = kbuf + s * C::STAGE_BYTES;
-        const unsigned char* vb = vbuf + s * C::STAGE_BYTES;
-        const int tok0 = tok_begin + st * kStageTokens;
-
-        float sc[C::PASSES][G];
-#pragma unroll
-        for (int pp = 0; pp < C::PASSES; ++pp) {
-            const int tt = warp * C::TW + pp * C::TPP + r;
-            const bool valid = tok0 + tt < tok_end;
-            const uint4 u = *reinterpret_cast<const uint4*>(kb + (tt * D * C::E) + c * 16);
-            float kf[C::VEC];
-            Vec16<CACHE>::to_float(u, kf);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float d = 0.f;
-#pragma unroll
-                for (int v = 0; v < C::VEC; ++v) d = fmaf(qf[g][v], kf[v], d);
-#pragma unroll
-                for (int off = C::LPR / 2; off >= 1; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-                sc[pp][g] = valid ? d : -INFINITY;
-            }
-        }
-
-        float pr[C::PASSES][G];
+    auto consume = [&](auto mixed_tag) {
+        constexpr bool MIX = decltype(mixed_tag)::value;
+        constexpr int QN = MIX ? C::VEC / 2 : C::VEC;
+        // float path: q * scale (log2 units, k_scale folded in); mixed path: binary16 pairs of q
+        float qf[G][MIX ? 1 : C::VEC];
+        uint32_t qh[G][MIX ? QN : 1];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            float mx = sc[0][g];
 #pragma unroll
-            for (int pp = 1; pp < C::PASSES; ++pp) mx = fmaxf(mx, sc[pp][g]);
+            for (int v = 0; v < C::VEC; v += 8) {
+                const uint4 u = *reinterpret_cast<const uint4*>(qsrc + g * D + c * C::VEC + v);
+                const uint16_t* e = reinterpret_cast<const uint16_t*>(&u);
 #pragma unroll
-            for (int off = C::LPR; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_new = fmaxf(m[g], mx);
-            const float alpha = m_new == -INFINITY ? 1.f : exp2f(m[g] - m_new);
-            m[g] = m_new;
-            l[g] *= alpha;
-#pragma unroll
-            for (int v = 0; v < C::VEC; ++v) acc[g][v] *= alpha;
-#pragma unroll
-            for (int pp = 0; pp < C::PASSES; ++pp) {
-                pr[pp][g] = sc[pp][g] == -INFINITY ? 0.f : exp2f(sc[pp][g] - m_new);
-                l[g] += pr[pp][g];
+                for (int i = 0; i < 8; ++i) {
+                    const float x = act_to_float<ACT>(e[i]);
+                    if constexpr (MIX) {
+                        const uint32_t h = __half_as_ushort(__float2half_rn(x));
+                        if (i % 2 == 0) qh[g][(v + i) / 2] = h;
+                        else qh[g][(v + i) / 2] |= h << 16;
+                    } else {
+                        qf[g][v + i] = x * qscale;
+                    }
+                }
             }
         }
 
-#pragma unroll
-        for (int pp = 0; pp < C::PASSES; ++pp) {
-            const int tt = warp * C::TW + pp * C::TPP + r;
-            if (tok0 + tt < tok_end) {
-                const uint4 u = *reinterpret_cast<const uint4*>(vb + (tt * D * C::E) + c * 16);
-                float vf[C::VEC];
-                Vec16<CACHE>::to_float(u, vf);
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int v = 0; v < C::VEC; ++v) acc[g][v] = fmaf(pr[pp][g], vf[v], acc[g][v]);
+        for (int st = 0; st < n_stage; ++st) {
+            const int s = st % C::STAGES;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (st / C::STAGES) & 1))) {
+                if (lane == 0) {
+                    atomicOr(p.err, kErrTimeout);
+                    s_failed = 1;
+                }
+                break;
             }
+            const unsigned char* kb = kbuf + s * C::STAGE_BYTES;
+            const unsigned char* vb = vbuf + s * C::STAGE_BYTES;
+            const int tok0 = tok_begin + st * kStageTokens;
+
+            float sc[C::PASSES][G];
+#pragma unroll
+            for (int pp = 0; pp < C::PASSES; ++pp) {
+                const int tt = warp * C::TW + pp * C::TPP + r;
+                const bool valid = tok0 + tt < tok_end;
+                const uint4 u = *reinterpret_cast<const uint4*>(kb + (tt * D * C::E) + c * 16);
+                if constexpr (MIX) {
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                    uint32_t kh[QN];
+#pragma unroll
+                    for (int i = 0; i < QN; ++i)
+                        kh[i] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i / 2] >> (16 * (i % 2))));
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                        for (int i = 0; i < QN; ++i) fma_f16x2_f32(qh[g][i], kh[i], d0, d1);
+                        float d = d0 + d1;
+#pragma unroll
+                        for (int off = C::LPR / 2; off >= 1; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+                        sc[pp][g] = valid ? d * qscale : -INFINITY;
+                    }
+                } else {
+                    float kf[C::VEC];
+                    Vec16<CACHE>::to_float(u, kf);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        float d = 0.f;
+#pragma unroll
+                        for (int v = 0; v < C::VEC; ++v) d = fmaf(qf[g][v], kf[v], d);
+#pragma unroll
+                        for (int off = C::LPR / 2; off >= 1; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+                        sc[pp][g] = valid ? d : -INFINITY;
+                    }
+                }
+            }
+
+            float pr[C::PASSES][G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float mx = sc[0][g];
+#pragma unroll
+                for (int pp = 1; pp < C::PASSES; ++pp) mx = fmaxf(mx, sc[pp][g]);
+#pragma unroll
+                for (int off = C::LPR; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float m_new = fmaxf(m[g], mx);
+                const float alpha = m_new == -INFINITY ? 1.f : exp2f(m[g] - m_new);
+                m[g] = m_new;
+                l[g] *= alpha;
+#pragma unroll
+                for (int v = 0; v < C::VEC; ++v) acc[g][v] *= alpha;
+#pragma unroll
+                for (int pp = 0; pp < C::PASSES; ++pp) {
+                    pr[pp][g] = sc[pp][g] == -INFINITY ? 0.f : exp2f(sc[pp][g] - m_new);
+                    l[g] += pr[pp][g];
+                }
+            }
+
+#pragma unroll
+            for (int pp = 0; pp < C::PASSES; ++pp) {
+                const int tt = warp * C::TW + pp * C::TPP + r;
+                if (tok0 + tt < tok_end) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(vb + (tt * D * C::E) + c * 16);
+                    if constexpr (MIX) {
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int i = 0; i < QN; ++i) {
+                            const uint32_t vh = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i / 2] >> (16 * (i % 2))));
+#pragma unroll
+                            for (int g = 0; g < G; ++g)
+                                fma_f16s_f32(__half_as_ushort(__float2half_rn(pr[pp][g])), vh, acc[g][2 * i],
+                                             acc[g][2 * i + 1]);
+                        }
+                    } else {
+                        float vf[C::VEC];
+                        Vec16<CACHE>::to_float(u, vf);
+#pragma unroll
+                        for (int g = 0; g < G; ++g)
+#pragma unroll
+                            for (int v = 0; v < C::VEC; ++v) acc[g][v] = fmaf(pr[pp][g], vf[v], acc[g][v]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+    };
+    if constexpr (CACHE == kE4M3) {
+        if (mixed) consume(std::true_type{});
+        else consume(std::false_type{});
+    } else {
+        consume(std::false_type{});
     }
 
     // Merge the token rows of this warp: lanes of equal chunk c hold partial sums.

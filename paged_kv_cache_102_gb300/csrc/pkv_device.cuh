@@ -143,6 +143,36 @@ struct Vec16<kE4M3> {
     }
 };
 
+// E4M3 pair -> binary16 pair (exact: every E4M3 value is a binary16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
+    return d;
+}
+
+// Mixed-precision fused multiply-adds with binary16 sources and binary32
+// accumulators (the product of two binary16 values is exact in binary32):
+// d0 += a.lo * b.lo, d1 += a.hi * b.hi.
+__device__ __forceinline__ void fma_f16x2_f32(uint32_t a, uint32_t b, float& d0, float& d1) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "mov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.f16 %1, ah, bh, %1;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "r"(a), "r"(b));
+}
+
+// d0 += s * b.lo, d1 += s * b.hi (s, b binary16; d0, d1 binary32).
+__device__ __forceinline__ void fma_f16s_f32(uint16_t s, uint32_t b, float& d0, float& d1) {
+    asm("{\n\t.reg .b16 bl, bh;\n\t"
+        "mov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, %2, bl, %0;\n\t"
+        "fma.rn.f32.f16 %1, %2, bh, %1;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "h"(s), "r"(b));
+}
+
 // Activation (16-bit) scalar conversion.
 template <int T>
 __device__ __forceinline__ float act_to_float(uint16_t bits);

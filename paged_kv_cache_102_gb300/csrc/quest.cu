@@ -406,7 +406,7 @@ __device__ __forceinline__ uint32_t bound_key(float f) {
 constexpr int kTopkThreads = 256;
 
 __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(QuestSelectParams p) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int hist[256];
     __shared__ uint32_t warp_scan[kTopkThreads / 32];
     __shared__ int warp_tokens[kTopkThreads / 32];
