@@ -34,6 +34,7 @@
 namespace pkv {
 
 constexpr int kStageTokens = 32;
+constexpr float kRescaleLog2 = 8.0f;  // largest log2 growth of the running max left unrescaled
 constexpr int kConsumerWarps = 4;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 
@@ -300,15 +301,20 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
                 for (int pp = 1; pp < C::PASSES; ++pp) mx = fmaxf(mx, sc[pp][g]);
 #pragma unroll
                 for (int off = C::LPR; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                const float m_new = fmaxf(m[g], mx);
-                const float alpha = m_new == -INFINITY ? 1.f : exp2f(m[g] - m_new);
-                m[g] = m_new;
-                l[g] *= alpha;
+                // Lazy rescaling: the reference max m moves only when the
+                // stage max exceeds it by more than kRescaleLog2 (warp-uniform
+                // test), so probabilities stay below 2^kRescaleLog2 and l and
+                // acc, both relative to m, stay consistent.
+                if (mx > m[g] + kRescaleLog2) {
+                    const float alpha = m[g] == -INFINITY ? 0.f : exp2f(m[g] - mx);
+                    m[g] = mx;
+                    l[g] *= alpha;
 #pragma unroll
-                for (int v = 0; v < C::VEC; ++v) acc[g][v] *= alpha;
+                    for (int v = 0; v < C::VEC; ++v) acc[g][v] *= alpha;
+                }
 #pragma unroll
                 for (int pp = 0; pp < C::PASSES; ++pp) {
-                    pr[pp][g] = sc[pp][g] == -INFINITY ? 0.f : exp2f(sc[pp][g] - m_new);
+                    pr[pp][g] = sc[pp][g] == -INFINITY ? 0.f : exp2f(sc[pp][g] - m[g]);
                     l[g] += pr[pp][g];
                 }
             }
