@@ -141,6 +141,20 @@ def _traffic(workload: str):
         return None
 
 
+def reduce_over_ranks(dist, dev, seconds: float, work: dict):
+    """Replicas share no data: the job's time is the slowest rank's and its
+    work the sum of every rank's (ranks draw different batches).  Returns
+    (max seconds, {key: summed work}); identity without a process group."""
+    if dist is None:
+        return seconds, {k: float(v) for k, v in work.items()}
+    keys = sorted(work)
+    t = torch.tensor([float(seconds)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    w = torch.tensor([float(work[k]) for k in keys], dtype=torch.float64, device=dev)
+    dist.all_reduce(w, op=dist.ReduceOp.SUM)
+    return float(t.item()), dict(zip(keys, w.tolist()))
+
+
 def setup(pkv, W, workload: str, seed: int, dev, batch: int = 0):
     import dataclasses
     wl = W.WORKLOADS[workload]
@@ -269,13 +283,10 @@ def run_native(args):
     ms_total = ev_start.elapsed_time(ev_end)
     dec_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
     clocks = sampler.stop(t_soak, t1) if sampler else None
-    if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total, job = reduce_over_ranks(dist, dev, ms_total, {"bytes": step_bytes, "seqs": B})
 
     ms_step = ms_total / args.steps
-    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    value = job["bytes"] / (ms_step * 1e-3) / 1e9
     peak, peak_src = _peaks()
     dec_avg_ms = statistics.mean(dec_ms)
     kernel_bytes = dec_bytes + (app_bytes if args.fused else 0)  # the fused launch also does the append
@@ -324,13 +335,10 @@ def run_native(args):
         for _ in range(args.steps):
             e2e_step()
         te = (time.perf_counter() - te0) / args.steps
-        if dist:
-            t = torch.tensor([te], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            te = float(t.item())
-        e2e = {"value": round(step_bytes * world / te / 1e9, 2), "unit": "GB/s",
+        te, _ = reduce_over_ranks(dist, dev, te, {})
+        e2e = {"value": round(job["bytes"] / te / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(te * 1e3, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "seq_steps_per_s": round(B * world / te, 1)}
+               "seq_steps_per_s": round(job["seqs"] / te, 1)}
         if not torch.equal(out_h, st["out"].cpu()):
             raise RuntimeError("e2e output differs from the device-resident step")
 
@@ -360,8 +368,8 @@ def run_native(args):
                    "l2": "inputs larger than L2 (K/V read per step %.2f GB vs 129 MB L2)" % (dec_bytes / 1e9),
                    "parallelism": f"replicas x{world} (sequences sharded, no collective)",
                    "kernel_path": args.kernel_path, "fused_append": bool(args.fused)},
-        "pct_of_peak": round(100 * value / peak, 2),
-        "seq_steps_per_s": round(B * world / (ms_step * 1e-3), 1),
+        "pct_of_peak": round(100 * value / (peak * world), 2),  # per GPU
+        "seq_steps_per_s": round(job["seqs"] / (ms_step * 1e-3), 1),
         "bytes_per_step": {"decode": dec_bytes, "append": app_bytes},
         "roofline": {"bound": "hbm",
                      "kernel": ("paged_attention_decode_append" if args.fused else "paged_attention_decode")
