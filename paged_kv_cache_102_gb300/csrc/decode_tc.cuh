@@ -375,36 +375,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             return phys;
         };
-        // Arm one ring stage with tile t of an item; `map` is the K or V tensor map.
+        // Arm one ring stage with tile t of an item; `map` is the K or V tensor
+        // map.  Lane 0 waits for the stage and sets its byte count; lane 2j+h
+        // then loads half h of block j of the tile, so one warp instruction
+        // issues the tile's 2*BPT copies.
         auto issue_tile = [&](const TcItem& it, int phys, int t, const CUtensorMap* map) {
             const int n_blk = (it.n_tok + BS - 1) / BS;
-            int pb[BPT];
-#pragma unroll
-            for (int j = 0; j < BPT; ++j) pb[j] = __shfl_sync(0xffffffffu, phys, (t * BPT + j) & 31);
+            const int j = (lane >> 1) < BPT ? (lane >> 1) : 0;
+            const int half = lane & 1;
+            const int pbj = __shfl_sync(0xffffffffu, phys, (t * BPT + j) & 31);
+            const bool mine = lane < 2 * BPT && t * BPT + j < n_blk && pbj >= 0;
+            const unsigned loads = __ballot_sync(0xffffffffu, mine);
+            const int s = use % NS;
             bool good = true;
             if (lane == 0) {
-                const int s = use % NS;
                 if (use >= NS) good = tc_wait(&empty[s], ((use / NS) - 1) & 1, abort_flag, p.err);
-                if (good) {
-                    uint32_t bytes = 0;
-#pragma unroll
-                    for (int j = 0; j < BPT; ++j)
-                        if (t * BPT + j < n_blk && pb[j] >= 0) bytes += BS * 256;
-                    mbar_arrive_expect_tx(&full[s], bytes);
-                    unsigned char* st = ring + s * kTcStage;
-#pragma unroll
-                    for (int j = 0; j < BPT; ++j) {
-                        if (t * BPT + j < n_blk && pb[j] >= 0) {
-                            const int y = (pb[j] * p.num_kv_heads + it.kvh) * BS;
-                            tc::tma_load_2d(st + j * BS * 128, map, 0, y, &full[s], policy);
-                            tc::tma_load_2d(st + kTcHalf + j * BS * 128, map, 64, y, &full[s], policy);
-                        }
-                    }
-                }
+                if (good) mbar_arrive_expect_tx(&full[s], __popc(loads) * (BS * 128));
             }
             good = __shfl_sync(0xffffffffu, good, 0);
-            if (good) ++use;
-            return good;
+            if (!good) return false;
+            if (mine) {
+                const int y = (pbj * p.num_kv_heads + it.kvh) * BS;
+                tc::tma_load_2d(ring + s * kTcStage + half * kTcHalf + j * BS * 128, map, half * 64, y, &full[s],
+                                policy);
+            }
+            ++use;
+            return true;
         };
         auto issue_q_and_k = [&](const TcItem& it, int phys, int k) {
             bool good = true;
