@@ -139,6 +139,7 @@ struct QuestSelectParams {
     int num_blocks;
     int max_blocks_per_seq;
     int budget_blocks;
+    int group_heads;  // kv heads per bound item (set by launch_quest_select)
 };
 
 cudaError_t launch_quest_minmax(const QuestMetaParams& p, int dtype, cudaStream_t s);

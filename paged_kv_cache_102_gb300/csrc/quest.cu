@@ -12,6 +12,7 @@
 
 #include "kernels.h"
 #include "pkv_device.cuh"
+#include "pkv_tc.cuh"
 
 namespace pkv {
 
@@ -126,267 +127,384 @@ __global__ void __launch_bounds__(256) quest_append_minmax_kernel(QuestAppendPar
     }
 }
 
-// Packed float pairs (Blackwell's two-wide fp32 FMA).
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ float f2_sum(uint64_t v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return lo + hi;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-// Two 16-bit elements (one 32-bit word) -> a packed float pair.
-template <int T>
-__device__ __forceinline__ uint64_t word_to_pair(uint32_t w) {
-    if constexpr (T == kBF16) {
-        return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-    } else {
-        const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w));
-        return f2_pack(t.x, t.y);
-    }
-}
-
-// N (4 or 8) 16-bit elements at a 2N-byte aligned address -> N/2 float pairs.
-template <int T, int N>
-__device__ __forceinline__ void load_pairs(const void* src, uint64_t* f2) {
-    if constexpr (N == 8) {
-        const uint4 u = *reinterpret_cast<const uint4*>(src);
-        f2[0] = word_to_pair<T>(u.x);
-        f2[1] = word_to_pair<T>(u.y);
-        f2[2] = word_to_pair<T>(u.z);
-        f2[3] = word_to_pair<T>(u.w);
-    } else {
-        const uint2 u = *reinterpret_cast<const uint2*>(src);
-        f2[0] = word_to_pair<T>(u.x);
-        f2[1] = word_to_pair<T>(u.y);
-    }
-}
-
-// Sum v[0..N) over the lanes of an aligned group of LPB lanes, leaving lane l
-// with the sum of one value: at each halving step a lane keeps the half of
-// the values picked by its lane bit and receives its partner's copy of that
-// half, so N values need log2(N) exchanges of shrinking width before the
-// plain butterfly finishes the sum.  Afterwards lanes that differ only in the
-// bits LPB/2, LPB/4, ... (the first log2(N) of them) hold different values.
-template <int N, int OFF>
-struct SplitSum {
-    __device__ __forceinline__ static float run(float* v, int lane) {
-        if constexpr (OFF == 0) {
-            return v[0];
-        } else if constexpr (N == 1) {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], OFF);
-            return SplitSum<1, OFF / 2>::run(v, lane);
-        } else {
-            const bool upper = lane & OFF;
-#pragma unroll
-            for (int i = 0; i < N / 2; ++i) {
-                const float send = upper ? v[i] : v[i + N / 2];
-                const float keep = upper ? v[i + N / 2] : v[i];
-                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
-            }
-            return SplitSum<N / 2, OFF / 2>::run(v, lane);
-        }
-    }
-};
-
-// Selection, step 1: the bound of every (sequence, kv head, logical block).
-// For channel c the larger of q*min and q*max is q+ * max + q- * min, with q+
-// and q- the positive and negative parts of q, so a bound is two fused
-// multiply-adds per channel and head.
+// ---- selection, step 1: bounds on the tensor cores --------------------------
+// For channel c the larger of q*min and q*max is q+ * max + q- * min (q+, q-
+// the positive and negative parts of q), so a bound is a dot product of the
+// block's metadata row [min | max] with [q- | q+].  For a group of HG kv
+// heads (HG a power of two dividing Hkv, HG*G <= 32) and BPI = 128/HG blocks,
+// all bounds come from one product
+//     U[128 x N] = A[128 x 2D] * B[N x 2D]^T,
+// A's row r = metadata row of (block r % BPI, kv head r / BPI) as stored,
+// B's row n = [q- | q+] of query head n of the group (rows HG*G .. N-1 zero,
+// N = HG*G rounded up to 16), accumulated in float32 by tcgen05.mma kind::f16
+// with A in tensor memory and B in shared memory (each product of two 16-bit
+// values is exact in float32).  Row r uses only its kv head's G columns; the
+// bound is their max.
 //
-// Persistent CTAs walk a contiguous range of items; an item is 32 logical
-// blocks of one (sequence, kv head) row, items ordered (sequence, kv head,
-// chunk) so a CTA mostly stays on one row and keeps its query registers.
-// Warp 0 reads the item's block ids and bulk-copies each block's min and max
-// rows (4*D contiguous bytes) into a ring of shared-memory stages; warps 1..4
-// compute from shared memory, D/8 lanes per block (D/4 for a group of 8),
-// lane c holding q+ and q- of its 8 (or 4) channels of the group's query
-// heads.  Bounds go to the workspace
-// [B][Hkv][max_blocks] (-inf past the context).
-constexpr int kBItem = 32;
-constexpr int kBConsumerWarps = 4;
-constexpr int kBThreads = 32 * (1 + kBConsumerWarps);
+// An item is one (sequence, kv-head group, chunk of BPI blocks).  Persistent
+// CTAs (one per SM) walk contiguous ranges of items:
+//  warp 0     bulk-copies each block's HG metadata rows (one HG*4*D-byte copy:
+//             the Hkv rows of a physical block are contiguous) into a ring of
+//             staging stages, blocks 16 bytes apart beyond their rows; block
+//             ids are fetched one item ahead.
+//  warps 1-4  the warp owning tensor-memory lanes 32w'..32w'+31 loads rows
+//             32w'.. of the item from staging (row-major reads; consecutive
+//             rows are different blocks, so a quarter warp hits distinct
+//             banks) and stores them into one of two A buffers in tensor
+//             memory (tcgen05.st, 32 columns per instruction); rewrites B when
+//             the (sequence, group) changes; frees the stage.
+//  warp 5     allocates 512 tensor-memory columns (A: 2 x 128, D: 2 x 32) and
+//             issues the 2D/16 MMAs of an item.
+//  warps 6-9  thread i reads row i of the D buffer, takes the max over its kv
+//             head's G columns and stores the bound; rows past the context or
+//             with a bad block id get -inf.
+// Bounds go to the workspace [B][Hkv][max_blocks].  Every barrier wait is
+// bounded; a timeout stops the CTA's roles, which drain their copies and
+// MMAs before the tensor memory is freed.
+constexpr int kQRows = 128;
+constexpr int kQTranscribeWarps = 4;
+constexpr int kQMmaWarp = 1 + kQTranscribeWarps;
+constexpr int kQThreads = 32 * (kQMmaWarp + 1 + 4);
+constexpr int kQMaxN = 32;
+constexpr int kQTmemCols = 512;
+constexpr int kQTmemD = 256;  // first D column; A buffers at 0 and 128
+constexpr int kQFetchAhead = 3;  // items whose lengths and block ids are in flight
 
 template <int D>
-struct BoundsCfg {
-    static constexpr int kSlotBytes = 4 * D;  // min row then max row
-    static constexpr int kStageBytes = kBItem * kSlotBytes;
-    static constexpr int kStages = 65536 / kStageBytes < 4 ? 4 : (65536 / kStageBytes > 8 ? 8 : 65536 / kStageBytes);
-    static constexpr int kSmem = kStages * kStageBytes;
+struct QBoundsCfg {
+    static constexpr int KCH = 2 * D / 8;               // 16-byte chunks per metadata row
+    static constexpr int ROW = 4 * D;                   // bytes per metadata row
+    static constexpr int SBO = KCH * 128;               // bytes between 8-row groups of B
+    static constexpr int STG = kQRows * ROW + kQRows * 16;  // one staging stage (blocks padded by 16 bytes)
+    static constexpr int B_BYTES = kQMaxN * ROW;
+    static constexpr int NSTG_FIT = (224 * 1024 - B_BYTES) / STG;
+    static constexpr int NSTG = NSTG_FIT > 4 ? 4 : NSTG_FIT;
+    static constexpr int SMEM = NSTG * STG + B_BYTES + 128;  // + room to align the base
+    static_assert(NSTG >= 2, "at least two staging stages");
+    static_assert(KCH * 4 <= 128, "a row fits one 128-column A buffer");
 };
 
-template <int T, int D, int G>
-__global__ void __launch_bounds__(kBThreads, 3) quest_bounds_kernel(QuestSelectParams p, int64_t num_items) {
-    using Cfg = BoundsCfg<D>;
-    constexpr int S = Cfg::kStages;
-    constexpr int CPL = G >= 8 ? 4 : 8;                    // channels per lane
-    constexpr int LPB = D / CPL;                           // lanes per block
-    constexpr int PER_PASS = 32 * kBConsumerWarps / LPB;   // blocks per consumer pass
-    static_assert(G <= LPB, "the split sum leaves one head per lane");
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint64_t full_bar[S], empty_bar[S];
-    __shared__ unsigned valid_mask[S];
-    __shared__ int abort_flag;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chunks = (p.max_blocks_per_seq + kBItem - 1) / kBItem;
-    const int64_t begin = num_items * blockIdx.x / gridDim.x;
-    const int64_t end = num_items * (blockIdx.x + 1) / gridDim.x;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < S; ++i) {
-            mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], kBConsumerWarps);
+// Bounded wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool q_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            *abort_flag = 1;
+            return false;
         }
-        abort_flag = 0;
+    }
+    return true;
+}
+
+// q+ and q- of eight 16-bit values, by their sign bits (exact).
+__device__ __forceinline__ void split_signs(const uint4& u, uint4& pos, uint4& neg) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t pw[4], nw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t m = ((w[i] >> 15) & 0x00010001u) * 0xffffu;  // all ones in each negative half
+        nw[i] = w[i] & m;
+        pw[i] = w[i] & ~m;
+    }
+    pos = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+    neg = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+}
+
+template <int T, int D, int G>
+__global__ void __launch_bounds__(kQThreads, 1) quest_bounds_kernel(QuestSelectParams p, int64_t num_items) {
+    using Cfg = QBoundsCfg<D>;
+    constexpr int NSTG = Cfg::NSTG;
+    constexpr int KS = 2 * D / 16;  // MMA k-steps of 16 elements (8 tensor-memory columns each)
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ uint64_t full[NSTG], empty[NSTG], a_full[2], a_free[2], d_full[2], d_free[2], final_bar;
+    __shared__ unsigned valid_mask[NSTG][kQRows / 32];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_flag_s;
+    volatile int* abort_flag = &abort_flag_s;
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 127) & ~uintptr_t(127));
+    unsigned char* staging = sm;
+    unsigned char* Btile = sm + NSTG * Cfg::STG;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int HG = p.group_heads;                 // kv heads per item
+    const int BPI = kQRows / HG;                  // blocks per item
+    const int SB = HG * Cfg::ROW + 16;            // staging bytes per block
+    const int HGG = HG * G;                       // query heads per item
+    const int N = (HGG + 15) / 16 * 16;           // MMA N
+    const int groups = p.num_kv_heads / HG;
+    const int chunks = (p.max_blocks_per_seq + BPI - 1) / BPI;
+    const int64_t begin = num_items * blockIdx.x / gridDim.x;
+    const int count = static_cast<int>(num_items * (blockIdx.x + 1) / gridDim.x - begin);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTG; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kQTranscribeWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&a_full[i], kQTranscribeWarps);
+            mbar_init(&a_free[i], 1);
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_free[i], 4);
+        }
+        mbar_init(&final_bar, 1);
+        abort_flag_s = 0;
         mbar_init_fence();
     }
+    if (warp == kQMmaWarp) {
+        tc::tmem_alloc(&tmem_base_s, kQTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
     __syncthreads();
-    auto item_coords = [&](int64_t it, int& seq, int& kvh, int& j0) {
-        j0 = static_cast<int>(it % chunks) * kBItem;
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base_s;
+    // item -> (sequence, kv-head group, first block)
+    auto coords = [&](int i, int& seq, int& kvg, int& j0) {
+        const int64_t it = begin + i;
+        j0 = static_cast<int>(it % chunks) * BPI;
         const int64_t r = it / chunks;
-        kvh = static_cast<int>(r % p.num_kv_heads);
-        seq = static_cast<int>(r / p.num_kv_heads);
+        kvg = static_cast<int>(r % groups);
+        seq = static_cast<int>(r / groups);
     };
+    auto nblocks_of = [&](int L) {
+        return L >= 1 && L <= p.max_blocks_per_seq * p.block_size ? (L + p.block_size - 1) / p.block_size : 0;
+    };
+
     if (warp == 0) {
-        // Block ids (and context lengths) are fetched S items ahead, one
-        // register slot per stage, so the table reads overlap the copies.
+        // ------------------------------------------------------------- producer
+        // lane l copies blocks l, l+32, ... of the item.  Lengths and block ids
+        // are loaded kQFetchAhead items ahead, in rotating registers (table
+        // entries read for every j < max_blocks, checked against the length
+        // when used).
         const uint64_t policy = l2_policy_evict_first();
-        auto fetch = [&](int64_t it, int& len, int& blk) {
+        const unsigned char* kmeta = static_cast<const unsigned char*>(p.kmeta);
+        const uint32_t copy_bytes = HG * Cfg::ROW;
+        constexpr int BPL = kQRows / 32;  // most blocks per lane (HG = 1)
+        int pf_len[kQFetchAhead], pf_blk[kQFetchAhead][BPL];
+        auto fetch = [&](int i, int& len, int* blks) {
             len = 0;
-            blk = -1;
-            if (it >= end) return;
-            int seq, kvh, j0;
-            item_coords(it, seq, kvh, j0);
+            if (i >= count) return;
+            int seq, kvg, j0;
+            coords(i, seq, kvg, j0);
             len = p.context_lens[seq];
-            if (j0 + lane < p.max_blocks_per_seq)
-                blk = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks_per_seq + j0 + lane];
+#pragma unroll
+            for (int u = 0; u < BPL; ++u) {
+                const int jl = u * 32 + lane, j = j0 + jl;
+                blks[u] = jl < BPI && j < p.max_blocks_per_seq
+                              ? p.block_tables[static_cast<int64_t>(seq) * p.max_blocks_per_seq + j]
+                              : -1;
+            }
         };
-        int pf_len[S], pf_blk[S];
 #pragma unroll
-        for (int k = 0; k < S; ++k) fetch(begin + k, pf_len[k], pf_blk[k]);
-        int n = 0;
-        bool stop = false;
-        for (int64_t base = begin; base < end && !stop; base += S) {
+        for (int k = 0; k < kQFetchAhead; ++k) fetch(k, pf_len[k], pf_blk[k]);
+        // one item: wait for its stage, check its block ids, refill the fetch
+        // slot, issue its copies; false on an abort
+        auto produce = [&](int i, int& len, int* pblk) {
+            const int s = i % NSTG;
+            if (i >= NSTG &&
+                !__all_sync(0xffffffffu, q_wait(&empty[s], ((i / NSTG) - 1) & 1, abort_flag, p.err)))
+                return false;
+            int seq, kvg, j0;
+            coords(i, seq, kvg, j0);
+            const int nblk = nblocks_of(len);
+            int blk[BPL];
+            unsigned ncopies = 0;
 #pragma unroll
-            for (int k = 0; k < S; ++k) {
-                const int64_t it = base + k;
-                if (it >= end) break;
-                if (n >= S && !mbar_wait(&empty_bar[k], ((n / S) - 1) & 1)) {
-                    if (lane == 0) {
-                        atomicOr(p.err, kErrTimeout);
-                        abort_flag = 1;
-                    }
-                    stop = true;
-                    break;
-                }
-                int seq, kvh, j0;
-                item_coords(it, seq, kvh, j0);
-                const int L = pf_len[k];
-                const bool len_ok = L >= 1 && L <= p.max_blocks_per_seq * p.block_size;
-                const int nblk = len_ok ? (L + p.block_size - 1) / p.block_size : 0;
-                int blk = -1;
-                if (j0 + lane < nblk) {
-                    blk = pf_blk[k];
-                    if (blk < 0 || blk >= p.num_blocks) {
+            for (int u = 0; u < BPL; ++u) {
+                const int jl = u * 32 + lane, j = j0 + jl;
+                blk[u] = -1;
+                if (jl < BPI && j < nblk) {
+                    blk[u] = pblk[u];
+                    if (blk[u] < 0 || blk[u] >= p.num_blocks) {
                         atomicOr(p.err, kErrBadBlock);
-                        blk = -1;
+                        blk[u] = -1;
                     }
                 }
-                fetch(it + S, pf_len[k], pf_blk[k]);
-                const unsigned m = __ballot_sync(0xffffffffu, blk >= 0);
-                if (lane == 0) {
-                    valid_mask[k] = m;
-                    mbar_arrive_expect_tx(&full_bar[k], __popc(m) * Cfg::kSlotBytes);
+                ncopies += __popc(__ballot_sync(0xffffffffu, blk[u] >= 0));
+            }
+            // valid rows: row r is valid when its block r % BPI is
+            for (int w = 0; w < kQRows / 32; ++w) {
+                const int jl = (w * 32 + lane) % BPI;
+                int b = __shfl_sync(0xffffffffu, blk[0], jl & 31);
+#pragma unroll
+                for (int u = 1; u < BPL; ++u) {
+                    const int bu = __shfl_sync(0xffffffffu, blk[u], jl & 31);
+                    if ((jl >> 5) == u) b = bu;
                 }
-                __syncwarp();
-                if (blk >= 0)
-                    bulk_copy_g2s(smem + k * Cfg::kStageBytes + lane * Cfg::kSlotBytes,
-                                  static_cast<const uint16_t*>(p.kmeta) +
-                                      (static_cast<int64_t>(blk) * p.num_kv_heads + kvh) * 2 * D,
-                                  Cfg::kSlotBytes, &full_bar[k], policy);
-                ++n;
+                const unsigned m = __ballot_sync(0xffffffffu, b >= 0);
+                if (lane == 0) valid_mask[s][w] = m;
+            }
+            fetch(i + kQFetchAhead, len, pblk);
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], ncopies * copy_bytes);
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < BPL; ++u)
+                if (blk[u] >= 0)
+                    bulk_copy_g2s(staging + s * Cfg::STG + (u * 32 + lane) * SB,
+                                  kmeta + (static_cast<int64_t>(blk[u]) * p.num_kv_heads + kvg * HG) * Cfg::ROW,
+                                  copy_bytes, &full[s], policy);
+            return true;
+        };
+        int i = 0;
+        bool ok = true;
+        for (int base = 0; base < count && ok; base += kQFetchAhead) {
+#pragma unroll
+            for (int k = 0; k < kQFetchAhead; ++k) {  // fetch slot k holds item base + k
+                if (base + k >= count || !(ok = produce(base + k, pf_len[k], pf_blk[k]))) break;
+                i = base + k + 1;
             }
         }
         // let every copy this warp issued land before the CTA can exit
-        for (int k = n - 1; k >= 0 && k >= n - S; --k)
-            if (!mbar_wait(&full_bar[k % S], (k / S) & 1) && lane == 0) atomicOr(p.err, kErrTimeout);
-        return;
-    }
-    const int ct = threadIdx.x - 32;
-    const int c = ct % LPB, grp = ct / LPB;
-    uint64_t qp[G][CPL / 2], qn[G][CPL / 2];
-    int64_t q_row = -1;
-    int n = 0;
-    for (int64_t it = begin; it < end; ++it, ++n) {
-        const int s = n % S;
-        if (!mbar_wait(&full_bar[s], (n / S) & 1)) {
-            if (lane == 0) atomicOr(p.err, kErrTimeout);
-            break;
-        }
-        if (abort_flag) break;
-        int seq, kvh, j0;
-        item_coords(it, seq, kvh, j0);
-        const int64_t row = static_cast<int64_t>(seq) * p.num_kv_heads + kvh;
-        if (row != q_row) {
-            q_row = row;
-            const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) +
-                                   (static_cast<int64_t>(seq) * p.num_q_heads + kvh * G) * D + c * CPL;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                uint64_t f2[CPL / 2];
-                load_pairs<T, CPL>(qsrc + g * D, f2);
-#pragma unroll
-                for (int i = 0; i < CPL / 2; ++i) {
-                    float lo, hi;
-                    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(f2[i]));
-                    qp[g][i] = f2_pack(fmaxf(lo, 0.f), fmaxf(hi, 0.f));
-                    qn[g][i] = f2_pack(fminf(lo, 0.f), fminf(hi, 0.f));
-                }
+        for (int k = i - 1; k >= 0 && k >= i - NSTG; --k)
+            if (!mbar_wait(&full[k % NSTG], (k / NSTG) & 1) && lane == 0) atomicOr(p.err, kErrTimeout);
+    } else if (warp <= kQTranscribeWarps) {
+        // ----------------------------------------------------------- transcribe
+        const int quad = warp & 3;            // tensor-memory lanes 32*quad .. 32*quad+31
+        const int r = quad * 32 + lane;       // row of the item
+        const int t = threadIdx.x - 32;       // 0..127, for the B rows
+        const int h = r / BPI, jl = r % BPI;  // kv head within the group, block within the item
+        for (int i = 0; i < count; ++i) {
+            const int s = i % NSTG, ab = i & 1;
+            int seq, kvg, j0;
+            coords(i, seq, kvg, j0);
+            bool same = false;
+            if (i >= 1) {
+                int ps, pg, pj;
+                coords(i - 1, ps, pg, pj);
+                same = ps == seq && pg == kvg;
             }
-        }
-        const unsigned m = valid_mask[s];
-        float* out = p.bounds + row * p.max_blocks_per_seq;
-        const unsigned char* stage = smem + s * Cfg::kStageBytes;
-#pragma unroll
-        for (int pass = 0; pass < kBItem / PER_PASS; ++pass) {
-            const int slot = pass * PER_PASS + grp;
-            float best = -INFINITY;
-            if (m != 0) {  // uniform over the CTA
-                const bool live = (m >> slot) & 1u;
-                uint64_t a[CPL / 2], b[CPL / 2];
-                const unsigned char* src = stage + (live ? slot : 0) * Cfg::kSlotBytes + c * CPL * 2;
-                load_pairs<T, CPL>(src, a);
-                load_pairs<T, CPL>(src + 2 * D, b);
-                float v[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    uint64_t acc = f2_fma(qp[g][0], b[0], 0ull);
-                    acc = f2_fma(qn[g][0], a[0], acc);
-#pragma unroll
-                    for (int i = 1; i < CPL / 2; ++i) {
-                        acc = f2_fma(qp[g][i], b[i], acc);
-                        acc = f2_fma(qn[g][i], a[i], acc);
+            if (!same) {
+                // B = [q- | q+] of the group's query heads (rows HGG..N-1 zero),
+                // written before this item's metadata arrives; the previous
+                // item's MMAs read B, so they must have completed
+                if (i >= 1 &&
+                    !__all_sync(0xffffffffu, q_wait(&a_free[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, p.err)))
+                    break;
+                const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
+                                       (static_cast<int64_t>(seq) * p.num_q_heads + kvg * HGG) * D;
+                for (int idx = t; idx < N * Cfg::KCH; idx += 32 * kQTranscribeWarps) {
+                    const int n = idx / Cfg::KCH, c = idx % Cfg::KCH;
+                    uint4 val = make_uint4(0, 0, 0, 0);
+                    if (n < HGG) {
+                        const bool positive = c >= Cfg::KCH / 2;
+                        const int cc = positive ? c - Cfg::KCH / 2 : c;
+                        uint4 pos, neg;
+                        split_signs(*reinterpret_cast<const uint4*>(qrow + n * D + cc * 8), pos, neg);
+                        val = positive ? pos : neg;
                     }
-                    v[g] = f2_sum(acc);
+                    *reinterpret_cast<uint4*>(Btile + (n / 8) * Cfg::SBO + c * 128 + (n % 8) * 16) = val;
                 }
-                best = SplitSum<G, LPB / 2>::run(v, lane);
-#pragma unroll
-                for (int off = LPB / 2; off > LPB / 2 / G; off >>= 1)
-                    best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
-                if (!live) best = -INFINITY;
+                tc::fence_proxy_async_smem();
             }
-            const int j = j0 + slot;
-            if (c == 0 && j < p.max_blocks_per_seq) out[j] = best;
+            if (!__all_sync(0xffffffffu, q_wait(&full[s], (i / NSTG) & 1, abort_flag, p.err))) break;
+            if (i >= 2 && !__all_sync(0xffffffffu, q_wait(&a_free[ab], ((i >> 1) - 1) & 1, abort_flag, p.err)))
+                break;
+            const bool valid = (valid_mask[s][r >> 5] >> (r & 31)) & 1u;
+            const unsigned char* src = staging + s * Cfg::STG + jl * SB + h * Cfg::ROW;
+            const uint32_t a_col = tmem + (static_cast<uint32_t>(quad * 32) << 16) + ab * 128;
+#pragma unroll
+            for (int g = 0; g < Cfg::KCH / 8; ++g) {  // 128 bytes = 32 columns per store
+                uint32_t w[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 u = valid ? *reinterpret_cast<const uint4*>(src + (g * 8 + c) * 16) : make_uint4(0, 0, 0, 0);
+                    w[4 * c] = u.x;
+                    w[4 * c + 1] = u.y;
+                    w[4 * c + 2] = u.z;
+                    w[4 * c + 3] = u.w;
+                }
+                tc::tmem_st32(a_col + g * 32, w);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&a_full[ab]);
+                mbar_arrive(&empty[s]);
+            }
+        }
+    } else if (warp == kQMmaWarp) {
+        // ------------------------------------------------------------------ MMA
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_f16(kQRows, N, T == kBF16, false, false);
+            const uint32_t b0 = smem_addr(Btile);
+            for (int i = 0; i < count; ++i) {
+                const int ab = i & 1;
+                if (!q_wait(&a_full[ab], (i >> 1) & 1, abort_flag, p.err)) break;
+                if (i >= 2 && !q_wait(&d_free[ab], ((i >> 1) - 1) & 1, abort_flag, p.err)) break;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks)
+                    tc::mma_f16_ts(tmem + kQTmemD + ab * kQMaxN, tmem + ab * 128 + ks * 8,
+                                   tc::desc_noswizzle(b0 + ks * 256, 128, Cfg::SBO), idesc, ks > 0 ? 1u : 0u);
+                tc::commit(&d_full[ab]);
+                tc::commit(&a_free[ab]);
+            }
+            // every MMA this thread issued completes before the tensor memory is freed
+            tc::commit(&final_bar);
+            if (!mbar_wait(&final_bar, 0)) atomicOr(p.err, kErrTimeout);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
+    } else {
+        // ------------------------------------------------------------- epilogue
+        // the row's length and block id load kQFetchAhead items ahead
+        const int quad = warp & 3;  // tensor-memory lanes 32*quad .. 32*quad+31
+        const int R = quad * 32 + lane;
+        const int h = R / BPI, jl = R % BPI;
+        int pf_len[kQFetchAhead], pf_blk[kQFetchAhead];
+        auto fetch = [&](int i, int& len, int& blk) {
+            len = 0;
+            blk = -1;
+            if (i >= count) return;
+            int seq, kvg, j0;
+            coords(i, seq, kvg, j0);
+            len = p.context_lens[seq];
+            if (j0 + jl < p.max_blocks_per_seq)
+                blk = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks_per_seq + j0 + jl];
+        };
+#pragma unroll
+        for (int k = 0; k < kQFetchAhead; ++k) fetch(k, pf_len[k], pf_blk[k]);
+        auto finish = [&](int i, int& len, int& pblk) {
+            const int b = i & 1;
+            int seq, kvg, j0;
+            coords(i, seq, kvg, j0);
+            const int j = j0 + jl;
+            const bool valid = j < nblocks_of(len) && pblk >= 0 && pblk < p.num_blocks;
+            fetch(i + kQFetchAhead, len, pblk);
+            if (!__all_sync(0xffffffffu, q_wait(&d_full[b], (i >> 1) & 1, abort_flag, p.err))) return false;
+            tc::fence_after_sync();
+            float best = -INFINITY;
+            for (int c0 = 0; c0 < N; c0 += 16) {  // columns h*G .. h*G+G-1 are this row's heads
+                float v[16];
+                tc::TmemLd<16>::load(tmem + (static_cast<uint32_t>(quad * 32) << 16) + kQTmemD + b * kQMaxN + c0,
+                                     v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    if (c0 + k >= h * G && c0 + k < h * G + G) best = fmaxf(best, v[k]);
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&d_free[b]);
+            if (j < p.max_blocks_per_seq)
+                p.bounds[(static_cast<int64_t>(seq) * p.num_kv_heads + kvg * HG + h) * p.max_blocks_per_seq + j] =
+                    valid ? best : -INFINITY;
+            return true;
+        };
+        bool ok = true;
+        for (int base = 0; base < count && ok; base += kQFetchAhead) {
+#pragma unroll
+            for (int k = 0; k < kQFetchAhead; ++k)  // fetch slot k holds item base + k
+                if (base + k >= count || !(ok = finish(base + k, pf_len[k], pf_blk[k]))) break;
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kQMmaWarp) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kQTmemCols);
     }
 }
 
@@ -555,9 +673,10 @@ cudaError_t launch_quest_append_minmax(const QuestAppendParams& p, int dtype, cu
 namespace {
 template <int T, int D, int G>
 cudaError_t bounds_one(const QuestSelectParams& p, cudaStream_t s) {
-    const int64_t items = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads *
-                          ((p.max_blocks_per_seq + kBItem - 1) / kBItem);
-    constexpr int smem = BoundsCfg<D>::kSmem;
+    const int bpi = kQRows / p.group_heads;
+    const int64_t items = static_cast<int64_t>(p.num_seqs) * (p.num_kv_heads / p.group_heads) *
+                          ((p.max_blocks_per_seq + bpi - 1) / bpi);
+    constexpr int smem = QBoundsCfg<D>::SMEM;
     static bool configured[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -570,9 +689,8 @@ cudaError_t bounds_one(const QuestSelectParams& p, cudaStream_t s) {
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int64_t want = static_cast<int64_t>(sms) * 3;
-    const int grid = static_cast<int>(items < want ? items : want);
-    quest_bounds_kernel<T, D, G><<<grid, kBThreads, smem, s>>>(p, items);
+    const int grid = static_cast<int>(items < sms ? items : sms);
+    quest_bounds_kernel<T, D, G><<<grid, kQThreads, smem, s>>>(p, items);
     return cudaGetLastError();
 }
 template <int T, int D>
@@ -587,8 +705,14 @@ cudaError_t bounds_g(const QuestSelectParams& p, int G, cudaStream_t s) {
 }
 }  // namespace
 
-cudaError_t launch_quest_select(const QuestSelectParams& p, int dtype, int G, cudaStream_t s) {
-    if (p.num_seqs == 0) return cudaSuccess;
+cudaError_t launch_quest_select(const QuestSelectParams& p_in, int dtype, int G, cudaStream_t s) {
+    if (p_in.num_seqs == 0) return cudaSuccess;
+    // kv heads per bound item: the largest power of two dividing Hkv with at
+    // most 32 query heads (the MMA's N) and at most 128 rows
+    QuestSelectParams p = p_in;
+    int hg = 1;
+    while (p.num_kv_heads % (2 * hg) == 0 && 2 * hg * G <= kQMaxN && 2 * hg <= kQRows) hg *= 2;
+    p.group_heads = hg;
     cudaError_t e;
     if (dtype == kBF16)
         e = p.head_dim == 128 ? bounds_g<kBF16, 128>(p, G, s) : bounds_g<kBF16, 64>(p, G, s);
