@@ -360,6 +360,17 @@ const char* pkv_last_error(void);
  */
 int pkv_device_error(int* bits, int reset, void* stream);
 
+/*
+ * pkv_selftest_wait_timeout -- check of the kernels' bounded waits.  Launches
+ * one CTA that waits, through the same bounded-wait routine the kernels use,
+ * on a shared-memory barrier that nothing ever arrives at, with a limit of
+ * limit_us microseconds (1 .. 2,000,000) instead of the kernels' 2 s.  The
+ * wait gives up, the kernel sets PKV_DEV_WAIT_TIMEOUT in the device error word
+ * (read it with pkv_device_error) and returns; the context stays usable.
+ * Returns PKV_OK, PKV_ERR_INVALID (limit out of range) or PKV_ERR_CUDA.
+ */
+int pkv_selftest_wait_timeout(int limit_us, void* stream);
+
 /* Library ABI version (major*100 + minor). */
 int pkv_version(void);
 

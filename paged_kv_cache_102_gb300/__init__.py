@@ -289,6 +289,13 @@ def device_error(reset: bool = True, stream=None, device=None) -> int:
     return bits.value
 
 
+def selftest_wait_timeout(limit_us: int = 1000, stream=None, device=None) -> None:
+    """Run the bounded-wait check kernel (a wait on a barrier nothing arrives
+    at, given up after limit_us); read the outcome with device_error()."""
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    _native.call("pkv_selftest_wait_timeout", int(limit_us), _stream(stream, device))
+
+
 class BlockManager:
     """Host-side block allocator (C++ in libpagedkv.so): FIFO free list,
     per-block reference counts, copy-on-write of a shared last block."""

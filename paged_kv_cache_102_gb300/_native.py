@@ -43,6 +43,7 @@ SIGNATURES = {
     "pkv_last_error": (ctypes.c_char_p, []),
     "pkv_device_error": (I32, [P, I32, P]),
     "pkv_version": (I32, []),
+    "pkv_selftest_wait_timeout": (I32, [I32, P]),
     "pkv_set_kernel_path": (I32, [I32]),
     "pkv_bm_create": (P, [I32, I32, P, I32]),
     "pkv_bm_destroy": (None, [P]),

@@ -62,6 +62,16 @@ const char* pkv_last_error(void) { return t_last_error.c_str(); }
 
 int pkv_version(void) { return 100; }
 
+int pkv_selftest_wait_timeout(int limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 2000000)
+        return fail(PKV_ERR_INVALID, "pkv_selftest_wait_timeout: limit_us must be in 1 .. 2,000,000");
+    int* err = device_error_word();
+    if (!err) return fail(PKV_ERR_CUDA, "pkv_selftest_wait_timeout: cannot resolve the device error word");
+    const cudaError_t e =
+        launch_selftest_wait(static_cast<uint64_t>(limit_us) * 1000u, err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail("pkv_selftest_wait_timeout: launch", e);
+}
+
 int pkv_set_kernel_path(int path) {
     if (path < PKV_PATH_AUTO || path > PKV_PATH_TENSOR_2CTA) return -1;
     return g_kernel_path.exchange(path);

@@ -150,6 +150,7 @@ cudaError_t launch_append(const AppendParams& p, int act, int cache, cudaStream_
 cudaError_t launch_block_copy(const CopyParams& p, int num_pairs, cudaStream_t stream);
 cudaError_t launch_block_swap(const SwapParams& p, int n, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int act, cudaStream_t stream);
+cudaError_t launch_selftest_wait(uint64_t limit_ns, int* err, cudaStream_t stream);
 
 // Partition kernel for one (act, cache) pair; returns cudaErrorInvalidValue
 // for a (head_dim, block_size, group) it was not built for.

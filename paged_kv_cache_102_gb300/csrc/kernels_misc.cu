@@ -277,6 +277,23 @@ cudaError_t merge_w(const MergeParams& p, cudaStream_t stream) {
     return merge_one<ACT, D, 1>(p, stream);
 }
 
+// Bounded-wait check: nothing arrives on the barrier, so the wait must give
+// up after limit_ns and report kErrTimeout.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, int* err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait_for(&bar, 0, limit_ns)) atomicOr(err, kErrTimeout);
+}
+
+cudaError_t launch_selftest_wait(uint64_t limit_ns, int* err, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_merge(const MergeParams& p, int act, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
     if (p.head_dim == 128) return act == kF16 ? merge_w<kF16, 128>(p, stream) : merge_w<kBF16, 128>(p, stream);

@@ -187,3 +187,44 @@ def test_swap_out_in_matches_oracle(pkv_lib, seed):
             (live if s in live else out).remove(s)
         assert list(bm.free_list()) == ref.free
         assert [bm.ref_count(b) for b in range(NB)] == ref.ref
+
+
+def _snapshot(bm, ids, NB):
+    t, lens = bm.tables(ids)
+    return (t.tolist(), lens.tolist(), list(bm.free_list()), [bm.ref_count(b) for b in range(NB)])
+
+
+def test_pool_exhausted_mid_step_changes_nothing(pkv_lib):
+    """A batched append that runs out of blocks part-way fails as a whole: no
+    slot is handed out, and tables, lengths, free list and reference counts
+    stay as they were (host-side fault injection: the pool empties mid-step)."""
+    NB, bs = 4, 4
+    bm = pkv_lib.BlockManager(NB, bs)
+    bm.add_sequence(1, 8)  # two full blocks
+    bm.add_sequence(2, 4)  # one full block; one block left
+    before = _snapshot(bm, [1, 2], NB)
+    with pytest.raises(pkv_lib.OutOfBlocks):
+        bm.append_slots([1, 2])  # each needs a fresh block, only one is free
+    assert _snapshot(bm, [1, 2], NB) == before
+    slots, copies = bm.append_slots([1])  # the pool still serves a step that fits
+    assert len(slots) == 1 and len(copies) == 0 and bm.num_free == 0
+
+
+def test_copy_on_write_without_a_free_block_changes_nothing(pkv_lib):
+    """The last block of a forked sequence is shared and partly filled; the
+    child's write needs a copy, the pool is empty, so the step fails and the
+    shared block keeps its reference count of 2."""
+    NB, bs = 3, 4
+    bm = pkv_lib.BlockManager(NB, bs)
+    bm.add_sequence(1, 6)  # blocks: one full, one partly filled
+    bm.fork(1, 2)
+    bm.add_sequence(3, 4)  # takes the last free block
+    before = _snapshot(bm, [1, 2, 3], NB)
+    shared = before[0][0][1]
+    assert bm.ref_count(shared) == 2 and bm.num_free == 0
+    with pytest.raises(pkv_lib.OutOfBlocks):
+        bm.append_slots([2])
+    assert _snapshot(bm, [1, 2, 3], NB) == before
+    bm.free_sequence(3)  # a block comes back; now the copy succeeds
+    slots, copies = bm.append_slots([2])
+    assert len(copies) == 1 and copies[0][0] == shared and bm.ref_count(shared) == 1

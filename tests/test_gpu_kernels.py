@@ -324,3 +324,24 @@ def test_tensor_path_refuses_unsupported_shapes(kernel_path):
         _run_decode(pkv, q, kc, vc, tables, lens, 0.1, -1)
     with pytest.raises(ValueError):
         pkv.set_kernel_path(9)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(kernel_path):
+    """A wait on a barrier nothing arrives at gives up after its limit and sets
+    the timeout bit; the context stays usable for the next decode."""
+    pkv = kernel_path
+    pkv.device_error(reset=True)
+    pkv.selftest_wait_timeout(2000)  # 2 ms instead of the kernels' 2 s
+    assert pkv.device_error(reset=True) == pkv.DEV_WAIT_TIMEOUT
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(2, 4, 64, generator=g).half().cuda()
+    kc = torch.randn(4, 4, 16, 64, generator=g).half().cuda()
+    vc = torch.randn(4, 4, 16, 64, generator=g).half().cuda()
+    tables = torch.tensor([[0, 1], [3, 2]], dtype=torch.int32).cuda()
+    lens = torch.tensor([20, 32], dtype=torch.int32).cuda()
+    out = pkv.paged_attention_decode(q, kc, vc, tables, lens, 0.125)
+    torch.cuda.synchronize()
+    assert pkv.device_error(reset=True) == 0
+    want = oracle.paged_decode(bits(q.cpu()), oracle.F16, bits(kc.cpu()), bits(vc.cpu()), oracle.F16,
+                               tables.cpu().numpy(), lens.cpu().numpy(), 0.125)
+    assert np.abs(out.float().cpu().numpy() - want).max() <= TOL["f16"]
