@@ -1,5 +1,6 @@
 """Full-size decode steps of each workload, in the launch configuration the
-benchmark times (library-chosen partition size), checked against the float64
+benchmark times (the append fused into the decode launch, library-chosen
+partition size and kernel path), checked against the float64
 oracle on sampled sequences; the block manager's tables and slots are checked
 against the oracle allocator for the whole batch, and the append bit for bit
 on the sampled sequences' blocks."""
@@ -66,11 +67,10 @@ def test_workload_decode_step(pkv, name):
     ks = vals.get("k_scale")
     vs = vals.get("v_scale")
 
-    # device: append then decode, as the benchmark runs it
-    pkv.paged_kv_append(vals["k_new"], vals["v_new"], torch.from_numpy(slots).to(dev), vals["k_cache"],
-                        vals["v_cache"], ks, vs)
-    out = pkv.paged_attention_decode(vals["q"], vals["k_cache"], vals["v_cache"], torch.from_numpy(tables).to(dev),
-                                     torch.from_numpy(lens).to(dev), wl.scale, k_scale=ks, v_scale=vs)
+    # device: the append fused into the decode launch, as the benchmark times it
+    out = pkv.paged_attention_decode_append(vals["q"], vals["k_new"], vals["v_new"], torch.from_numpy(slots).to(dev),
+                                            vals["k_cache"], vals["v_cache"], torch.from_numpy(tables).to(dev),
+                                            torch.from_numpy(lens).to(dev), wl.scale, k_scale=ks, v_scale=vs)
     torch.cuda.synchronize()
 
     # oracle on the sampled sequences, on the compacted copy of their blocks
