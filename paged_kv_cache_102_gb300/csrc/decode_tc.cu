@@ -51,14 +51,15 @@ template <int ACT, int BS, int G, int NS>
 cudaError_t launch(const DecodeParams& p, const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& qm,
                    int ctas_per_sm, cudaStream_t s) {
     auto kern = paged_decode_tc_kernel<ACT, BS, G, NS>;
-    constexpr int smem = TcSmem<NS>::ALLOC;
+    const int rows = p.table_kvh_stride != 0 ? p.num_seqs * p.num_kv_heads : p.num_seqs;
+    const int smem = TcSmem<NS>::alloc(rows);
     static bool configured[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<NS>::alloc(kTcMaxSeqs));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
@@ -103,10 +104,16 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int act, int BS, int G, int 
         return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(p.work_counter, 0, sizeof(int), s);
     if (e != cudaSuccess) return e;
-    // variant 0: five 32 KB stages, one CTA per SM; variant 1: two stages, two CTAs per SM
-    if (act == kBF16)
-        return variant == 0 ? by_shape<kBF16, 5>(p, km, vm, qm, BS, G, 1, s) : by_shape<kBF16, 2>(p, km, vm, qm, BS, G, 2, s);
-    return variant == 0 ? by_shape<kF16, 5>(p, km, vm, qm, BS, G, 1, s) : by_shape<kF16, 2>(p, km, vm, qm, BS, G, 2, s);
+    // variant 0: five 32 KB stages, one CTA per SM; variant 1: two CTAs per SM
+    // with three stages when the per-row tables leave room for them, else two
+    const int rows = p.table_kvh_stride != 0 ? p.num_seqs * p.num_kv_heads : p.num_seqs;
+    const bool three = 2 * (TcSmem<3>::alloc(rows) + 1024) <= kTcSmemPerSm;
+    if (act == kBF16) {
+        if (variant == 0) return by_shape<kBF16, 5>(p, km, vm, qm, BS, G, 1, s);
+        return three ? by_shape<kBF16, 3>(p, km, vm, qm, BS, G, 2, s) : by_shape<kBF16, 2>(p, km, vm, qm, BS, G, 2, s);
+    }
+    if (variant == 0) return by_shape<kF16, 5>(p, km, vm, qm, BS, G, 1, s);
+    return three ? by_shape<kF16, 3>(p, km, vm, qm, BS, G, 2, s) : by_shape<kF16, 2>(p, km, vm, qm, BS, G, 2, s);
 }
 
 }  // namespace pkv

@@ -60,6 +60,7 @@ constexpr int kTcPBuf = (2 * kTcMaxTiles + 1) * 1024;  // P: tile x token-half 8
 constexpr int kTcSlotCols = kTcMaxTiles * kTcN + kTcN;  // S (4 x 16) + O (16) per buffer
 constexpr int kTcTmemCols = 256;              // two buffers of 80 columns, rounded to a power of 2
 constexpr int kTcMaxSeqs = 2048;              // sequences served (lengths and item prefix in shared memory)
+constexpr int kTcSmemPerSm = 228 * 1024;      // shared memory of one SM, including the 1 KB each CTA reserves
 constexpr int kTcQueue = 4;                   // claimed items in flight between the roles
 constexpr int kTcLenBuckets = 8;              // length buckets of the partly filled partitions
 
@@ -67,20 +68,19 @@ template <int NS>
 struct TcSmem {
     static constexpr int RING = 0;
     static constexpr int Q = NS * kTcStage;
-    static constexpr int P = Q + 2 * kTcQBuf;
-    static constexpr int LENS = P + 2 * kTcPBuf;
-    static constexpr int PREFIX = LENS + kTcMaxSeqs * 4;      // full-partition items before each row, [B + 2]
-    static constexpr int ORDER = PREFIX + (kTcMaxSeqs + 2) * 4;  // rows with a partly filled partition, longest first
-    static constexpr int QUEUE = ORDER + kTcMaxSeqs * 2;
+    static constexpr int P = Q + kTcQBuf;
+    static constexpr int QUEUE = P + kTcPBuf;
     static constexpr int BARS = (QUEUE + kTcQueue * 4 + 7) / 8 * 8;
     // full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_free[2], final,
-    // item_full[4], item_empty[4]
+    // item_full[4], item_empty[4] (Q and P use entry 0 of their pairs)
     static constexpr int NBARS = 2 * NS + 13 + 2 * kTcQueue;
     static constexpr int RED = BARS + NBARS * 8;
     static constexpr int RED_FLOATS = 64 + 32;  // red_max[4][8], red_sum[4][8], stats[2][2][8]
     static constexpr int MISC = RED + RED_FLOATS * 4;
-    static constexpr int BYTES = MISC + 16;
-    static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
+    // per row: length (int), item prefix (int, rows + 2 entries), length order (uint16)
+    static constexpr int ROWS = (MISC + 16 + 15) / 16 * 16;
+    __host__ __device__ static constexpr int bytes(int rows) { return ROWS + rows * 4 + (rows + 2) * 4 + rows * 2; }
+    __host__ __device__ static constexpr int alloc(int rows) { return bytes(rows) + 1024; }  // room to align the base
 };
 
 struct TcItem {
@@ -189,9 +189,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* ring = sm + S::RING;
     unsigned char* qbuf = sm + S::Q;
     unsigned char* pbuf = sm + S::P;
-    int* s_lens = reinterpret_cast<int*>(sm + S::LENS);
-    int* s_prefix = reinterpret_cast<int*>(sm + S::PREFIX);
-    uint16_t* s_order = reinterpret_cast<uint16_t*>(sm + S::ORDER);
     volatile int* item_q = reinterpret_cast<volatile int*>(sm + S::QUEUE);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BARS);
     uint64_t* full = bars;
@@ -214,6 +211,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int B = tc_rows(p);  // rows: <= kTcMaxSeqs (checked on the host)
+    int* s_lens = reinterpret_cast<int*>(sm + S::ROWS);
+    int* s_prefix = s_lens + B;
+    uint16_t* s_order = reinterpret_cast<uint16_t*>(s_prefix + B + 2);
     const int heads_per_row = tc_per_kvh(p) ? 1 : p.num_kv_heads;
 
     // Lengths, the exclusive prefix of full-partition items per row and the
@@ -412,13 +412,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                           const_cast<void*>(p.v_cache), nullptr, nullptr, p.err, lane);
             }
             if (lane == 0) {
-                const int b = k & 1;
-                if (k >= 2) good = tc_wait(&q_empty[b], ((k >> 1) - 1) & 1, abort_flag, p.err);
+                // one Q buffer: item k's Q loads once the S MMAs of item k-1 have read it
+                if (k >= 1) good = tc_wait(&q_empty[0], (k - 1) & 1, abort_flag, p.err);
                 if (good) {
-                    mbar_arrive_expect_tx(&q_full[b], 2 * G * 128);
+                    mbar_arrive_expect_tx(&q_full[0], 2 * G * 128);
                     const int row = it.seq * p.num_q_heads + it.kvh * G;
-                    tc::tma_load_2d(qbuf + b * kTcQBuf, &qmap, 0, row, &q_full[b], policy);
-                    tc::tma_load_2d(qbuf + b * kTcQBuf + 1024, &qmap, 64, row, &q_full[b], policy);
+                    tc::tma_load_2d(qbuf, &qmap, 0, row, &q_full[0], policy);
+                    tc::tma_load_2d(qbuf + 1024, &qmap, 64, row, &q_full[0], policy);
                 }
             }
             good = __shfl_sync(0xffffffffu, good, 0);
@@ -453,8 +453,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t first = use > static_cast<uint32_t>(NS) ? use - NS : 0;
             for (uint32_t u = first; u < use; ++u)
                 if (!mbar_wait(&full[u % NS], (u / NS) & 1)) atomicOr(p.err, kErrTimeout);
-            for (int k = nq > 2 ? nq - 2 : 0; k < nq; ++k)
-                if (!mbar_wait(&q_full[k & 1], (k >> 1) & 1)) atomicOr(p.err, kErrTimeout);
+            if (nq > 0 && !mbar_wait(&q_full[0], (nq - 1) & 1)) atomicOr(p.err, kErrTimeout);
         }
     } else if (warp == 1) {
         // --------------------------------------------------------------------- MMA
@@ -483,11 +482,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         auto mma_s = [&](const TcItem& it, int k) {
             const int b = k & 1;
             bool good = true;
-            if (lane == 0) good = tc_wait(&q_full[b], (k >> 1) & 1, abort_flag, p.err);
+            if (lane == 0) good = tc_wait(&q_full[0], k & 1, abort_flag, p.err);
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) return false;
             tc::fence_after_sync();
-            const uint32_t qb = smem_addr(qbuf + b * kTcQBuf);
+            const uint32_t qb = smem_addr(qbuf);
             for (int t = 0; t < it.n_tiles; ++t) {
                 const int s = use % NS;
                 if (lane == 0) good = tc_wait(&full[s], (use / NS) & 1, abort_flag, p.err);
@@ -509,7 +508,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ++use;
             }
             if (lane == 0) {
-                tc::commit(&q_empty[b]);
+                tc::commit(&q_empty[0]);
                 tc::commit(&s_full[b]);
             }
             __syncwarp();
@@ -519,13 +518,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int b = k & 1;
             bool good = true;
             if (lane == 0) {
-                good = tc_wait(&p_full[b], (k >> 1) & 1, abort_flag, p.err);
+                good = tc_wait(&p_full[0], k & 1, abort_flag, p.err);
                 if (good && k >= 2) good = tc_wait(&o_free[b], ((k >> 1) - 1) & 1, abort_flag, p.err);
             }
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) return false;
             tc::fence_after_sync();
-            const uint32_t pbase = smem_addr(pbuf + b * kTcPBuf);
+            const uint32_t pbase = smem_addr(pbuf);
             for (int t = 0; t < it.n_tiles; ++t) {
                 const int s = use % NS;
                 good = __all_sync(0xffffffffu, tc_wait(&full[s], (use / NS) & 1, abort_flag, p.err));
@@ -608,7 +607,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         auto softmax = [&](const TcItem& it, int k) {
             const int b = k & 1;
-            const bool good = __all_sync(0xffffffffu, tc_wait(&s_full[b], (k >> 1) & 1, abort_flag, p.err));
+            // one P buffer: item k writes it once the O MMAs of item k-1 have read it
+            const bool good = __all_sync(0xffffffffu, tc_wait(&s_full[b], (k >> 1) & 1, abort_flag, p.err) &&
+                                                          (k == 0 || tc_wait(&o_full[(k - 1) & 1], ((k - 1) >> 1) & 1,
+                                                                             abort_flag, p.err)));
             float sc[kTcMaxTiles][G] = {};
             if (good) {
                 tc::fence_after_sync();
@@ -647,7 +649,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 M[g] = fmaxf(fmaxf(red_max[g], red_max[8 + g]), fmaxf(red_max[16 + g], red_max[24 + g]));
                 sum[g] = 0.f;
             }
-            unsigned char* pb = pbuf + b * kTcPBuf;
+            unsigned char* pb = pbuf;
 #pragma unroll
             for (int t = 0; t < kTcMaxTiles; ++t) {
                 if (t < it.n_tiles) {
@@ -679,7 +681,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     stats[b * 16 + g] = M[g];
                     stats[b * 16 + 8 + g] = red_sum[g] + red_sum[8 + g] + red_sum[16 + g] + red_sum[24 + g];
                 }
-                mbar_arrive(&p_full[b]);
+                mbar_arrive(&p_full[0]);
             }
             return true;
         };
