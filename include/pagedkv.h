@@ -112,7 +112,11 @@ int paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping, i
  *  block_tables  int32 [num_seqs][max_blocks_per_seq] (device); only the
  *                first ceil(L/block_size) entries of a row are read.
  *  context_lens  int32 [num_seqs] (device), each in 1..max_blocks_per_seq*block_size.
- *  out           [num_seqs][num_q_heads][head_dim] of act_dtype (device, written).
+ *  out           [num_seqs][num_q_heads][head_dim] of act_dtype (written): device
+ *                memory, or pinned host memory the device can address (the
+ *                kernels then store the result over the host link within the
+ *                same launch; measured slower than device memory plus one
+ *                copy for a 0.5 MB result).
  *  act_dtype     PKV_F16 or PKV_BF16; cache_dtype == act_dtype or PKV_E4M3.
  *  head_dim      64 or 128; block_size 16 or 32; group num_q_heads/num_kv_heads
  *                in {1, 2, 4, 8}.

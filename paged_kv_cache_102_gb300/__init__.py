@@ -61,20 +61,32 @@ def _code(t: torch.Tensor) -> int:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # ctypes converts a Python int for a c_void_p argument
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream, device) -> ctypes.c_void_p:
+def _stream(stream, device) -> int:
     if stream is None:
         stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
+
+
+def _require_out(device, out):
+    """`out` may be a CUDA tensor on `device` or a pinned host tensor, which the
+    kernels write directly over the host link."""
+    if out.is_pinned() and not out.is_cuda:
+        if not out.is_contiguous():
+            raise ValueError("out must be contiguous")
+        return
+    _require_cuda(device, out=out)
 
 
 def _require_cuda(device, **tensors):
+    index = device.index if device.index is not None else torch.cuda.current_device()
     for name, t in tensors.items():
         if t is None:
             continue
-        if not t.is_cuda or t.device != device:
+        if t.get_device() != index:  # -1 for a CPU tensor
             raise ValueError(f"{name} must be a CUDA tensor on {device}")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
@@ -145,13 +157,15 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
         out = torch.empty_like(q)
     elif out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("paged_attention_decode: out must match q")
+    _require_out(q.device, out)
     _require_cuda(q.device, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
-                  context_lens=context_lens, out=out, k_scale=k_scale, v_scale=v_scale, workspace=workspace)
+                  context_lens=context_lens, k_scale=k_scale, v_scale=v_scale, workspace=workspace)
     max_blocks = block_tables.shape[1]
     s = _stream(stream, q.device)
-    need = workspace_size(B, Hq, Hkv, D, max_blocks, bs, partition_size)
-    if need and workspace is None:
-        workspace = _workspace(q.device, s.value or 0, need)
+    if workspace is None:
+        need = workspace_size(B, Hq, Hkv, D, max_blocks, bs, partition_size)
+        if need:
+            workspace = _workspace(q.device, s, need)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _native.call("paged_attention_decode", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks,
                  _ptr(context_lens), B, Hq, Hkv, bs, D, NB, float(scale), _ptr(out), _code(q), _code(k_cache),
@@ -174,14 +188,16 @@ def paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cach
         raise ValueError("paged_attention_decode_append: block_tables and context_lens must be int32")
     if out is None:
         out = torch.empty_like(q)
+    _require_out(q.device, out)
     _require_cuda(q.device, q=q, k_new=k_new, v_new=v_new, slot_mapping=slot_mapping, k_cache=k_cache,
-                  v_cache=v_cache, block_tables=block_tables, context_lens=context_lens, out=out, k_scale=k_scale,
+                  v_cache=v_cache, block_tables=block_tables, context_lens=context_lens, k_scale=k_scale,
                   v_scale=v_scale, workspace=workspace)
     max_blocks = block_tables.shape[1]
     s = _stream(stream, q.device)
-    need = workspace_size(B, Hq, Hkv, D, max_blocks, bs, partition_size)
-    if need and workspace is None:
-        workspace = _workspace(q.device, s.value or 0, need)
+    if workspace is None:
+        need = workspace_size(B, Hq, Hkv, D, max_blocks, bs, partition_size)
+        if need:
+            workspace = _workspace(q.device, s, need)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _native.call("paged_attention_decode_append", _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
                  _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), B, Hq, Hkv, bs, D,
@@ -224,7 +240,7 @@ def quest_select(q, kmeta, block_tables, context_lens, block_size, budget_blocks
     s = _stream(stream, q.device)
     need = int(_native.lib().quest_workspace_size(B, Hkv, block_tables.shape[1]))
     if workspace is None:
-        workspace = _workspace(q.device, -(s.value or 0) - 1, need)  # separate from the decode workspace
+        workspace = _workspace(q.device, -s - 1, need)  # separate from the decode workspace
     _native.call("quest_select", _ptr(q), _ptr(kmeta), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
                  B, Hq, Hkv, block_size, D, NB, _code(q), int(budget_blocks), _ptr(sel_tables), _ptr(sel_lens),
                  _ptr(workspace), workspace.numel() * workspace.element_size(), s)
@@ -238,13 +254,14 @@ def paged_attention_decode_sparse(q, k_cache, v_cache, sel_tables, sel_lens, sca
     NB, Hkv, bs, _ = k_cache.shape
     if out is None:
         out = torch.empty_like(q)
+    _require_out(q.device, out)
     _require_cuda(q.device, q=q, k_cache=k_cache, v_cache=v_cache, sel_tables=sel_tables, sel_lens=sel_lens,
-                  out=out, k_scale=k_scale, v_scale=v_scale, workspace=workspace)
+                  k_scale=k_scale, v_scale=v_scale, workspace=workspace)
     max_sel = sel_tables.shape[2]
     s = _stream(stream, q.device)
     need = workspace_size(B, Hq, Hkv, D, max_sel, bs, partition_size)
     if need and workspace is None:
-        workspace = _workspace(q.device, s.value or 0, need)
+        workspace = _workspace(q.device, s, need)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _native.call("paged_attention_decode_sparse", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(sel_tables), max_sel,
                  _ptr(sel_lens), B, Hq, Hkv, bs, D, NB, float(scale), _ptr(out), _code(q), _code(k_cache),

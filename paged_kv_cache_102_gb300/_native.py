@@ -70,9 +70,14 @@ class PagedKVError(RuntimeError):
         self.code = code
 
 
+_fns: dict = {}
+
+
 def lib():
     """The loaded library; raises if it has not been built."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -93,4 +98,9 @@ def check(func: str, code: int) -> None:
 
 
 def call(func: str, *args) -> None:
-    check(func, getattr(lib(), func)(*args))
+    fn = _fns.get(func)
+    if fn is None:
+        fn = _fns[func] = getattr(lib(), func)
+    code = fn(*args)
+    if code != 0:
+        raise PagedKVError(func, code, lib().pkv_last_error().decode())

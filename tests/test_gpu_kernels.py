@@ -345,3 +345,26 @@ def test_bounded_wait_reports_timeout_and_context_survives(kernel_path):
     want = oracle.paged_decode(bits(q.cpu()), oracle.F16, bits(kc.cpu()), bits(vc.cpu()), oracle.F16,
                                tables.cpu().numpy(), lens.cpu().numpy(), 0.125)
     assert np.abs(out.float().cpu().numpy() - want).max() <= TOL["f16"]
+
+
+@pytest.mark.parametrize("path", [1, 3])
+def test_output_to_pinned_host_memory(kernel_path, path):
+    """out in pinned host memory: the kernels (partition, tensor-core and merge)
+    store the result over the host link; it equals the device-memory output."""
+    pkv = kernel_path
+    pkv.set_kernel_path(path)
+    g = torch.Generator().manual_seed(17 + path)
+    B, Hq, Hkv, D, bs = 5, 32, 4, 128, 16
+    lens = torch.tensor([1, 100, 700, 1500, 2000], dtype=torch.int32)
+    maxb = -(-int(lens.max()) // bs)
+    NB = B * maxb
+    tables = torch.randperm(NB, generator=g)[: B * maxb].reshape(B, maxb).to(torch.int32)
+    q = torch.randn(B, Hq, D, generator=g).bfloat16().cuda()
+    kc = torch.randn(NB, Hkv, bs, D, generator=g).bfloat16().cuda()
+    vc = torch.randn(NB, Hkv, bs, D, generator=g).bfloat16().cuda()
+    t_d, l_d = tables.cuda(), lens.cuda()
+    want = pkv.paged_attention_decode(q, kc, vc, t_d, l_d, 0.088, partition_size=512)
+    host = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16).pin_memory()
+    got = pkv.paged_attention_decode(q, kc, vc, t_d, l_d, 0.088, out=host, partition_size=512)
+    torch.cuda.synchronize()
+    assert got is host and torch.equal(host, want.cpu())
