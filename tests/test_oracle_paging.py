@@ -176,3 +176,34 @@ def test_out_of_blocks_raises():
         bm.append_slot(0)
     with pytest.raises(OutOfBlocks):
         bm.add_sequence(1, 1)
+
+
+def test_reference_swap_hand_example():
+    """Preemption by swapping, worked by hand: a 10-token sequence at block
+    size 4 holds 3 blocks; swapping it out returns them to the back of the free
+    list (FIFO); another request then takes blocks from the front; swapping
+    back in takes 3 fresh blocks from the front in order, with the length kept.
+    A shared (forked) block is only released when its last holder leaves."""
+    from oracle.block_manager_ref import OutOfBlocks, RefBlockManager
+    ref = RefBlockManager(8, 4)                     # free list 0..7
+    ref.add_sequence("a", 10)                       # blocks 0, 1, 2
+    assert ref.tables["a"] == [0, 1, 2] and ref.free == [3, 4, 5, 6, 7]
+    assert ref.swap_out("a") == [0, 1, 2]
+    assert ref.free == [3, 4, 5, 6, 7, 0, 1, 2] and "a" not in ref.tables
+    ref.add_sequence("b", 17)                       # ceil(17/4) = 5 blocks from the front
+    assert ref.tables["b"] == [3, 4, 5, 6, 7] and ref.free == [0, 1, 2]
+    assert ref.swap_in("a") == [0, 1, 2] and ref.lens["a"] == 10 and ref.free == []
+    assert ref.swap_out("b") == [3, 4, 5, 6, 7]
+    ref.add_sequence("c", 20)                       # 5 blocks: b's freed blocks
+    with pytest.raises(OutOfBlocks):
+        ref.swap_in("b")                            # no room: b stays swapped out
+    assert ref.swapped == {"b": 17}
+    # a forked sequence shares its parent's blocks: swapping the child out
+    # releases nothing, swapping the parent out too releases them
+    ref2 = RefBlockManager(4, 4)
+    ref2.add_sequence("p", 6)                       # blocks 0, 1
+    ref2.fork("p", "q")
+    ref2.swap_out("q")
+    assert ref2.free == [2, 3] and ref2.ref[:2] == [1, 1]
+    ref2.swap_out("p")
+    assert ref2.free == [2, 3, 0, 1]
