@@ -73,6 +73,9 @@ WORKLOADS = {
     "gqa_bs32": Workload(
         "gqa_bs32", 128, 64, 8, 128, 32, "bf16", "bf16", ("lognormal", 1024, 1.0, 16, 8192),
         description="GQA decode as gqa_bs16 with block 32"),
+    "gqa_fp8": Workload(
+        "gqa_fp8", 128, 64, 8, 128, 16, "bf16", "e4m3", ("lognormal", 1024, 1.0, 16, 8192),
+        description="GQA decode as gqa_bs16 with an FP8-E4M3 cache (per-tensor scales from the N(0,1) data)"),
     "shared_prefix": Workload(
         "shared_prefix", 32, 32, 32, 128, 16, "f16", "f16", ("uniform_not_multiple", 1000, 1030),
         samples_per_prompt=4, divergent_tokens=(0, 256),
