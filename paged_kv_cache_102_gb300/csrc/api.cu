@@ -300,7 +300,7 @@ static int decode_impl(const char* fn, const void* q, const void* k_cache, const
     const bool use_tc = path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA ||
                         (path == PKV_PATH_AUTO && tc_ok && G >= 4);
     if (use_tc)
-        e = launch_decode_tc(p, act_dtype, block_size, G, path == PKV_PATH_TENSOR ? 0 : 1, s);
+        e = launch_decode_tc(p, act_dtype, cache_dtype, block_size, G, path == PKV_PATH_TENSOR ? 0 : 1, s);
     else if (act_dtype == PKV_F16)
         e = cache_dtype == PKV_E4M3 ? launch_decode_f16_e4m3(p, head_dim, block_size, G, s)
                                     : launch_decode_f16_f16(p, head_dim, block_size, G, s);

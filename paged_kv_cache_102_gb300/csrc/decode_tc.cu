@@ -2,6 +2,7 @@
 // over the caches and the queries, persistent grid sizing, instantiations.
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "decode_tc.cuh"
@@ -47,19 +48,20 @@ int sm_count() {
     return counts[dev];
 }
 
-template <int ACT, int BS, int G, int NS>
+template <int ACT, int CACHE, int BS, int G, int NS, int NSS>
 cudaError_t launch(const DecodeParams& p, const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& qm,
                    int ctas_per_sm, cudaStream_t s) {
-    auto kern = paged_decode_tc_kernel<ACT, BS, G, NS>;
+    auto kern = paged_decode_tc_kernel<ACT, CACHE, BS, G, NS, NSS>;
+    constexpr int threads = CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads;
     const int rows = p.table_kvh_stride != 0 ? p.num_seqs * p.num_kv_heads : p.num_seqs;
-    const int smem = TcSmem<NS>::alloc(rows);
+    const int smem = TcSmem<NS, NSS>::alloc(rows);
     static bool configured[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<NS>::alloc(kTcMaxSeqs));
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<NS, NSS>::alloc(kTcMaxSeqs));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
@@ -68,35 +70,55 @@ cudaError_t launch(const DecodeParams& p, const CUtensorMap& km, const CUtensorM
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = static_cast<int>(items < static_cast<long long>(sms) * ctas_per_sm ? items : sms * ctas_per_sm);
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, kTcThreads, smem, s>>>(km, vm, qm, p);
+    kern<<<grid, threads, smem, s>>>(km, vm, qm, p);
     return cudaGetLastError();
 }
 
-template <int ACT, int NS>
+template <int ACT, int CACHE, int NS, int NSS>
 cudaError_t by_shape(const DecodeParams& p, const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& qm,
                      int BS, int G, int ctas_per_sm, cudaStream_t s) {
     if (BS == 16) {
-        if (G == 2) return launch<ACT, 16, 2, NS>(p, km, vm, qm, ctas_per_sm, s);
-        if (G == 4) return launch<ACT, 16, 4, NS>(p, km, vm, qm, ctas_per_sm, s);
-        if (G == 8) return launch<ACT, 16, 8, NS>(p, km, vm, qm, ctas_per_sm, s);
+        if (G == 2) return launch<ACT, CACHE, 16, 2, NS, NSS>(p, km, vm, qm, ctas_per_sm, s);
+        if (G == 4) return launch<ACT, CACHE, 16, 4, NS, NSS>(p, km, vm, qm, ctas_per_sm, s);
+        if (G == 8) return launch<ACT, CACHE, 16, 8, NS, NSS>(p, km, vm, qm, ctas_per_sm, s);
     } else if (BS == 32) {
-        if (G == 2) return launch<ACT, 32, 2, NS>(p, km, vm, qm, ctas_per_sm, s);
-        if (G == 4) return launch<ACT, 32, 4, NS>(p, km, vm, qm, ctas_per_sm, s);
-        if (G == 8) return launch<ACT, 32, 8, NS>(p, km, vm, qm, ctas_per_sm, s);
+        if (G == 2) return launch<ACT, CACHE, 32, 2, NS, NSS>(p, km, vm, qm, ctas_per_sm, s);
+        if (G == 4) return launch<ACT, CACHE, 32, 4, NS, NSS>(p, km, vm, qm, ctas_per_sm, s);
+        if (G == 8) return launch<ACT, CACHE, 32, 8, NS, NSS>(p, km, vm, qm, ctas_per_sm, s);
     }
     return cudaErrorInvalidValue;
+}
+
+// E4M3 cache: raw tiles land in the upper half of a ring stage and are
+// converted in place; five stages at one CTA per SM (variant 0), else three
+// (or two) at two CTAs per SM, as for 16-bit caches.
+template <int ACT>
+cudaError_t launch_fp8(const DecodeParams& p, int BS, int G, int variant, bool three, cudaStream_t s) {
+    CUtensorMap unused;
+    std::memset(&unused, 0, sizeof(unused));
+    if (variant == 0) return by_shape<ACT, kE4M3, 5, 5>(p, unused, unused, unused, BS, G, 1, s);
+    if (three) return by_shape<ACT, kE4M3, 3, 3>(p, unused, unused, unused, BS, G, 2, s);
+    return by_shape<ACT, kE4M3, 2, 2>(p, unused, unused, unused, BS, G, 2, s);
 }
 
 }  // namespace
 
 bool decode_tc_supported(int num_seqs, int head_dim, int block_size, int group, int act, int cache,
                          int partition_size) {
-    return num_seqs <= kTcMaxSeqs && head_dim == kTcD && (block_size == 16 || block_size == 32) && (group == 2 || group == 4 || group == 8) &&
-           act == cache && (act == kF16 || act == kBF16) && partition_size <= kTcMaxTiles * kTcTile &&
-           encode_fn() != nullptr;
+    return num_seqs <= kTcMaxSeqs && head_dim == kTcD && (block_size == 16 || block_size == 32) &&
+           (group == 2 || group == 4 || group == 8) && (act == kF16 || act == kBF16) &&
+           (cache == act || cache == kE4M3) && partition_size <= kTcMaxTiles * kTcTile && encode_fn() != nullptr;
 }
 
-cudaError_t launch_decode_tc(const DecodeParams& p, int act, int BS, int G, int variant, cudaStream_t s) {
+cudaError_t launch_decode_tc(const DecodeParams& p, int act, int cache, int BS, int G, int variant, cudaStream_t s) {
+    if (cache == kE4M3) {
+        cudaError_t e = cudaMemsetAsync(p.work_counter, 0, sizeof(int), s);
+        if (e != cudaSuccess) return e;
+        const int rows = p.table_kvh_stride != 0 ? p.num_seqs * p.num_kv_heads : p.num_seqs;
+        const bool three = 2 * (TcSmem<3, 3>::alloc(rows) + 1024) <= kTcSmemPerSm;
+        return act == kBF16 ? launch_fp8<kBF16>(p, BS, G, variant, three, s)
+                            : launch_fp8<kF16>(p, BS, G, variant, three, s);
+    }
     CUtensorMap km, vm, qm;
     const uint64_t cache_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * BS;
     if (!make_map(&km, p.k_cache, act, cache_rows, BS) || !make_map(&vm, p.v_cache, act, cache_rows, BS) ||
@@ -107,13 +129,15 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int act, int BS, int G, int 
     // variant 0: five 32 KB stages, one CTA per SM; variant 1: two CTAs per SM
     // with three stages when the per-row tables leave room for them, else two
     const int rows = p.table_kvh_stride != 0 ? p.num_seqs * p.num_kv_heads : p.num_seqs;
-    const bool three = 2 * (TcSmem<3>::alloc(rows) + 1024) <= kTcSmemPerSm;
+    const bool three = 2 * (TcSmem<3, 0>::alloc(rows) + 1024) <= kTcSmemPerSm;
     if (act == kBF16) {
-        if (variant == 0) return by_shape<kBF16, 5>(p, km, vm, qm, BS, G, 1, s);
-        return three ? by_shape<kBF16, 3>(p, km, vm, qm, BS, G, 2, s) : by_shape<kBF16, 2>(p, km, vm, qm, BS, G, 2, s);
+        if (variant == 0) return by_shape<kBF16, kBF16, 5, 0>(p, km, vm, qm, BS, G, 1, s);
+        return three ? by_shape<kBF16, kBF16, 3, 0>(p, km, vm, qm, BS, G, 2, s)
+                     : by_shape<kBF16, kBF16, 2, 0>(p, km, vm, qm, BS, G, 2, s);
     }
-    if (variant == 0) return by_shape<kF16, 5>(p, km, vm, qm, BS, G, 1, s);
-    return three ? by_shape<kF16, 3>(p, km, vm, qm, BS, G, 2, s) : by_shape<kF16, 2>(p, km, vm, qm, BS, G, 2, s);
+    if (variant == 0) return by_shape<kF16, kF16, 5, 0>(p, km, vm, qm, BS, G, 1, s);
+    return three ? by_shape<kF16, kF16, 3, 0>(p, km, vm, qm, BS, G, 2, s)
+                 : by_shape<kF16, kF16, 2, 0>(p, km, vm, qm, BS, G, 2, s);
 }
 
 }  // namespace pkv

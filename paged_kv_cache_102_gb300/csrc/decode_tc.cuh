@@ -49,6 +49,8 @@
 namespace pkv {
 
 constexpr int kTcThreads = 192;
+constexpr int kTcThreadsFp8 = 256;            // E4M3 cache: two more warps convert the tiles
+constexpr int kTcFp8Stage = 128 * 128;        // one E4M3 tile in staging: 128 tokens x 128 bytes
 constexpr int kTcTile = 128;                  // tokens per tile (MMA M of S = K Q^T)
 constexpr int kTcMaxTiles = 4;                // partitions of at most 512 tokens
 constexpr int kTcD = 128;                     // head_dim served by this kernel
@@ -64,16 +66,16 @@ constexpr int kTcSmemPerSm = 228 * 1024;      // shared memory of one SM, includ
 constexpr int kTcQueue = 4;                   // claimed items in flight between the roles
 constexpr int kTcLenBuckets = 8;              // length buckets of the partly filled partitions
 
-template <int NS>
+template <int NS, int NSS = 0>
 struct TcSmem {
     static constexpr int RING = 0;
     static constexpr int Q = NS * kTcStage;
     static constexpr int P = Q + kTcQBuf;
-    static constexpr int QUEUE = P + kTcPBuf;
-    static constexpr int BARS = (QUEUE + kTcQueue * 4 + 7) / 8 * 8;
+    static constexpr int QUEUE = P + kTcPBuf;                  // item numbers [4], q shifts [4]
+    static constexpr int BARS = (QUEUE + 2 * kTcQueue * 4 + 7) / 8 * 8;
     // full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_free[2], final,
-    // item_full[4], item_empty[4] (Q and P use entry 0 of their pairs)
-    static constexpr int NBARS = 2 * NS + 13 + 2 * kTcQueue;
+    // item_full[4], item_empty[4], stg_full[NSS] (Q and P use entry 0 of their pairs)
+    static constexpr int NBARS = 2 * NS + 13 + 2 * kTcQueue + NSS;
     static constexpr int RED = BARS + NBARS * 8;
     static constexpr int RED_FLOATS = 64 + 32;  // red_max[4][8], red_sum[4][8], stats[2][2][8]
     static constexpr int MISC = RED + RED_FLOATS * 4;
@@ -85,6 +87,7 @@ struct TcSmem {
 
 struct TcItem {
     int seq, kvh, row, part, tok_begin, n_tok, n_tiles;
+    int qshift;  // E4M3 cache: q enters the MMA as binary16 times 2^-qshift
 };
 
 // Rows: a sequence (tables shared by its kv heads) or, with per-(sequence,
@@ -170,14 +173,18 @@ __device__ __forceinline__ int named_bar_or(int id, int count, int pred) {
     return r;
 }
 
-template <int ACT, int BS, int G, int NS>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int ACT, int CACHE, int BS, int G, int NS, int NSS>
+__global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, CACHE == kE4M3 && NS < 5 ? 2 : 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const __grid_constant__ CUtensorMap qmap, const DecodeParams p) {
-    using S = TcSmem<NS>;
+    using S = TcSmem<NS, NSS>;
+    constexpr bool FP8 = CACHE == kE4M3;
+    constexpr int OT = FP8 ? kF16 : ACT;  // the MMA's operand type
+    constexpr int THREADS = FP8 ? kTcThreadsFp8 : kTcThreads;
     constexpr int BPT = kTcTile / BS;  // blocks per tile
-    constexpr uint32_t IDESC_S = tc::idesc_f16(128, kTcN, ACT == kBF16, false, false);
-    constexpr uint32_t IDESC_O = tc::idesc_f16(128, kTcN, ACT == kBF16, true, false);
+    constexpr uint32_t IDESC_S = tc::idesc_f16(128, kTcN, OT == kBF16, false, false);
+    constexpr uint32_t IDESC_O = tc::idesc_f16(128, kTcN, OT == kBF16, true, false);
+    static_assert(!FP8 || (NSS == NS && (ACT == kF16 || ACT == kBF16)), "E4M3 cache: one staging barrier per stage");
     static_assert(G == 2 || G == 4 || G == 8, "query heads per kv head");
     static_assert(kTcMaxTiles * kTcTile / BS <= 32, "one warp holds the table entries of an item");
 
@@ -190,6 +197,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* qbuf = sm + S::Q;
     unsigned char* pbuf = sm + S::P;
     volatile int* item_q = reinterpret_cast<volatile int*>(sm + S::QUEUE);
+    volatile int* item_shift = item_q + kTcQueue;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BARS);
     uint64_t* full = bars;
     uint64_t* empty = bars + NS;
@@ -202,6 +210,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* final_bar = q_full + 12;
     uint64_t* item_full = q_full + 13;
     uint64_t* item_empty = item_full + kTcQueue;
+    uint64_t* stg_full = item_empty + kTcQueue;  // E4M3: the stage's raw tile has landed
     float* red_max = reinterpret_cast<float*>(sm + S::RED);
     float* red_sum = red_max + 32;
     float* stats = red_max + 64;  // [buffer][max, sum][8]
@@ -224,7 +233,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // every CTA.
     {
         constexpr int NBK = kTcLenBuckets;
-        const int chunk = (B + kTcThreads - 1) / kTcThreads;
+        const int chunk = (B + THREADS - 1) / THREADS;
         const int s0 = min(B, threadIdx.x * chunk), s1 = min(B, s0 + chunk);
         auto bucket_of = [&](int L) { return (L % p.partition_size) * NBK / p.partition_size; };
         auto valid_len = [&](int L) { return L >= 1 && L <= p.max_blocks_per_seq * BS; };
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int k = 0; k <= NBK; ++k) {
             int before = 0, all = 0;
-            for (int w = 0; w < kTcThreads / 32; ++w) {
+            for (int w = 0; w < THREADS / 32; ++w) {
                 const int t = warp_tot[w * (NBK + 1) + k];
                 if (w < warp) before += t;
                 all += t;
@@ -298,19 +307,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], FP8 ? 2 : 1);  // E4M3: the two converting warps fill a stage
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 13; ++i) mbar_init(&q_full[i], 1);
         for (int i = 0; i < kTcQueue; ++i) {
             mbar_init(&item_full[i], 1);
-            mbar_init(&item_empty[i], 2);  // the MMA warp and the softmax warps
+            // the MMA warp and the softmax warps (and the two converting warps)
+            mbar_init(&item_empty[i], FP8 ? 4 : 2);
         }
+        for (int i = 0; i < NSS; ++i) mbar_init(&stg_full[i], 1);
         *abort_flag = 0;
         mbar_init_fence();
-        tc::prefetch_tensormap(&kmap);
-        tc::prefetch_tensormap(&vmap);
-        tc::prefetch_tensormap(&qmap);
+        if constexpr (!FP8) {
+            tc::prefetch_tensormap(&kmap);
+            tc::prefetch_tensormap(&vmap);
+            tc::prefetch_tensormap(&qmap);
+        }
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_base_smem, kTcTmemCols);
@@ -340,27 +353,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // at the end of the work (the end marker is queued) or on an abort.
         auto claim = [&](TcItem& it) {
             int ci = -1;
-            bool good = true;
             if (lane == 0) {
                 ci = atomicAdd(p.work_counter, 1);
                 if (ci >= total) ci = -1;
+            }
+            ci = __shfl_sync(0xffffffffu, ci, 0);
+            it.qshift = 0;
+            if (ci >= 0) {
+                tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
+                if constexpr (FP8) {
+                    // q enters the MMA as binary16: scale it by 2^-qshift (exact)
+                    // so that its largest magnitude stays below 2^15
+                    const uint16_t* qg = static_cast<const uint16_t*>(p.q) +
+                                         (static_cast<int64_t>(it.seq) * p.num_q_heads + it.kvh * G) * kTcD;
+                    float m = 0.f;
+                    for (int i = lane; i < G * kTcD / 8; i += 32) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(qg + i * 8);
+                        const uint16_t* e = reinterpret_cast<const uint16_t*>(&u);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(act_to_float<ACT>(e[j])));
+                    }
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                    const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m)
+                    it.qshift = m > 32768.f ? e - 14 : 0;
+                }
+            }
+            bool good = true;
+            if (lane == 0) {
                 const int slot = nclaim % kTcQueue;
                 if (nclaim >= kTcQueue) good = tc_wait(&item_empty[slot], ((nclaim / kTcQueue) - 1) & 1, abort_flag, p.err);
                 if (good) {
                     item_q[slot] = ci;
+                    item_shift[slot] = it.qshift;
                     mbar_arrive(&item_full[slot]);
                 }
             }
             good = __shfl_sync(0xffffffffu, good, 0);
-            ci = __shfl_sync(0xffffffffu, ci, 0);
             if (!good) {
                 ok = false;
                 return false;
             }
             ++nclaim;
-            if (ci < 0) return false;
-            tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
-            return true;
+            return ci >= 0;
         };
         auto table_entry = [&](const TcItem& it) {
             const int n_blk = (it.n_tok + BS - 1) / BS;
@@ -379,7 +414,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // map.  Lane 0 waits for the stage and sets its byte count; lane 2j+h
         // then loads half h of block j of the tile, so one warp instruction
         // issues the tile's 2*BPT copies.
+        // E4M3: tile t's (block, kv head) tiles of 128 contiguous bytes per token
+        // go by 1-D bulk copies (one lane per block) into the upper half of a
+        // ring stage; the converting warps rewrite the stage in place as the
+        // MMA's binary16 layout.
+        auto issue_tile_fp8 = [&](const TcItem& it, int phys, int t, const void* cache) {
+            const int n_blk = (it.n_tok + BS - 1) / BS;
+            const int j = lane < BPT ? lane : 0;
+            const int pbj = __shfl_sync(0xffffffffu, phys, (t * BPT + j) & 31);
+            const bool mine = lane < BPT && t * BPT + j < n_blk && pbj >= 0;
+            const unsigned loads = __ballot_sync(0xffffffffu, mine);
+            const int s = use % NS;
+            bool good = true;
+            if (lane == 0) {
+                if (use >= NS) good = tc_wait(&empty[s], ((use / NS) - 1) & 1, abort_flag, p.err);
+                if (good) mbar_arrive_expect_tx(&stg_full[s], __popc(loads) * (BS * kTcD));
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) return false;
+            if (mine)
+                bulk_copy_g2s(ring + s * kTcStage + kTcHalf + j * BS * kTcD,
+                              static_cast<const uint8_t*>(cache) +
+                                  (static_cast<int64_t>(pbj) * p.num_kv_heads + it.kvh) * BS * kTcD,
+                              BS * kTcD, &stg_full[s], policy);
+            ++use;
+            return true;
+        };
         auto issue_tile = [&](const TcItem& it, int phys, int t, const CUtensorMap* map) {
+            if constexpr (FP8) return issue_tile_fp8(it, phys, t, map == &kmap ? p.k_cache : p.v_cache);
             const int n_blk = (it.n_tok + BS - 1) / BS;
             const int j = (lane >> 1) < BPT ? (lane >> 1) : 0;
             const int half = lane & 1;
@@ -407,9 +469,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (p.new_slots != nullptr && it.tok_begin + it.n_tok == s_lens[it.row]) {
                 // fused append: this item holds the new (last) token; write it before
                 // the TMA reads of its block
-                append_row_warp<ACT, ACT>(p.k_new, p.v_new, p.new_slots[it.seq], it.seq, it.kvh, p.num_kv_heads,
-                                          BS, kTcD, p.num_blocks, const_cast<void*>(p.k_cache),
-                                          const_cast<void*>(p.v_cache), nullptr, nullptr, p.err, lane);
+                append_row_warp<ACT, CACHE>(p.k_new, p.v_new, p.new_slots[it.seq], it.seq, it.kvh, p.num_kv_heads,
+                                            BS, kTcD, p.num_blocks, const_cast<void*>(p.k_cache),
+                                            const_cast<void*>(p.v_cache), p.k_scale, p.v_scale, p.err, lane);
+            }
+            if constexpr (FP8) {
+                // Q as binary16 x 2^-qshift, written in the MMA's 128-byte swizzled
+                // layout (row g = head g, two 64-column halves 1 KB apart)
+                if (lane == 0 && k >= 1) good = tc_wait(&q_empty[0], (k - 1) & 1, abort_flag, p.err);
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) return false;
+                const float f = __uint_as_float(static_cast<uint32_t>(127 - it.qshift) << 23);  // 2^-qshift
+                const uint16_t* qg = static_cast<const uint16_t*>(p.q) +
+                                     (static_cast<int64_t>(it.seq) * p.num_q_heads + it.kvh * G) * kTcD;
+                for (int i = lane; i < G * kTcD / 8; i += 32) {
+                    const int g = i >> 4, cc = i & 15;  // head, 8-column chunk
+                    const uint4 u = *reinterpret_cast<const uint4*>(qg + g * kTcD + cc * 8);
+                    const uint16_t* e = reinterpret_cast<const uint16_t*>(&u);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        w[j] = static_cast<uint32_t>(float_to_act<kF16>(act_to_float<ACT>(e[2 * j]) * f)) |
+                               (static_cast<uint32_t>(float_to_act<kF16>(act_to_float<ACT>(e[2 * j + 1]) * f)) << 16);
+                    *reinterpret_cast<uint4*>(qbuf + (cc >> 3) * 1024 + g * 128 + (((cc & 7) ^ (g & 7)) * 16)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_full[0]);
+                ++nq;
+                for (int t = 0; t < it.n_tiles; ++t)
+                    if (!issue_tile(it, phys, t, &kmap)) return false;
+                return true;
             }
             if (lane == 0) {
                 // one Q buffer: item k's Q loads once the S MMAs of item k-1 have read it
@@ -451,8 +542,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // Leave only when every copy into this CTA's shared memory has landed.
         if (lane == 0) {
             const uint32_t first = use > static_cast<uint32_t>(NS) ? use - NS : 0;
-            for (uint32_t u = first; u < use; ++u)
-                if (!mbar_wait(&full[u % NS], (u / NS) & 1)) atomicOr(p.err, kErrTimeout);
+            if constexpr (!FP8) {
+                for (uint32_t u = first; u < use; ++u)
+                    if (!mbar_wait(&full[u % NS], (u / NS) & 1)) atomicOr(p.err, kErrTimeout);
+            }
+            if constexpr (FP8) {
+                for (uint32_t u = first; u < use; ++u)
+                    if (!mbar_wait(&stg_full[u % NS], (u / NS) & 1)) atomicOr(p.err, kErrTimeout);
+            }
             if (nq > 0 && !mbar_wait(&q_full[0], (nq - 1) & 1)) atomicOr(p.err, kErrTimeout);
         }
     } else if (warp == 1) {
@@ -534,7 +631,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int ksteps = (valid + 15) / 16;
                 // rows past the context inside the last 16-token step: zero them so
                 // that never-written pool slots cannot turn P = 0 into NaN
-                const int zero_rows = ksteps * 16 - valid;
+                const int zero_rows = FP8 ? 0 : ksteps * 16 - valid;  // E4M3: zeroed by the converting warps
                 if (zero_rows > 0) {
                     for (int i = lane; i < zero_rows * 16; i += 32) {
                         const int r = valid + (i >> 4);
@@ -582,7 +679,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!mbar_wait(final_bar, 0)) atomicOr(p.err, kErrTimeout);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------------ softmax + epilogue
         const int q4 = warp & 3;         // tensor-memory lane quarter of this warp
         const int row = q4 * 32 + lane;  // token of each tile (S) / dimension d (O)
@@ -598,11 +695,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool good =
                 __all_sync(0xffffffffu, tc_wait(&item_full[slot], (nread / kTcQueue) & 1, abort_flag, p.err));
             const int ci = good ? item_q[slot] : -1;
+            const int qshift = good ? item_shift[slot] : 0;
             ++nread;
             if (named_bar_or(3, 128, !good)) return -1;
             if (tid == 0) mbar_arrive(&item_empty[slot]);
             if (ci < 0) return 0;
             tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
+            it.qshift = qshift;
             return 1;
         };
         auto softmax = [&](const TcItem& it, int k) {
@@ -612,6 +711,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                           (k == 0 || tc_wait(&o_full[(k - 1) & 1], ((k - 1) >> 1) & 1,
                                                                              abort_flag, p.err)));
             float sc[kTcMaxTiles][G] = {};
+            // E4M3: S was computed on the stored codes and on q x 2^-qshift
+            const float sl = FP8 ? p.scale_log2 * *p.k_scale * __uint_as_float(static_cast<uint32_t>(127 + it.qshift) << 23)
+                                 : p.scale_log2;
             if (good) {
                 tc::fence_after_sync();
 #pragma unroll
@@ -627,7 +729,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const bool valid = t < it.n_tiles && t * kTcTile + row < it.n_tok;
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        sc[t][g] = valid ? sc[t][g] * p.scale_log2 : -INFINITY;
+                        sc[t][g] = valid ? sc[t][g] * sl : -INFINITY;
                         mx[g] = fmaxf(mx[g], sc[t][g]);
                     }
                 }
@@ -660,7 +762,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         sum[g] += pv;
                         const int chunk = ((row & 63) >> 3) ^ g;
                         *reinterpret_cast<uint16_t*>(pt + g * 128 + chunk * 16 + (row & 7) * 2) =
-                            float_to_act<ACT>(pv);
+                            float_to_act<OT>(pv);
                     }
                 }
             }
@@ -700,11 +802,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (tid == 0) mbar_arrive(&o_free[b]);
             const int d = row;
             const bool single = p.max_parts == 1 || s_lens[it.row] <= p.partition_size;
+            const float vmul = FP8 ? *p.v_scale : 1.0f;  // E4M3: O was computed on the stored codes
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float Mg = stats[b * 16 + g];
                 const float Lg = stats[b * 16 + 8 + g];
-                const float val = o[g] / Lg;
+                const float val = o[g] / Lg * vmul;
                 const size_t hrow = static_cast<size_t>(it.seq) * p.num_q_heads + it.kvh * G + g;
                 if (single) {
                     static_cast<uint16_t*>(p.out)[hrow * kTcD + d] = float_to_act<ACT>(val);
@@ -731,6 +834,83 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (ok) ok = epilogue(cur, k);
             rc = rn;
             cur = nxt;
+        }
+    }
+
+    if constexpr (FP8) {
+        if (warp >= 6) {
+            // -------------------------------------------- E4M3 tiles -> binary16
+            // The two warps follow the producer's tile order (K of item 0, then
+            // for each item n: K of n+1, V of n).  A ring stage holds the raw tile
+            // in its upper half; thread t rewrites rows t and t+64 in place as
+            // exact binary16 in the MMA's 128-byte swizzled layout: it loads the
+            // row's 128 bytes first, and the swizzle only permutes 16-byte chunks
+            // within that row, so no thread writes another thread's raw bytes.
+            // Rows past the context become zeros, so never-written pool slots
+            // cannot reach the products.
+            const int dt = threadIdx.x - 192;  // 0..63
+            uint32_t use = 0;
+            int nread = 0;
+            auto read_item = [&](TcItem& it) {
+                const int slot = nread % kTcQueue;
+                const bool good =
+                    __all_sync(0xffffffffu, tc_wait(&item_full[slot], (nread / kTcQueue) & 1, abort_flag, p.err));
+                const int ci = good ? item_q[slot] : -1;
+                ++nread;
+                if (!good) return -1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&item_empty[slot]);
+                if (ci < 0) return 0;
+                tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
+                return 1;
+            };
+            auto convert_tile = [&](const TcItem& it, int t) {
+                const int s = use % NS;
+                if (!__all_sync(0xffffffffu, tc_wait(&stg_full[s], (use / NS) & 1, abort_flag, p.err))) return false;
+                unsigned char* st = ring + s * kTcStage;
+                const int valid = min(kTcTile, it.n_tok - t * kTcTile);
+#pragma unroll
+                for (int rr = 0; rr < kTcTile / 64; ++rr) {
+                    const int r = dt + rr * 64;
+                    uint4 raw[8];  // raw[i]: chunk (i + r) & 7, rotated for distinct banks in a quarter warp
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        raw[i] = r < valid ? *reinterpret_cast<const uint4*>(st + kTcHalf + r * kTcD + ((i + r) & 7) * 16)
+                                           : make_uint4(0u, 0u, 0u, 0u);
+                    unsigned char* rowp = st + r * 128;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int c = (i + r) & 7;  // 16 E4M3 values: columns 16c .. 16c+15
+                        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+                        uint32_t h[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            h[j] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1))));
+                        const int half = c >> 2, c16 = (c & 3) * 2;  // 8-column chunks c16, c16+1 of the half
+                        *reinterpret_cast<uint4*>(rowp + half * kTcHalf + ((c16 ^ (r & 7)) * 16)) =
+                            make_uint4(h[0], h[1], h[2], h[3]);
+                        *reinterpret_cast<uint4*>(rowp + half * kTcHalf + (((c16 + 1) ^ (r & 7)) * 16)) =
+                            make_uint4(h[4], h[5], h[6], h[7]);
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
+                ++use;
+                return true;
+            };
+            TcItem cur, nxt;
+            int rc = read_item(cur);
+            bool ok = rc >= 0;
+            for (int t = 0; rc > 0 && ok && t < cur.n_tiles; ++t) ok = convert_tile(cur, t);
+            while (rc > 0 && ok) {
+                const int rn = read_item(nxt);
+                if (rn < 0) break;
+                for (int t = 0; rn > 0 && ok && t < nxt.n_tiles; ++t) ok = convert_tile(nxt, t);
+                for (int t = 0; ok && t < cur.n_tiles; ++t) ok = convert_tile(cur, t);
+                rc = rn;
+                cur = nxt;
+            }
         }
     }
 

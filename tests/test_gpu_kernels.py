@@ -298,6 +298,54 @@ def test_decode_tensor_core_parity(kernel_path, case, path, partition_size):
     assert_attention_close(got, want, TOL[act], rounding_slack=True)
 
 
+TC_FP8_CASES = [
+    # act, Hq, Hkv, bs (E4M3 cache)
+    ("bf16", 32, 4, 16),
+    ("f16", 16, 4, 32),
+    ("bf16", 16, 8, 16),
+]
+
+
+@pytest.mark.parametrize("case", TC_FP8_CASES, ids=lambda c: "-".join(map(str, c)))
+@pytest.mark.parametrize("path", [2, 3])
+@pytest.mark.parametrize("partition_size", [-1, 128, 256])
+def test_decode_tensor_core_e4m3_parity(kernel_path, case, path, partition_size):
+    """E4M3 cache on the tensor cores: tiles converted to binary16 in shared
+    memory, q as binary16 x 2^-shift, scales applied to S and O."""
+    pkv = kernel_path
+    act, Hq, Hkv, bs = case
+    if partition_size > 0 and partition_size % bs:
+        pytest.skip("partition must be a multiple of the block size")
+    if partition_size == -1 and Hq // Hkv < 4:
+        partition_size = 512
+    g = _gen(zlib.crc32(repr(("e4m3", case, path, partition_size)).encode()))
+    lens = [1, 2, 15, 16, 17, 100, 127, 128, 129, 255, 256, 257, 511, 512, 513, 1000, 1531]
+    q, kc, vc, tables, lens = _random_paged(g, len(lens), Hq, Hkv, 128, bs, lens, act, "e4m3")
+    ks, vs, scale = 0.021, 0.013, 1.0 / math.sqrt(128)
+    want = oracle.paged_decode(bits(q), ACT_CODE[DT[act]], bits(kc), bits(vc), oracle.E4M3, tables, lens, scale,
+                               k_scale=ks, v_scale=vs)
+    pkv.set_kernel_path(path)
+    got = _run_decode(pkv, q, kc, vc, tables, lens, scale, partition_size, ks, vs)
+    assert_attention_close(got, want, TOL["e4m3"], rounding_slack=True)
+
+
+def test_decode_tensor_core_e4m3_large_queries(kernel_path):
+    """Queries beyond the binary16 range take the exact power-of-two pre-scale."""
+    pkv = kernel_path
+    g = _gen(91)
+    lens = [40, 700, 1300]
+    q, kc, vc, tables, lens = _random_paged(g, 3, 32, 4, 128, 16, lens, "bf16", "e4m3")
+    q = (q.float() * 3.0e5).bfloat16()
+    q[1, 5] = q[1, 5] * 1.0e-6  # one group's head tiny, another's huge
+    ks, vs, scale = 1.0e-6, 0.013, 1.0 / math.sqrt(128)
+    want = oracle.paged_decode(bits(q), oracle.BF16, bits(kc), bits(vc), oracle.E4M3, tables, lens, scale,
+                               k_scale=ks, v_scale=vs)
+    for path in (2, 3):
+        pkv.set_kernel_path(path)
+        got = _run_decode(pkv, q, kc, vc, tables, lens, scale, -1, ks, vs)
+        assert_attention_close(got, want, TOL["e4m3"], rounding_slack=True)
+
+
 @pytest.mark.parametrize("path", [1, 2, 3])
 def test_decode_ignores_unwritten_slots(kernel_path, path):
     """NaN in the never-written slots of each sequence's last block does not reach the output."""
@@ -313,6 +361,24 @@ def test_decode_ignores_unwritten_slots(kernel_path, path):
     pkv.set_kernel_path(path)
     got = _run_decode(pkv, q, kc, vc, tables, lens, 0.09, -1)
     assert_attention_close(got, want, TOL["bf16"], rounding_slack=True)
+
+
+@pytest.mark.parametrize("path", [1, 2, 3])
+def test_decode_e4m3_ignores_unwritten_slots(kernel_path, path):
+    """NaN codes in the never-written slots of an E4M3 cache's last blocks do not reach the output."""
+    pkv = kernel_path
+    g = _gen(78)
+    lens = [5, 37, 130, 300]
+    q, kc, vc, tables, lens = _random_paged(g, 4, 32, 4, 128, 16, lens, "bf16", "e4m3")
+    want = oracle.paged_decode(bits(q), oracle.BF16, bits(kc), bits(vc), oracle.E4M3, tables, lens, 0.09,
+                               k_scale=0.02, v_scale=0.01)
+    for b, L in enumerate(lens):
+        last = int(tables[b, (L - 1) // 16])
+        kc[last, :, L % 16 or 16:] = 0x7F  # E4M3 NaN
+        vc[last, :, L % 16 or 16:] = 0xFF
+    pkv.set_kernel_path(path)
+    got = _run_decode(pkv, q, kc, vc, tables, lens, 0.09, -1, 0.02, 0.01)
+    assert_attention_close(got, want, TOL["e4m3"], rounding_slack=True)
 
 
 def test_tensor_path_refuses_unsupported_shapes(kernel_path):

@@ -38,7 +38,7 @@ def _sample(lens, n, seed):
     return np.array(sorted(pick))
 
 
-SAMPLES = {"tiny": 4, "llama7b": 6, "gqa_bs16": 6, "gqa_bs32": 6, "fp8_13b": 6, "long_gqa": 2}
+SAMPLES = {"tiny": 4, "llama7b": 6, "gqa_bs16": 6, "gqa_bs32": 6, "fp8_13b": 6, "long_gqa": 2, "gqa_fp8": 6}
 
 
 @pytest.mark.parametrize("name", list(SAMPLES))
