@@ -49,14 +49,13 @@
 namespace pkv {
 
 constexpr int kTcThreads = 192;
-constexpr int kTcThreadsFp8 = 256;            // E4M3 cache: two more warps convert the tiles
-constexpr int kTcFp8Stage = 128 * 128;        // one E4M3 tile in staging: 128 tokens x 128 bytes
 constexpr int kTcTile = 128;                  // tokens per tile (MMA M of S = K Q^T)
 constexpr int kTcMaxTiles = 4;                // partitions of at most 512 tokens
 constexpr int kTcD = 128;                     // head_dim served by this kernel
 constexpr int kTcN = 16;                      // MMA N: query heads padded to 16
 constexpr int kTcHalf = kTcTile * 128;        // one 64-column half of a tile: 128 rows x 128 B
 constexpr int kTcStage = 2 * kTcHalf;         // 32 KB
+constexpr int kTcStage8 = kTcTile * kTcD;     // E4M3 cache: 128 tokens x 128 one-byte codes, 16 KB
 constexpr int kTcQBuf = 3 * 1024;             // Q: two 8-row halves + 1 KB that rows 8-15 of half 1 alias
 constexpr int kTcPBuf = (2 * kTcMaxTiles + 1) * 1024;  // P: tile x token-half 8-row regions + alias pad
 constexpr int kTcSlotCols = kTcMaxTiles * kTcN + kTcN;  // S (4 x 16) + O (16) per buffer
@@ -66,16 +65,20 @@ constexpr int kTcSmemPerSm = 228 * 1024;      // shared memory of one SM, includ
 constexpr int kTcQueue = 4;                   // claimed items in flight between the roles
 constexpr int kTcLenBuckets = 8;              // length buckets of the partly filled partitions
 
-template <int NS, int NSS = 0>
+template <int NS, int STG = kTcStage>
 struct TcSmem {
     static constexpr int RING = 0;
-    static constexpr int Q = NS * kTcStage;
-    static constexpr int P = Q + kTcQBuf;
-    static constexpr int QUEUE = P + kTcPBuf;                  // item numbers [4], q shifts [4]
+    static constexpr int Q = NS * STG;
+    // E4M3 cache: 4 KB of Q operands (high + middle parts, low part + 8 zero rows)
+    // and two 8 KB P buffers (4 tiles x 16 rows x 128 one-byte codes)
+    static constexpr int P = Q + (STG == kTcStage8 ? 4096 : kTcQBuf);
+    static constexpr int PBUF = STG == kTcStage8 ? 8192 : kTcPBuf;  // one P buffer
+    static constexpr int PBUFS = STG == kTcStage8 ? 2 : 1;           // P buffers
+    static constexpr int QUEUE = P + PBUFS * PBUF;             // item numbers [4], q shifts [4]
     static constexpr int BARS = (QUEUE + 2 * kTcQueue * 4 + 7) / 8 * 8;
     // full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_free[2], final,
-    // item_full[4], item_empty[4], stg_full[NSS] (Q and P use entry 0 of their pairs)
-    static constexpr int NBARS = 2 * NS + 13 + 2 * kTcQueue + NSS;
+    // item_full[4], item_empty[4] (Q, and P when single, use entry 0 of their pairs)
+    static constexpr int NBARS = 2 * NS + 13 + 2 * kTcQueue;
     static constexpr int RED = BARS + NBARS * 8;
     static constexpr int RED_FLOATS = 64 + 32;  // red_max[4][8], red_sum[4][8], stats[2][2][8]
     static constexpr int MISC = RED + RED_FLOATS * 4;
@@ -87,7 +90,7 @@ struct TcSmem {
 
 struct TcItem {
     int seq, kvh, row, part, tok_begin, n_tok, n_tiles;
-    int qshift;  // E4M3 cache: q enters the MMA as binary16 times 2^-qshift
+    int qshift;  // E4M3 cache: q enters the MMA scaled by 2^-qshift
 };
 
 // Rows: a sequence (tables shared by its kv heads) or, with per-(sequence,
@@ -173,18 +176,42 @@ __device__ __forceinline__ int named_bar_or(int id, int count, int pred) {
     return r;
 }
 
-template <int ACT, int CACHE, int BS, int G, int NS, int NSS>
-__global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, CACHE == kE4M3 && NS < 5 ? 2 : 1)
+// x0, x1 -> E4M3 codes hi (nearest) and lo (nearest to the exact remainder
+// x - hi), x0 in the low byte of each.  hi + lo carries about 8 significant
+// bits of x; the remainder is exact in binary32 (hi lies within a factor of 2
+// of x).
+__device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+    __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
+    const float2 hv = __half22float2(*reinterpret_cast<__half2*>(&hr));
+    hi = h;
+    lo = __nv_cvt_float2_to_fp8x2(make_float2(x0 - hv.x, x1 - hv.y), __NV_SATFINITE, __NV_E4M3);
+}
+
+// x0, x1 -> three E4M3 codes each, hi + mid + lo carrying about 12
+// significant bits (enough for binary16 queries).
+__device__ __forceinline__ void split3_e4m3x2(float x0, float x1, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+    const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+    __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
+    const float2 hv = __half22float2(*reinterpret_cast<__half2*>(&hr));
+    hi = h;
+    split_e4m3x2(x0 - hv.x, x1 - hv.y, mid, lo);
+}
+
+template <int ACT, int CACHE, int BS, int G, int NS>
+__global__ void __launch_bounds__(kTcThreads, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const __grid_constant__ CUtensorMap qmap, const DecodeParams p) {
-    using S = TcSmem<NS, NSS>;
     constexpr bool FP8 = CACHE == kE4M3;
-    constexpr int OT = FP8 ? kF16 : ACT;  // the MMA's operand type
-    constexpr int THREADS = FP8 ? kTcThreadsFp8 : kTcThreads;
+    constexpr int STG = FP8 ? kTcStage8 : kTcStage;  // bytes of one ring stage
+    using S = TcSmem<NS, STG>;
+    constexpr int THREADS = kTcThreads;
     constexpr int BPT = kTcTile / BS;  // blocks per tile
-    constexpr uint32_t IDESC_S = tc::idesc_f16(128, kTcN, OT == kBF16, false, false);
-    constexpr uint32_t IDESC_O = tc::idesc_f16(128, kTcN, OT == kBF16, true, false);
-    static_assert(!FP8 || (NSS == NS && (ACT == kF16 || ACT == kBF16)), "E4M3 cache: one staging barrier per stage");
+    // E4M3 x E4M3 (kind::f8f6f4) has the same descriptor bits as binary16 x binary16
+    constexpr uint32_t IDESC_S = tc::idesc_f16(128, kTcN, !FP8 && ACT == kBF16, false, false);
+    constexpr uint32_t IDESC_O = tc::idesc_f16(128, kTcN, !FP8 && ACT == kBF16, true, false);
+    static_assert(!FP8 || G <= 8, "E4M3 cache: rows 0-7 of Q and P hold the high parts, rows 8-15 the low parts");
+    constexpr bool Q3 = FP8 && ACT == kF16;  // binary16 queries: three E4M3 parts
     static_assert(G == 2 || G == 4 || G == 8, "query heads per kv head");
     static_assert(kTcMaxTiles * kTcTile / BS <= 32, "one warp holds the table entries of an item");
 
@@ -210,7 +237,6 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
     uint64_t* final_bar = q_full + 12;
     uint64_t* item_full = q_full + 13;
     uint64_t* item_empty = item_full + kTcQueue;
-    uint64_t* stg_full = item_empty + kTcQueue;  // E4M3: the stage's raw tile has landed
     float* red_max = reinterpret_cast<float*>(sm + S::RED);
     float* red_sum = red_max + 32;
     float* stats = red_max + 64;  // [buffer][max, sum][8]
@@ -307,23 +333,19 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], FP8 ? 2 : 1);  // E4M3: the two converting warps fill a stage
+            mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 13; ++i) mbar_init(&q_full[i], 1);
         for (int i = 0; i < kTcQueue; ++i) {
             mbar_init(&item_full[i], 1);
-            // the MMA warp and the softmax warps (and the two converting warps)
-            mbar_init(&item_empty[i], FP8 ? 4 : 2);
+            mbar_init(&item_empty[i], 2);  // the MMA warp and the softmax warps
         }
-        for (int i = 0; i < NSS; ++i) mbar_init(&stg_full[i], 1);
         *abort_flag = 0;
         mbar_init_fence();
-        if constexpr (!FP8) {
-            tc::prefetch_tensormap(&kmap);
-            tc::prefetch_tensormap(&vmap);
-            tc::prefetch_tensormap(&qmap);
-        }
+        tc::prefetch_tensormap(&kmap);
+        tc::prefetch_tensormap(&vmap);
+        if constexpr (!FP8) tc::prefetch_tensormap(&qmap);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_base_smem, kTcTmemCols);
@@ -342,6 +364,11 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
         int nq = 0;        // Q tiles requested so far
         int nclaim = 0;    // queue entries written so far
         bool ok = true;
+        if constexpr (Q3) {
+            // rows 8-15 of the low-part operand stay zero (made visible to the
+            // MMA by the fence before the first Q is published)
+            for (int i = lane; i < 64; i += 32) reinterpret_cast<uint4*>(qbuf + 3072)[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
         if (lane == 0) {
             // sequences with a context length outside 1..max_blocks*BS are skipped; report them once
             for (int s = blockIdx.x; s < B; s += gridDim.x) {
@@ -362,8 +389,9 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
             if (ci >= 0) {
                 tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
                 if constexpr (FP8) {
-                    // q enters the MMA as binary16: scale it by 2^-qshift (exact)
-                    // so that its largest magnitude stays below 2^15
+                    // q enters the MMA as E4M3 high and low parts of q x 2^-qshift:
+                    // the exact power-of-2 scale puts its largest magnitude in
+                    // [128, 256), below the E4M3 maximum of 448
                     const uint16_t* qg = static_cast<const uint16_t*>(p.q) +
                                          (static_cast<int64_t>(it.seq) * p.num_q_heads + it.kvh * G) * kTcD;
                     float m = 0.f;
@@ -376,7 +404,7 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
                     const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m)
-                    it.qshift = m > 32768.f ? e - 14 : 0;
+                    it.qshift = m > 0.f ? min(120, max(-120, e - 7)) : 0;
                 }
             }
             bool good = true;
@@ -413,40 +441,15 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
         // Arm one ring stage with tile t of an item; `map` is the K or V tensor
         // map.  Lane 0 waits for the stage and sets its byte count; lane 2j+h
         // then loads half h of block j of the tile, so one warp instruction
-        // issues the tile's 2*BPT copies.
-        // E4M3: tile t's (block, kv head) tiles of 128 contiguous bytes per token
-        // go by 1-D bulk copies (one lane per block) into the upper half of a
-        // ring stage; the converting warps rewrite the stage in place as the
-        // MMA's binary16 layout.
-        auto issue_tile_fp8 = [&](const TcItem& it, int phys, int t, const void* cache) {
-            const int n_blk = (it.n_tok + BS - 1) / BS;
-            const int j = lane < BPT ? lane : 0;
-            const int pbj = __shfl_sync(0xffffffffu, phys, (t * BPT + j) & 31);
-            const bool mine = lane < BPT && t * BPT + j < n_blk && pbj >= 0;
-            const unsigned loads = __ballot_sync(0xffffffffu, mine);
-            const int s = use % NS;
-            bool good = true;
-            if (lane == 0) {
-                if (use >= NS) good = tc_wait(&empty[s], ((use / NS) - 1) & 1, abort_flag, p.err);
-                if (good) mbar_arrive_expect_tx(&stg_full[s], __popc(loads) * (BS * kTcD));
-            }
-            good = __shfl_sync(0xffffffffu, good, 0);
-            if (!good) return false;
-            if (mine)
-                bulk_copy_g2s(ring + s * kTcStage + kTcHalf + j * BS * kTcD,
-                              static_cast<const uint8_t*>(cache) +
-                                  (static_cast<int64_t>(pbj) * p.num_kv_heads + it.kvh) * BS * kTcD,
-                              BS * kTcD, &stg_full[s], policy);
-            ++use;
-            return true;
-        };
+        // issues the tile's 2*BPT copies.  E4M3: a token's 128 codes are one
+        // 128-byte row, so lane j loads block j whole.
         auto issue_tile = [&](const TcItem& it, int phys, int t, const CUtensorMap* map) {
-            if constexpr (FP8) return issue_tile_fp8(it, phys, t, map == &kmap ? p.k_cache : p.v_cache);
+            constexpr int PER_BLOCK = FP8 ? 1 : 2;  // copies per block
             const int n_blk = (it.n_tok + BS - 1) / BS;
-            const int j = (lane >> 1) < BPT ? (lane >> 1) : 0;
-            const int half = lane & 1;
+            const int j = (lane / PER_BLOCK) < BPT ? (lane / PER_BLOCK) : 0;
+            const int half = FP8 ? 0 : (lane & 1);
             const int pbj = __shfl_sync(0xffffffffu, phys, (t * BPT + j) & 31);
-            const bool mine = lane < 2 * BPT && t * BPT + j < n_blk && pbj >= 0;
+            const bool mine = lane < PER_BLOCK * BPT && t * BPT + j < n_blk && pbj >= 0;
             const unsigned loads = __ballot_sync(0xffffffffu, mine);
             const int s = use % NS;
             bool good = true;
@@ -458,8 +461,7 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
             if (!good) return false;
             if (mine) {
                 const int y = (pbj * p.num_kv_heads + it.kvh) * BS;
-                tc::tma_load_2d(ring + s * kTcStage + half * kTcHalf + j * BS * 128, map, half * 64, y, &full[s],
-                                policy);
+                tc::tma_load_2d(ring + s * STG + half * kTcHalf + j * BS * 128, map, half * 64, y, &full[s], policy);
             }
             ++use;
             return true;
@@ -474,25 +476,46 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
                                             const_cast<void*>(p.v_cache), p.k_scale, p.v_scale, p.err, lane);
             }
             if constexpr (FP8) {
-                // Q as binary16 x 2^-qshift, written in the MMA's 128-byte swizzled
-                // layout (row g = head g, two 64-column halves 1 KB apart)
+                // Q x 2^-qshift = hi + lo, both E4M3 (hi the nearest code, lo the
+                // nearest code to the exact remainder: about 8 significant bits in
+                // all, so every bfloat16 query is exact), written as the MMA's B
+                // operand in the 128-byte swizzled layout: row g holds hi of head
+                // g, row 8 + g lo (1 KB further).  Binary16 queries (11 bits) take
+                // a third part: rows 8 + g hold the middle part and the low part
+                // sits in a second operand 2 KB further, over 8 zero rows, so that a
+                // second MMA adds K lo^T into the same accumulator columns.
                 if (lane == 0 && k >= 1) good = tc_wait(&q_empty[0], (k - 1) & 1, abort_flag, p.err);
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) return false;
                 const float f = __uint_as_float(static_cast<uint32_t>(127 - it.qshift) << 23);  // 2^-qshift
                 const uint16_t* qg = static_cast<const uint16_t*>(p.q) +
                                      (static_cast<int64_t>(it.seq) * p.num_q_heads + it.kvh * G) * kTcD;
-                for (int i = lane; i < G * kTcD / 8; i += 32) {
-                    const int g = i >> 4, cc = i & 15;  // head, 8-column chunk
-                    const uint4 u = *reinterpret_cast<const uint4*>(qg + g * kTcD + cc * 8);
-                    const uint16_t* e = reinterpret_cast<const uint16_t*>(&u);
-                    uint32_t w[4];
+                for (int i = lane; i < G * kTcD / 16; i += 32) {
+                    const int g = i >> 3, c = i & 7;  // head, 16-column chunk
+                    const uint4 u0 = *reinterpret_cast<const uint4*>(qg + g * kTcD + c * 16);
+                    const uint4 u1 = *reinterpret_cast<const uint4*>(qg + g * kTcD + c * 16 + 8);
+                    const uint32_t e[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                    uint32_t hw[4], mw[4], lw[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        w[j] = static_cast<uint32_t>(float_to_act<kF16>(act_to_float<ACT>(e[2 * j]) * f)) |
-                               (static_cast<uint32_t>(float_to_act<kF16>(act_to_float<ACT>(e[2 * j + 1]) * f)) << 16);
-                    *reinterpret_cast<uint4*>(qbuf + (cc >> 3) * 1024 + g * 128 + (((cc & 7) ^ (g & 7)) * 16)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t hb[2], mb[2], lb[2];
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const uint32_t w = e[2 * j + h2];
+                            const float x0 = act_to_float<ACT>(static_cast<uint16_t>(w & 0xffffu)) * f;
+                            const float x1 = act_to_float<ACT>(static_cast<uint16_t>(w >> 16)) * f;
+                            if constexpr (Q3) split3_e4m3x2(x0, x1, hb[h2], mb[h2], lb[h2]);
+                            else split_e4m3x2(x0, x1, hb[h2], mb[h2]);
+                        }
+                        hw[j] = hb[0] | (hb[1] << 16);
+                        mw[j] = mb[0] | (mb[1] << 16);
+                        if constexpr (Q3) lw[j] = lb[0] | (lb[1] << 16);
+                    }
+                    const int off = g * 128 + ((c ^ g) * 16);
+                    *reinterpret_cast<uint4*>(qbuf + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(qbuf + 1024 + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+                    if constexpr (Q3)
+                        *reinterpret_cast<uint4*>(qbuf + 2048 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();
@@ -542,14 +565,8 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
         // Leave only when every copy into this CTA's shared memory has landed.
         if (lane == 0) {
             const uint32_t first = use > static_cast<uint32_t>(NS) ? use - NS : 0;
-            if constexpr (!FP8) {
-                for (uint32_t u = first; u < use; ++u)
-                    if (!mbar_wait(&full[u % NS], (u / NS) & 1)) atomicOr(p.err, kErrTimeout);
-            }
-            if constexpr (FP8) {
-                for (uint32_t u = first; u < use; ++u)
-                    if (!mbar_wait(&stg_full[u % NS], (u / NS) & 1)) atomicOr(p.err, kErrTimeout);
-            }
+            for (uint32_t u = first; u < use; ++u)
+                if (!mbar_wait(&full[u % NS], (u / NS) & 1)) atomicOr(p.err, kErrTimeout);
             if (nq > 0 && !mbar_wait(&q_full[0], (nq - 1) & 1)) atomicOr(p.err, kErrTimeout);
         }
     } else if (warp == 1) {
@@ -591,13 +608,25 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
                 if (!good) return false;
                 tc::fence_after_sync();
                 if (lane == 0) {
-                    const uint32_t kb = smem_addr(ring + s * kTcStage);
+                    const uint32_t kb = smem_addr(ring + s * STG);
+                    if constexpr (FP8) {
+                        // K = 32 codes (32 bytes of the 128-byte row) per MMA
 #pragma unroll
-                    for (int kk = 0; kk < kTcD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kTcHalf + (kk & 3) * 32;
-                        const uint32_t qoff = (kk >> 2) * 1024 + (kk & 3) * 32;
-                        tc::mma_f16(tmem + b * kTcSlotCols + t * kTcN, tc::desc_sw128(kb + off, 16, 1024),
-                                    tc::desc_sw128(qb + qoff, 16, 1024), IDESC_S, kk > 0);
+                        for (int kk = 0; kk < kTcD / 32; ++kk) {
+                            tc::mma_f8(tmem + b * kTcSlotCols + t * kTcN, tc::desc_sw128(kb + kk * 32, 16, 1024),
+                                       tc::desc_sw128(qb + kk * 32, 16, 1024), IDESC_S, kk > 0);
+                            if constexpr (Q3)  // + K lo^T into columns 0-7 (rows 8-15 of this operand are zero)
+                                tc::mma_f8(tmem + b * kTcSlotCols + t * kTcN, tc::desc_sw128(kb + kk * 32, 16, 1024),
+                                           tc::desc_sw128(qb + 2048 + kk * 32, 16, 1024), IDESC_S, 1u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < kTcD / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kTcHalf + (kk & 3) * 32;
+                            const uint32_t qoff = (kk >> 2) * 1024 + (kk & 3) * 32;
+                            tc::mma_f16(tmem + b * kTcSlotCols + t * kTcN, tc::desc_sw128(kb + off, 16, 1024),
+                                        tc::desc_sw128(qb + qoff, 16, 1024), IDESC_S, kk > 0);
+                        }
                     }
                     tc::commit(&empty[s]);
                 }
@@ -615,27 +644,30 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
             const int b = k & 1;
             bool good = true;
             if (lane == 0) {
-                good = tc_wait(&p_full[0], k & 1, abort_flag, p.err);
+                good = S::PBUFS == 2 ? tc_wait(&p_full[b], (k >> 1) & 1, abort_flag, p.err)
+                                     : tc_wait(&p_full[0], k & 1, abort_flag, p.err);
                 if (good && k >= 2) good = tc_wait(&o_free[b], ((k >> 1) - 1) & 1, abort_flag, p.err);
             }
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) return false;
             tc::fence_after_sync();
-            const uint32_t pbase = smem_addr(pbuf);
+            const uint32_t pbase = smem_addr(pbuf + (S::PBUFS == 2 ? b * S::PBUF : 0));
             for (int t = 0; t < it.n_tiles; ++t) {
                 const int s = use % NS;
                 good = __all_sync(0xffffffffu, tc_wait(&full[s], (use / NS) & 1, abort_flag, p.err));
                 if (!good) return false;
-                unsigned char* vb = ring + s * kTcStage;
+                unsigned char* vb = ring + s * STG;
                 const int valid = min(kTcTile, it.n_tok - t * kTcTile);
-                const int ksteps = (valid + 15) / 16;
-                // rows past the context inside the last 16-token step: zero them so
-                // that never-written pool slots cannot turn P = 0 into NaN
-                const int zero_rows = FP8 ? 0 : ksteps * 16 - valid;  // E4M3: zeroed by the converting warps
+                constexpr int KSTEP = FP8 ? 32 : 16;  // tokens per MMA
+                constexpr int CHUNKS = FP8 ? 8 : 16;  // 16-byte chunks per token row
+                const int ksteps = (valid + KSTEP - 1) / KSTEP;
+                // rows past the context inside the last step: zero them so that
+                // never-written pool slots cannot turn P = 0 into NaN
+                const int zero_rows = ksteps * KSTEP - valid;
                 if (zero_rows > 0) {
-                    for (int i = lane; i < zero_rows * 16; i += 32) {
-                        const int r = valid + (i >> 4);
-                        const int c = i & 15;  // 16-byte chunk of the 256-byte row (two halves)
+                    for (int i = lane; i < zero_rows * CHUNKS; i += 32) {
+                        const int r = valid + i / CHUNKS;
+                        const int c = i % CHUNKS;  // 16-byte chunk of the row (two halves when 16-bit)
                         *reinterpret_cast<uint4*>(vb + (c >> 3) * kTcHalf + r * 128 + (c & 7) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
@@ -646,10 +678,19 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
                 if (lane == 0) {
                     const uint32_t vaddr = smem_addr(vb);
                     for (int j = 0; j < ksteps; ++j) {
-                        const uint32_t poff = (2 * t + (j >> 2)) * 1024 + (j & 3) * 32;
-                        tc::mma_f16(tmem + b * kTcSlotCols + kTcMaxTiles * kTcN,
-                                    tc::desc_sw128(vaddr + j * 2048, kTcHalf, 1024),
-                                    tc::desc_sw128(pbase + poff, 16, 1024), IDESC_O, (t > 0 || j > 0) ? 1u : 0u);
+                        if constexpr (FP8) {
+                            // A = V^T: the 128 codes of a token are one 128-byte row, so
+                            // M = 128 is a single swizzle atom; 32 tokens = 4 KB per step
+                            tc::mma_f8(tmem + b * kTcSlotCols + kTcMaxTiles * kTcN,
+                                       tc::desc_sw128(vaddr + j * 4096, kTcStage8, 1024),
+                                       tc::desc_sw128(pbase + t * 2048 + j * 32, 16, 1024), IDESC_O,
+                                       (t > 0 || j > 0) ? 1u : 0u);
+                        } else {
+                            const uint32_t poff = (2 * t + (j >> 2)) * 1024 + (j & 3) * 32;
+                            tc::mma_f16(tmem + b * kTcSlotCols + kTcMaxTiles * kTcN,
+                                        tc::desc_sw128(vaddr + j * 2048, kTcHalf, 1024),
+                                        tc::desc_sw128(pbase + poff, 16, 1024), IDESC_O, (t > 0 || j > 0) ? 1u : 0u);
+                        }
                     }
                     tc::commit(&empty[s]);
                 }
@@ -706,20 +747,39 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
         };
         auto softmax = [&](const TcItem& it, int k) {
             const int b = k & 1;
-            // one P buffer: item k writes it once the O MMAs of item k-1 have read it
-            const bool good = __all_sync(0xffffffffu, tc_wait(&s_full[b], (k >> 1) & 1, abort_flag, p.err) &&
-                                                          (k == 0 || tc_wait(&o_full[(k - 1) & 1], ((k - 1) >> 1) & 1,
-                                                                             abort_flag, p.err)));
+            // one P buffer: item k writes it once the O MMAs of item k-1 have read
+            // it.  Two (E4M3): buffer b was last read by the O MMAs of item k-2,
+            // whose completion the epilogue of k-2 has already waited for.
+            const bool good = __all_sync(
+                0xffffffffu, tc_wait(&s_full[b], (k >> 1) & 1, abort_flag, p.err) &&
+                                 (k == 0 || S::PBUFS == 2 ||
+                                  tc_wait(&o_full[(k - 1) & 1], ((k - 1) >> 1) & 1, abort_flag, p.err)));
             float sc[kTcMaxTiles][G] = {};
             // E4M3: S was computed on the stored codes and on q x 2^-qshift
             const float sl = FP8 ? p.scale_log2 * *p.k_scale * __uint_as_float(static_cast<uint32_t>(127 + it.qshift) << 23)
                                  : p.scale_log2;
             if (good) {
                 tc::fence_after_sync();
+                if constexpr (FP8) {
+                    // column g: the high part of q, column 8 + g: the low part
+                    float lo[kTcMaxTiles][G] = {};
 #pragma unroll
-                for (int t = 0; t < kTcMaxTiles; ++t)
-                    if (t < it.n_tiles) tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN, sc[t]);
-                tc::tmem_wait_ld();
+                    for (int t = 0; t < kTcMaxTiles; ++t)
+                        if (t < it.n_tiles) {
+                            tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN, sc[t]);
+                            tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN + 8, lo[t]);
+                        }
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < kTcMaxTiles; ++t)
+#pragma unroll
+                        for (int g = 0; g < G; ++g) sc[t][g] += lo[t][g];
+                } else {
+#pragma unroll
+                    for (int t = 0; t < kTcMaxTiles; ++t)
+                        if (t < it.n_tiles) tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN, sc[t]);
+                    tc::tmem_wait_ld();
+                }
                 tc::fence_before_sync();  // these reads precede the next MMA into this S buffer
                 float mx[G];
 #pragma unroll
@@ -751,18 +811,40 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
                 M[g] = fmaxf(fmaxf(red_max[g], red_max[8 + g]), fmaxf(red_max[16 + g], red_max[24 + g]));
                 sum[g] = 0.f;
             }
-            unsigned char* pb = pbuf;
+            unsigned char* pb = pbuf + (S::PBUFS == 2 ? b * S::PBUF : 0);
 #pragma unroll
             for (int t = 0; t < kTcMaxTiles; ++t) {
                 if (t < it.n_tiles) {
-                    unsigned char* pt = pb + (2 * t + (row >> 6)) * 1024;
+                    if constexpr (FP8) {
+                        // P x 2^8 (at most 256) = hi + lo in E4M3: row g of the
+                        // tile's 2 KB operand holds hi of head g, row 8 + g lo
+                        unsigned char* pt = pb + t * 2048 + row;
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float pv = sc[t][g] == -INFINITY ? 0.f : exp2f(sc[t][g] - M[g]);
-                        sum[g] += pv;
-                        const int chunk = ((row & 63) >> 3) ^ g;
-                        *reinterpret_cast<uint16_t*>(pt + g * 128 + chunk * 16 + (row & 7) * 2) =
-                            float_to_act<OT>(pv);
+                        for (int g = 0; g < G; g += 2) {
+                            const float p0 = sc[t][g] == -INFINITY ? 0.f : exp2f(sc[t][g] - M[g]);
+                            const float p1 = sc[t][g + 1] == -INFINITY ? 0.f : exp2f(sc[t][g + 1] - M[g + 1]);
+                            sum[g] += p0;
+                            sum[g + 1] += p1;
+                            uint32_t hi, lo;
+                            split_e4m3x2(p0 * 256.f, p1 * 256.f, hi, lo);
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const int gg = g + h2;
+                                const int off = gg * 128 + ((((row >> 4) ^ gg) & 7) << 4) - (row & ~15);
+                                pt[off] = static_cast<unsigned char>(hi >> (8 * h2));
+                                pt[1024 + off] = static_cast<unsigned char>(lo >> (8 * h2));
+                            }
+                        }
+                    } else {
+                        unsigned char* pt = pb + (2 * t + (row >> 6)) * 1024;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const float pv = sc[t][g] == -INFINITY ? 0.f : exp2f(sc[t][g] - M[g]);
+                            sum[g] += pv;
+                            const int chunk = ((row & 63) >> 3) ^ g;
+                            *reinterpret_cast<uint16_t*>(pt + g * 128 + chunk * 16 + (row & 7) * 2) =
+                                float_to_act<ACT>(pv);
+                        }
                     }
                 }
             }
@@ -783,7 +865,7 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
                     stats[b * 16 + g] = M[g];
                     stats[b * 16 + 8 + g] = red_sum[g] + red_sum[8 + g] + red_sum[16 + g] + red_sum[24 + g];
                 }
-                mbar_arrive(&p_full[0]);
+                mbar_arrive(&p_full[S::PBUFS == 2 ? b : 0]);
             }
             return true;
         };
@@ -794,7 +876,15 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
             if (good) {
                 tc::fence_after_sync();
                 tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + kTcMaxTiles * kTcN, o);
-                tc::tmem_wait_ld();
+                if constexpr (FP8) {
+                    float lo[G];  // O of the low parts of P
+                    tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + kTcMaxTiles * kTcN + 8, lo);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int g = 0; g < G; ++g) o[g] += lo[g];
+                } else {
+                    tc::tmem_wait_ld();
+                }
                 tc::fence_before_sync();
             }
             // also orders the stats written by the softmax of this item before the reads below
@@ -802,7 +892,8 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
             if (tid == 0) mbar_arrive(&o_free[b]);
             const int d = row;
             const bool single = p.max_parts == 1 || s_lens[it.row] <= p.partition_size;
-            const float vmul = FP8 ? *p.v_scale : 1.0f;  // E4M3: O was computed on the stored codes
+            // E4M3: O was computed on the stored codes and on P x 2^8
+            const float vmul = FP8 ? *p.v_scale * (1.0f / 256.f) : 1.0f;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float Mg = stats[b * 16 + g];
@@ -834,83 +925,6 @@ __global__ void __launch_bounds__(CACHE == kE4M3 ? kTcThreadsFp8 : kTcThreads, C
             if (ok) ok = epilogue(cur, k);
             rc = rn;
             cur = nxt;
-        }
-    }
-
-    if constexpr (FP8) {
-        if (warp >= 6) {
-            // -------------------------------------------- E4M3 tiles -> binary16
-            // The two warps follow the producer's tile order (K of item 0, then
-            // for each item n: K of n+1, V of n).  A ring stage holds the raw tile
-            // in its upper half; thread t rewrites rows t and t+64 in place as
-            // exact binary16 in the MMA's 128-byte swizzled layout: it loads the
-            // row's 128 bytes first, and the swizzle only permutes 16-byte chunks
-            // within that row, so no thread writes another thread's raw bytes.
-            // Rows past the context become zeros, so never-written pool slots
-            // cannot reach the products.
-            const int dt = threadIdx.x - 192;  // 0..63
-            uint32_t use = 0;
-            int nread = 0;
-            auto read_item = [&](TcItem& it) {
-                const int slot = nread % kTcQueue;
-                const bool good =
-                    __all_sync(0xffffffffu, tc_wait(&item_full[slot], (nread / kTcQueue) & 1, abort_flag, p.err));
-                const int ci = good ? item_q[slot] : -1;
-                ++nread;
-                if (!good) return -1;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&item_empty[slot]);
-                if (ci < 0) return 0;
-                tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
-                return 1;
-            };
-            auto convert_tile = [&](const TcItem& it, int t) {
-                const int s = use % NS;
-                if (!__all_sync(0xffffffffu, tc_wait(&stg_full[s], (use / NS) & 1, abort_flag, p.err))) return false;
-                unsigned char* st = ring + s * kTcStage;
-                const int valid = min(kTcTile, it.n_tok - t * kTcTile);
-#pragma unroll
-                for (int rr = 0; rr < kTcTile / 64; ++rr) {
-                    const int r = dt + rr * 64;
-                    uint4 raw[8];  // raw[i]: chunk (i + r) & 7, rotated for distinct banks in a quarter warp
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        raw[i] = r < valid ? *reinterpret_cast<const uint4*>(st + kTcHalf + r * kTcD + ((i + r) & 7) * 16)
-                                           : make_uint4(0u, 0u, 0u, 0u);
-                    unsigned char* rowp = st + r * 128;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int c = (i + r) & 7;  // 16 E4M3 values: columns 16c .. 16c+15
-                        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-                        uint32_t h[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            h[j] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1))));
-                        const int half = c >> 2, c16 = (c & 3) * 2;  // 8-column chunks c16, c16+1 of the half
-                        *reinterpret_cast<uint4*>(rowp + half * kTcHalf + ((c16 ^ (r & 7)) * 16)) =
-                            make_uint4(h[0], h[1], h[2], h[3]);
-                        *reinterpret_cast<uint4*>(rowp + half * kTcHalf + (((c16 + 1) ^ (r & 7)) * 16)) =
-                            make_uint4(h[4], h[5], h[6], h[7]);
-                    }
-                }
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full[s]);
-                ++use;
-                return true;
-            };
-            TcItem cur, nxt;
-            int rc = read_item(cur);
-            bool ok = rc >= 0;
-            for (int t = 0; rc > 0 && ok && t < cur.n_tiles; ++t) ok = convert_tile(cur, t);
-            while (rc > 0 && ok) {
-                const int rn = read_item(nxt);
-                if (rn < 0) break;
-                for (int t = 0; rn > 0 && ok && t < nxt.n_tiles; ++t) ok = convert_tile(nxt, t);
-                for (int t = 0; ok && t < cur.n_tiles; ++t) ok = convert_tile(cur, t);
-                rc = rn;
-                cur = nxt;
-            }
         }
     }
 

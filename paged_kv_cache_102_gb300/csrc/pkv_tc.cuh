@@ -38,6 +38,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         : "memory");
 }
 
+// The same for E4M3 / E5M2 / 6- and 4-bit operands (kind::f8f6f4, K = 32).
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] = A * B (+ D if accumulate), A in tensor memory (lane = row, each
 // 32-bit column two consecutive K elements), B described in shared memory.
 __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -57,8 +68,9 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
                  : "memory");
 }
 
-// Instruction descriptor for kind::f16 with an f32 accumulator.
-// bits 4-5 D type (1 = f32), 7-9 A type, 10-12 B type (0 = f16, 1 = bf16),
+// Instruction descriptor for kind::f16 (and kind::f8f6f4) with an f32
+// accumulator.  bits 4-5 D type (1 = f32), 7-9 A type, 10-12 B type (kind::f16:
+// 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3),
 // 15 A major (0 = K, 1 = MN), 16 B major, 17-22 N/8, 24-28 M/16.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a_mn_major, bool b_mn_major) {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |

@@ -310,8 +310,8 @@ TC_FP8_CASES = [
 @pytest.mark.parametrize("path", [2, 3])
 @pytest.mark.parametrize("partition_size", [-1, 128, 256])
 def test_decode_tensor_core_e4m3_parity(kernel_path, case, path, partition_size):
-    """E4M3 cache on the tensor cores: tiles converted to binary16 in shared
-    memory, q as binary16 x 2^-shift, scales applied to S and O."""
+    """E4M3 cache on the tensor cores: E4M3 tiles straight into the MMA, q and
+    P as E4M3 high + low parts, scales applied to S and O."""
     pkv = kernel_path
     act, Hq, Hkv, bs = case
     if partition_size > 0 and partition_size % bs:
@@ -330,15 +330,34 @@ def test_decode_tensor_core_e4m3_parity(kernel_path, case, path, partition_size)
 
 
 def test_decode_tensor_core_e4m3_large_queries(kernel_path):
-    """Queries beyond the binary16 range take the exact power-of-two pre-scale."""
+    """Queries far beyond the E4M3 range take the exact power-of-two pre-scale;
+    a group whose queries are all zero gives the plain mean of V."""
     pkv = kernel_path
     g = _gen(91)
     lens = [40, 700, 1300]
     q, kc, vc, tables, lens = _random_paged(g, 3, 32, 4, 128, 16, lens, "bf16", "e4m3")
     q = (q.float() * 3.0e5).bfloat16()
     q[1, 5] = q[1, 5] * 1.0e-6  # one group's head tiny, another's huge
+    q[2, 8:16] = 0.0  # a whole group of zeros
     ks, vs, scale = 1.0e-6, 0.013, 1.0 / math.sqrt(128)
     want = oracle.paged_decode(bits(q), oracle.BF16, bits(kc), bits(vc), oracle.E4M3, tables, lens, scale,
+                               k_scale=ks, v_scale=vs)
+    for path in (2, 3):
+        pkv.set_kernel_path(path)
+        got = _run_decode(pkv, q, kc, vc, tables, lens, scale, -1, ks, vs)
+        assert_attention_close(got, want, TOL["e4m3"], rounding_slack=True)
+
+
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+def test_decode_tensor_core_e4m3_peaked_softmax(kernel_path, act):
+    """Scores spread over tens of units: the weights span many orders of
+    magnitude, and the small ones must still count (P's low E4M3 part)."""
+    pkv = kernel_path
+    g = _gen(92)
+    lens = [33, 511, 1024, 1700]
+    q, kc, vc, tables, lens = _random_paged(g, 4, 32, 4, 128, 32, lens, act, "e4m3")
+    ks, vs, scale = 0.1, 0.013, 1.0 / math.sqrt(128)  # scores with a standard deviation near 10
+    want = oracle.paged_decode(bits(q), ACT_CODE[DT[act]], bits(kc), bits(vc), oracle.E4M3, tables, lens, scale,
                                k_scale=ks, v_scale=vs)
     for path in (2, 3):
         pkv.set_kernel_path(path)
