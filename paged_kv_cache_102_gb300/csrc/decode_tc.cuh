@@ -48,7 +48,7 @@
 
 namespace pkv {
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 256;
 constexpr int kTcTile = 128;                  // tokens per tile (MMA M of S = K Q^T)
 constexpr int kTcMaxTiles = 4;                // partitions of at most 512 tokens
 constexpr int kTcD = 128;                     // head_dim served by this kernel
@@ -74,8 +74,8 @@ struct TcSmem {
     static constexpr int P = Q + (STG == kTcStage8 ? 4096 : kTcQBuf);
     static constexpr int PBUF = STG == kTcStage8 ? 8192 : kTcPBuf;  // one P buffer
     static constexpr int PBUFS = STG == kTcStage8 ? 2 : 1;           // P buffers
-    static constexpr int QUEUE = P + PBUFS * PBUF;             // item numbers [4], q shifts [4]
-    static constexpr int BARS = (QUEUE + 2 * kTcQueue * 4 + 7) / 8 * 8;
+    static constexpr int QUEUE = P + PBUFS * PBUF;  // item numbers [4], q shifts [4], block-table entries [4][32]
+    static constexpr int BARS = (QUEUE + 2 * kTcQueue * 4 + kTcQueue * 32 * 4 + 7) / 8 * 8;
     // full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_free[2], final,
     // item_full[4], item_empty[4] (Q, and P when single, use entry 0 of their pairs)
     static constexpr int NBARS = 2 * NS + 13 + 2 * kTcQueue;
@@ -199,7 +199,7 @@ __device__ __forceinline__ void split3_e4m3x2(float x0, float x1, uint32_t& hi, 
 }
 
 template <int ACT, int CACHE, int BS, int G, int NS>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const __grid_constant__ CUtensorMap qmap, const DecodeParams p) {
     constexpr bool FP8 = CACHE == kE4M3;
@@ -209,7 +209,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int BPT = kTcTile / BS;  // blocks per tile
     // E4M3 x E4M3 (kind::f8f6f4) has the same descriptor bits as binary16 x binary16
     constexpr uint32_t IDESC_S = tc::idesc_f16(128, kTcN, !FP8 && ACT == kBF16, false, false);
-    constexpr uint32_t IDESC_O = tc::idesc_f16(128, kTcN, !FP8 && ACT == kBF16, true, false);
+    // E4M3: P is the B operand in the MN-major layout without swizzle (a token's
+    // 16 codes, 8 high and 8 low parts, are 16 contiguous bytes)
+    constexpr uint32_t IDESC_O = tc::idesc_f16(128, kTcN, !FP8 && ACT == kBF16, true, FP8);
     static_assert(!FP8 || G <= 8, "E4M3 cache: rows 0-7 of Q and P hold the high parts, rows 8-15 the low parts");
     constexpr bool Q3 = FP8 && ACT == kF16;  // binary16 queries: three E4M3 parts
     static_assert(G == 2 || G == 4 || G == 8, "query heads per kv head");
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* pbuf = sm + S::P;
     volatile int* item_q = reinterpret_cast<volatile int*>(sm + S::QUEUE);
     volatile int* item_shift = item_q + kTcQueue;
+    volatile int* item_phys = item_shift + kTcQueue;  // [slot][32]: the item's physical blocks
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BARS);
     uint64_t* full = bars;
     uint64_t* empty = bars + NS;
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < 13; ++i) mbar_init(&q_full[i], 1);
         for (int i = 0; i < kTcQueue; ++i) {
             mbar_init(&item_full[i], 1);
-            mbar_init(&item_empty[i], 2);  // the MMA warp and the softmax warps
+            mbar_init(&item_empty[i], 4);  // the two tile producers, the MMA warp and the softmax warps
         }
         *abort_flag = 0;
         mbar_init_fence();
@@ -357,18 +360,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = *tmem_base_smem;
     const int total = s_prefix[B] + heads_per_row * s_prefix[B + 1];
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- producer
-        const uint64_t policy = l2_policy_evict_first();
-        uint32_t use = 0;  // ring stages armed so far
-        int nq = 0;        // Q tiles requested so far
-        int nclaim = 0;    // queue entries written so far
-        bool ok = true;
-        if constexpr (Q3) {
-            // rows 8-15 of the low-part operand stay zero (made visible to the
-            // MMA by the fence before the first Q is published)
-            for (int i = lane; i < 64; i += 32) reinterpret_cast<uint4*>(qbuf + 3072)[i] = make_uint4(0u, 0u, 0u, 0u);
+    const uint64_t policy = l2_policy_evict_first();
+    // Two producer warps share the ring: one arms the even stage uses, the other
+    // the odd ones (the lanes of one copy instruction are issued one after the
+    // other, so a single warp cannot issue the small copies fast enough).  Both
+    // follow the same tile order; `use` counts every tile, armed here or not.
+    // Arm one ring stage with tile t of an item; `map` is the K or V tensor map.
+    // Lane 0 waits for the stage and sets its byte count; lane 2j+h then loads
+    // half h of block j of the tile, so one warp instruction issues the tile's
+    // 2*BPT copies.  E4M3: a token's 128 codes are one 128-byte row, so lane j
+    // loads block j whole.
+    auto issue_tile = [&](uint32_t& use, uint32_t parity, const TcItem& it, int phys, int t,
+                          const CUtensorMap* map) {
+        if ((use & 1u) != parity) {
+            ++use;
+            return true;
         }
+        constexpr int PER_BLOCK = FP8 ? 1 : 2;  // copies per block
+        const int n_blk = (it.n_tok + BS - 1) / BS;
+        const int j = (lane / PER_BLOCK) < BPT ? (lane / PER_BLOCK) : 0;
+        const int half = FP8 ? 0 : (lane & 1);
+        const int pbj = __shfl_sync(0xffffffffu, phys, (t * BPT + j) & 31);
+        const bool mine = lane < PER_BLOCK * BPT && t * BPT + j < n_blk && pbj >= 0;
+        const unsigned loads = __ballot_sync(0xffffffffu, mine);
+        const int s = use % NS;
+        bool good = true;
+        if (lane == 0) {
+            if (use >= NS) good = tc_wait(&empty[s], ((use / NS) - 1) & 1, abort_flag, p.err);
+            if (good) mbar_arrive_expect_tx(&full[s], __popc(loads) * (BS * 128));
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) return false;
+        if (mine) {
+            const int y = (pbj * p.num_kv_heads + it.kvh) * BS;
+            tc::tma_load_2d(ring + s * STG + half * kTcHalf + j * BS * 128, map, half * 64, y, &full[s], policy);
+        }
+        ++use;
+        return true;
+    };
+    // A producer leaves only when every copy it issued into this CTA's shared
+    // memory has landed.
+    auto drain = [&](uint32_t use, uint32_t parity) {
+        if (lane == 0) {
+            const uint32_t first = use > static_cast<uint32_t>(NS) ? use - NS : 0;
+            for (uint32_t u = first; u < use; ++u)
+                if ((u & 1u) == parity && !mbar_wait(&full[u % NS], (u / NS) & 1)) atomicOr(p.err, kErrTimeout);
+        }
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ scheduler
+        // Claims items, reads their block-table entries, performs the fused
+        // append and publishes each item through the queue, up to four ahead of
+        // the slowest reader.
+        int nclaim = 0;  // queue entries written so far
+        bool ok = true;
         if (lane == 0) {
             // sequences with a context length outside 1..max_blocks*BS are skipped; report them once
             for (int s = blockIdx.x; s < B; s += gridDim.x) {
@@ -376,9 +422,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (L < 1 || L > p.max_blocks_per_seq * BS) atomicOr(p.err, kErrBadLen);
             }
         }
+        auto table_entry = [&](const TcItem& it) {
+            const int n_blk = (it.n_tok + BS - 1) / BS;
+            int phys = -1;
+            if (lane < n_blk) {
+                phys = p.block_tables[it.seq * p.table_seq_stride + it.kvh * p.table_kvh_stride + it.tok_begin / BS +
+                                      lane];
+                if (phys < 0 || phys >= p.num_blocks) {
+                    atomicOr(p.err, kErrBadBlock);
+                    phys = -1;
+                }
+            }
+            return phys;
+        };
         // Claim the next item for this CTA and pass it to the other roles; false
         // at the end of the work (the end marker is queued) or on an abort.
-        auto claim = [&](TcItem& it) {
+        auto claim = [&](TcItem& it, int& phys) {
+            phys = -1;
             int ci = -1;
             if (lane == 0) {
                 ci = atomicAdd(p.work_counter, 1);
@@ -406,75 +466,72 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m)
                     it.qshift = m > 0.f ? min(120, max(-120, e - 7)) : 0;
                 }
-            }
-            bool good = true;
-            if (lane == 0) {
-                const int slot = nclaim % kTcQueue;
-                if (nclaim >= kTcQueue) good = tc_wait(&item_empty[slot], ((nclaim / kTcQueue) - 1) & 1, abort_flag, p.err);
-                if (good) {
-                    item_q[slot] = ci;
-                    item_shift[slot] = it.qshift;
-                    mbar_arrive(&item_full[slot]);
+                phys = table_entry(it);
+                if (p.new_slots != nullptr && it.tok_begin + it.n_tok == s_lens[it.row]) {
+                    // fused append: this item holds the new (last) token; write it
+                    // before the item is published, so before any copy of its block
+                    append_row_warp<ACT, CACHE>(p.k_new, p.v_new, p.new_slots[it.seq], it.seq, it.kvh,
+                                                p.num_kv_heads, BS, kTcD, p.num_blocks, const_cast<void*>(p.k_cache),
+                                                const_cast<void*>(p.v_cache), p.k_scale, p.v_scale, p.err, lane);
                 }
             }
+            const int slot = nclaim % kTcQueue;
+            bool good = true;
+            if (lane == 0 && nclaim >= kTcQueue)
+                good = tc_wait(&item_empty[slot], ((nclaim / kTcQueue) - 1) & 1, abort_flag, p.err);
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) {
                 ok = false;
                 return false;
             }
+            item_phys[slot * 32 + lane] = phys;
+            if (lane == 0) {
+                item_q[slot] = ci;
+                item_shift[slot] = it.qshift;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_full[slot]);
             ++nclaim;
             return ci >= 0;
         };
-        auto table_entry = [&](const TcItem& it) {
-            const int n_blk = (it.n_tok + BS - 1) / BS;
-            int phys = -1;
-            if (lane < n_blk) {
-                phys = p.block_tables[it.seq * p.table_seq_stride + it.kvh * p.table_kvh_stride + it.tok_begin / BS +
-                                      lane];
-                if (phys < 0 || phys >= p.num_blocks) {
-                    atomicOr(p.err, kErrBadBlock);
-                    phys = -1;
-                }
-            }
-            return phys;
+        TcItem it;
+        int phys = -1;
+        while (ok && claim(it, phys)) {
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------------------ tile producers
+        // Warp 6 arms the even stage uses and writes Q, warp 7 arms the odd
+        // uses.  Both read the items from the queue and follow one tile order:
+        // K(0), then for each n: K(n+1), V(n).
+        const uint32_t parity = static_cast<uint32_t>(warp - 6);
+        uint32_t use = 0;  // ring stage uses so far (either parity)
+        int nq = 0;        // Q tiles written so far
+        int nread = 0;
+        if constexpr (Q3) {
+            // rows 8-15 of the low-part operand stay zero (made visible to the
+            // MMA by the fence before the first Q is published)
+            if (parity == 0)
+                for (int i = lane; i < 64; i += 32) reinterpret_cast<uint4*>(qbuf + 3072)[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        auto read_item = [&](TcItem& it, int& phys) {
+            const int slot = nread % kTcQueue;
+            const bool good =
+                __all_sync(0xffffffffu, tc_wait(&item_full[slot], (nread / kTcQueue) & 1, abort_flag, p.err));
+            ++nread;
+            if (!good) return -1;
+            const int ci = item_q[slot];
+            it.qshift = item_shift[slot];
+            phys = item_phys[slot * 32 + lane];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[slot]);
+            if (ci < 0) return 0;
+            // (an appended row of this item was written, and fenced for the copy
+            // engine, by the scheduler before it published the item)
+            tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
+            return 1;
         };
-        // Arm one ring stage with tile t of an item; `map` is the K or V tensor
-        // map.  Lane 0 waits for the stage and sets its byte count; lane 2j+h
-        // then loads half h of block j of the tile, so one warp instruction
-        // issues the tile's 2*BPT copies.  E4M3: a token's 128 codes are one
-        // 128-byte row, so lane j loads block j whole.
-        auto issue_tile = [&](const TcItem& it, int phys, int t, const CUtensorMap* map) {
-            constexpr int PER_BLOCK = FP8 ? 1 : 2;  // copies per block
-            const int n_blk = (it.n_tok + BS - 1) / BS;
-            const int j = (lane / PER_BLOCK) < BPT ? (lane / PER_BLOCK) : 0;
-            const int half = FP8 ? 0 : (lane & 1);
-            const int pbj = __shfl_sync(0xffffffffu, phys, (t * BPT + j) & 31);
-            const bool mine = lane < PER_BLOCK * BPT && t * BPT + j < n_blk && pbj >= 0;
-            const unsigned loads = __ballot_sync(0xffffffffu, mine);
-            const int s = use % NS;
+        auto issue_q = [&](const TcItem& it, int k) {
             bool good = true;
-            if (lane == 0) {
-                if (use >= NS) good = tc_wait(&empty[s], ((use / NS) - 1) & 1, abort_flag, p.err);
-                if (good) mbar_arrive_expect_tx(&full[s], __popc(loads) * (BS * 128));
-            }
-            good = __shfl_sync(0xffffffffu, good, 0);
-            if (!good) return false;
-            if (mine) {
-                const int y = (pbj * p.num_kv_heads + it.kvh) * BS;
-                tc::tma_load_2d(ring + s * STG + half * kTcHalf + j * BS * 128, map, half * 64, y, &full[s], policy);
-            }
-            ++use;
-            return true;
-        };
-        auto issue_q_and_k = [&](const TcItem& it, int phys, int k) {
-            bool good = true;
-            if (p.new_slots != nullptr && it.tok_begin + it.n_tok == s_lens[it.row]) {
-                // fused append: this item holds the new (last) token; write it before
-                // the TMA reads of its block
-                append_row_warp<ACT, CACHE>(p.k_new, p.v_new, p.new_slots[it.seq], it.seq, it.kvh, p.num_kv_heads,
-                                            BS, kTcD, p.num_blocks, const_cast<void*>(p.k_cache),
-                                            const_cast<void*>(p.v_cache), p.k_scale, p.v_scale, p.err, lane);
-            }
             if constexpr (FP8) {
                 // Q x 2^-qshift = hi + lo, both E4M3 (hi the nearest code, lo the
                 // nearest code to the exact remainder: about 8 significant bits in
@@ -521,8 +578,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&q_full[0]);
                 ++nq;
-                for (int t = 0; t < it.n_tiles; ++t)
-                    if (!issue_tile(it, phys, t, &kmap)) return false;
                 return true;
             }
             if (lane == 0) {
@@ -538,37 +593,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) return false;
             ++nq;
-            for (int t = 0; t < it.n_tiles; ++t)
-                if (!issue_tile(it, phys, t, &kmap)) return false;
             return true;
         };
 
-        TcItem cur, nxt, nn;
-        bool have_c = claim(cur);
-        int phys_c = have_c ? table_entry(cur) : -1;
-        bool have_n = have_c && claim(nxt);
-        int phys_n = have_n ? table_entry(nxt) : -1;
-        if (have_c && ok) ok = issue_q_and_k(cur, phys_c, 0);
-        for (int k = 0; have_c && ok; ++k) {
-            const bool have_nn = have_n && claim(nn);  // claims run two items ahead of the V loads
-            const int phys_nn = have_nn ? table_entry(nn) : -1;
-            if (!ok) break;
-            if (have_n) ok = issue_q_and_k(nxt, phys_n, k + 1);
-            for (int t = 0; t < cur.n_tiles && ok; ++t) ok = issue_tile(cur, phys_c, t, &vmap);
-            have_c = have_n;
+        auto issue_k = [&](const TcItem& it, int phys, int k) {
+            if (parity == 0 && !issue_q(it, k)) return false;
+            for (int t = 0; t < it.n_tiles; ++t)
+                if (!issue_tile(use, parity, it, phys, t, &kmap)) return false;
+            return true;
+        };
+        TcItem cur, nxt;
+        int phys_c = -1, phys_n = -1;
+        int rc = read_item(cur, phys_c);
+        bool ok = rc >= 0;
+        if (rc > 0) ok = issue_k(cur, phys_c, 0);
+        for (int k = 0; rc > 0 && ok; ++k) {
+            const int rn = read_item(nxt, phys_n);
+            if (rn < 0) break;
+            if (rn > 0) ok = issue_k(nxt, phys_n, k + 1);
+            for (int t = 0; ok && t < cur.n_tiles; ++t) ok = issue_tile(use, parity, cur, phys_c, t, &vmap);
+            rc = rn;
             cur = nxt;
             phys_c = phys_n;
-            have_n = have_nn;
-            nxt = nn;
-            phys_n = phys_nn;
         }
-        // Leave only when every copy into this CTA's shared memory has landed.
-        if (lane == 0) {
-            const uint32_t first = use > static_cast<uint32_t>(NS) ? use - NS : 0;
-            for (uint32_t u = first; u < use; ++u)
-                if (!mbar_wait(&full[u % NS], (u / NS) & 1)) atomicOr(p.err, kErrTimeout);
-            if (nq > 0 && !mbar_wait(&q_full[0], (nq - 1) & 1)) atomicOr(p.err, kErrTimeout);
-        }
+        drain(use, parity);
+        if (parity == 0 && lane == 0 && nq > 0 && !mbar_wait(&q_full[0], (nq - 1) & 1)) atomicOr(p.err, kErrTimeout);
     } else if (warp == 1) {
         // --------------------------------------------------------------------- MMA
         uint32_t use = 0;
@@ -681,9 +730,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if constexpr (FP8) {
                             // A = V^T: the 128 codes of a token are one 128-byte row, so
                             // M = 128 is a single swizzle atom; 32 tokens = 4 KB per step
+                            // B = P: core matrices of 8 tokens x 16 bytes, 128 B apart
                             tc::mma_f8(tmem + b * kTcSlotCols + kTcMaxTiles * kTcN,
                                        tc::desc_sw128(vaddr + j * 4096, kTcStage8, 1024),
-                                       tc::desc_sw128(pbase + t * 2048 + j * 32, 16, 1024), IDESC_O,
+                                       tc::desc_noswizzle(pbase + t * 2048 + j * 512, 128, 2048), IDESC_O,
                                        (t > 0 || j > 0) ? 1u : 0u);
                         } else {
                             const uint32_t poff = (2 * t + (j >> 2)) * 1024 + (j & 3) * 32;
@@ -816,9 +866,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int t = 0; t < kTcMaxTiles; ++t) {
                 if (t < it.n_tiles) {
                     if constexpr (FP8) {
-                        // P x 2^8 (at most 256) = hi + lo in E4M3: row g of the
-                        // tile's 2 KB operand holds hi of head g, row 8 + g lo
-                        unsigned char* pt = pb + t * 2048 + row;
+                        // P x 2^8 (at most 256) = hi + lo in E4M3; token `row` of
+                        // tile t holds 16 bytes: hi of heads 0-7, then lo of heads 0-7
+                        uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
                         for (int g = 0; g < G; g += 2) {
                             const float p0 = sc[t][g] == -INFINITY ? 0.f : exp2f(sc[t][g] - M[g]);
@@ -827,14 +877,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             sum[g + 1] += p1;
                             uint32_t hi, lo;
                             split_e4m3x2(p0 * 256.f, p1 * 256.f, hi, lo);
-#pragma unroll
-                            for (int h2 = 0; h2 < 2; ++h2) {
-                                const int gg = g + h2;
-                                const int off = gg * 128 + ((((row >> 4) ^ gg) & 7) << 4) - (row & ~15);
-                                pt[off] = static_cast<unsigned char>(hi >> (8 * h2));
-                                pt[1024 + off] = static_cast<unsigned char>(lo >> (8 * h2));
-                            }
+                            w[g >> 2] |= hi << (8 * (g & 3));
+                            w[2 + (g >> 2)] |= lo << (8 * (g & 3));
                         }
+                        *reinterpret_cast<uint4*>(pb + t * 2048 + row * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                     } else {
                         unsigned char* pt = pb + (2 * t + (row >> 6)) * 1024;
 #pragma unroll
