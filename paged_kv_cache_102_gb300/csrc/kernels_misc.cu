@@ -199,7 +199,54 @@ __global__ void __launch_bounds__(32 * kMergeWarps) paged_decode_merge_kernel(Me
     }
     float acc[V] = {};
     float den = 0.f;
-    if (active) {
+    if (active && W == 1 && n_parts <= 32) {
+        // One round trip for up to 16 partitions: part `lane`'s (max, sum) and
+        // the first 16 partial vectors are all loaded before any is used.
+        constexpr int C = 16;
+        const float* ml = p.ws_ml + row * p.max_parts * 2;
+        const float* o = p.ws_o + row * p.max_parts * D + lane * V;
+        const float2 a =
+            lane < n_parts ? *reinterpret_cast<const float2*>(ml + 2 * lane) : make_float2(-INFINITY, 0.f);
+        float x[C][V];
+#pragma unroll
+        for (int k = 0; k < C; ++k) {
+            if (k < n_parts) {
+                if constexpr (V == 4) {
+                    const float4 t = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(k) * D);
+                    x[k][0] = t.x;
+                    x[k][1] = t.y;
+                    x[k][2] = t.z;
+                    x[k][3] = t.w;
+                } else {
+                    const float2 t = *reinterpret_cast<const float2*>(o + static_cast<int64_t>(k) * D);
+                    x[k][0] = t.x;
+                    x[k][1] = t.y;
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < V; ++v) x[k][v] = 0.f;
+            }
+        }
+        float M = a.x;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float w = lane < n_parts ? a.y * exp2f(a.x - M) : 0.f;
+        den = w;
+#pragma unroll
+        for (int k = 0; k < C; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] = fmaf(wk, x[k][v], acc[v]);
+        }
+        for (int k = C; k < n_parts; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+            const float* src = o + static_cast<int64_t>(k) * D;
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] = fmaf(wk, src[v], acc[v]);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    } else if (active) {
         const float* ml = p.ws_ml + row * p.max_parts * 2;
         const float* o = p.ws_o + row * p.max_parts * D + lane * V;
         float M = -INFINITY;

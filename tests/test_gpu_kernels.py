@@ -365,6 +365,24 @@ def test_decode_tensor_core_e4m3_peaked_softmax(kernel_path, act):
         assert_attention_close(got, want, TOL["e4m3"], rounding_slack=True)
 
 
+@pytest.mark.parametrize("path", [1, 3])
+def test_decode_split_k_merge_many_rows(kernel_path, path):
+    """4096 (sequence, query head) rows, so the merge takes one warp per row;
+    1, 16, 17, 32, 33 and 35 partitions cover its 16-wide batch, the tail
+    after it and the fallback beyond 32 (partitions of 64 tokens)."""
+    pkv = kernel_path
+    g = _gen(93)
+    B, Hq, Hkv, bs = 64, 64, 8, 16
+    lens = torch.randint(1, 2241, (B,), generator=g).numpy()
+    lens[:8] = [1, 64, 1024, 1025, 2048, 2049, 2240, 63]
+    q, kc, vc, tables, lens = _random_paged(g, B, Hq, Hkv, 128, bs, lens, "bf16", "bf16")
+    scale = 1.0 / math.sqrt(128)
+    want = oracle.paged_decode(bits(q), oracle.BF16, bits(kc), bits(vc), oracle.BF16, tables, lens, scale)
+    pkv.set_kernel_path(path)
+    got = _run_decode(pkv, q, kc, vc, tables, lens, scale, 64)
+    assert_attention_close(got, want, TOL["bf16"], rounding_slack=True)
+
+
 @pytest.mark.parametrize("path", [1, 2, 3])
 def test_decode_ignores_unwritten_slots(kernel_path, path):
     """NaN in the never-written slots of each sequence's last block does not reach the output."""
