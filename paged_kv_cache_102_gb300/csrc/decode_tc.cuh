@@ -16,16 +16,23 @@
 // longest first (8 length buckets; a stable counting sort in shared memory
 // that every CTA computes alike).
 // The kernel is persistent and balances ragged lengths dynamically: the
-// producer of each CTA claims the next item number from a counter in the
-// workspace (zeroed before the launch) and passes it to the other roles
-// through a 4-entry queue in shared memory.  Roles (192 threads):
-//  warp 0    producer: claims, block-table entries (fetched one item ahead) ->
-//            2-D TMA loads (128-byte swizzle) of each (block, kv head) tile as
-//            two 64-column halves of head_dim, into a ring of 128-token
-//            stages.  Order: K(0), then for each item n: K(n+1), V(n).
+// scheduler warp of each CTA claims the next item number from a counter in the
+// workspace (zeroed before the launch) and passes it, with the item's block-
+// table entries, to the other roles through a 4-entry queue in shared memory.
+// Roles (256 threads):
+//  warp 0    scheduler: claims, block-table entries, the fused append (fenced
+//            for the copy engine before the item is published), and for an
+//            E4M3 cache the exact power-of-2 scale of the item's queries.
+//  warps 6-7 producers: 2-D TMA loads (128-byte swizzle) of each (block, kv
+//            head) tile into a ring of 128-token stages, warp 6 the even
+//            stage uses and Q, warp 7 the odd uses.  16-bit caches: a tile is
+//            two 64-column halves of head_dim; E4M3: one 128-byte row per
+//            token.  Order: K(0), then for each item n: K(n+1), V(n).
 //  warp 1    MMA: S = K Q^T (M = 128 tokens, N = 16, K = 128) into a
 //            16-column slot per tile; O = V^T P (M = 128 = D, N = 16, K =
-//            tokens).  Order: S(0), then for each n: S(n+1), O(n).
+//            tokens).  Order: S(0), then for each n: S(n+1), O(n).  16-bit:
+//            kind::f16; E4M3: kind::f8f6f4 with q and P as E4M3 high + low
+//            parts in rows 0-7 and 8-15 of the N = 16 operand.
 //  warps 2-5 softmax + epilogue: thread i owns tensor-memory lane i (token i
 //            of a tile for S, dimension i of O).  Partition-wide max and sum
 //            per head (the whole partition's scores sit in tensor memory, so
@@ -33,11 +40,11 @@
 //            memory layout, then the output (one partition) or the split-K
 //            partial (m, l, O/l).  Order: softmax(0), then for each n:
 //            softmax(n+1), epilogue(n).
-// S, O (tensor memory), Q and P (shared memory) are double-buffered by item
-// parity, so the MMA and softmax roles run one item ahead of the epilogue.
-// N = 16 columns are computed for at most 8 heads: rows 8-15 of the Q and P
-// operands alias the next 1 KB of shared memory, and the matching output
-// columns are never read.
+// S and O (tensor memory) are double-buffered by item parity, so the MMA and
+// softmax roles run one item ahead of the epilogue; Q is single, P single
+// (16-bit) or double (E4M3).  With 16-bit operands N = 16 columns are
+// computed for at most 8 heads: rows 8-15 of the Q and P operands alias the
+// next 1 KB of shared memory, and the matching output columns are never read.
 // Every barrier wait is bounded (kWaitLimitNs); on a timeout the CTA stops
 // issuing work, drains its in-flight copies and MMAs, frees tensor memory and
 // reports kErrTimeout.
