@@ -183,7 +183,9 @@ size_t pkv_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int h
  * possible context means a single pass), or -1 if partition_size is not
  * accepted.  PKV_PARTITION_AUTO gives 512 when num_q_heads/num_kv_heads >= 4,
  * head_dim is 128 and num_seqs <= 2048 (the shapes the tensor-core kernel
- * serves), else 1024.  Host only.
+ * serves), or 256 when num_seqs * num_kv_heads * the number of 512-token
+ * partitions of the longest possible context is in [256, 1024); else 1024.
+ * Host only.
  */
 int pkv_resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                int max_blocks_per_seq, int block_size, int partition_size);

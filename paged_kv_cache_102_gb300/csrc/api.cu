@@ -44,6 +44,13 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr int kStageTokens = 32;  // tokens per shared-memory stage of the decode kernel
 constexpr int kAutoPartition = 1024;
 constexpr int kAutoPartitionGrouped = 512;
+// Grouped shapes with a few hundred (sequence, kv head, partition) items get
+// 256-token partitions, so that the persistent grid's CTAs each get several
+// to balance.  Below 256 items every CTA has at most about one, and smaller
+// partitions only add merge work (QUEST's sparse decode of 8 x 8 rows: 41.0 ->
+// 37.1 us at 4096 selected tokens a row, 29.4 -> 28.7 at 2048, 20.6 -> 22.6 at
+// 1024 if it were applied there).
+constexpr long long kAutoGroupedItemsLow = 256, kAutoGroupedItemsHigh = 1024;
 constexpr size_t kWorkspaceHeader = 256;  // work counter of the tensor-core path
 
 std::atomic<int> g_kernel_path{PKV_PATH_AUTO};
@@ -107,6 +114,11 @@ int pkv_resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, 
         const int G = num_q_heads / num_kv_heads;
         const bool grouped = G >= 4 && head_dim == 128 && num_seqs <= 2048;
         P = grouped ? kAutoPartitionGrouped : kAutoPartition;
+        if (grouped) {
+            auto items = [&](long long p) { return static_cast<long long>(num_seqs) * num_kv_heads * ((max_ctx + p - 1) / p); };
+            if (items(P) >= kAutoGroupedItemsLow && items(P) < kAutoGroupedItemsHigh && (P / 2) % block_size == 0)
+                P /= 2;
+        }
     } else if (partition_size > 0) {
         if (partition_size % kStageTokens != 0 || partition_size % block_size != 0) return -1;
         P = partition_size;

@@ -67,7 +67,10 @@ def test_partition_and_workspace_sizes(pkv_lib):
     assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 129, 16, 0) == 2080   # single pass: 2064 -> 2080
     assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 129, 16, 512) == 512
     assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 129, 16, -1) == 1024  # CUDA-core shapes
-    assert lib.pkv_resolve_partition_size(4, 64, 8, 128, 129, 16, -1) == 512  # tensor-core shapes
+    # tensor-core shapes: 512 tokens, or 256 with 256..1023 (sequence, kv head, 512-token partition) items
+    assert lib.pkv_resolve_partition_size(4, 64, 8, 128, 129, 16, -1) == 512   # 4 * 8 * 5 = 160 items
+    assert lib.pkv_resolve_partition_size(16, 64, 8, 128, 129, 16, -1) == 256  # 16 * 8 * 5 = 640 items
+    assert lib.pkv_resolve_partition_size(32, 64, 8, 128, 129, 16, -1) == 512  # 32 * 8 * 5 = 1280 items
     assert lib.pkv_resolve_partition_size(4, 64, 8, 64, 129, 16, -1) == 1024
     assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 8, 16, 512) == 128    # whole context fits one
     assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 129, 32, 48) == -1
