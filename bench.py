@@ -333,15 +333,18 @@ def run_native(args):
 
         prep(h_in[0])
 
+        # the fused step as a serving loop issues it: validated and marshalled
+        # once for its fixed buffers, then one C call per step
+        plan = pkv.DecodePlan(dv_["q"], vals["k_cache"], vals["v_cache"], dv_["tables"], dv_["lens"], wl.scale,
+                              out=st["out"], k_scale=ks, v_scale=vs, partition_size=ps, workspace=ws,
+                              stream=stream_e2e, k_new=dv_["k_new"], v_new=dv_["v_new"], slot_mapping=dv_["slots"])
+
         def e2e_step():
             hb = h_in[state["n"] % 2]
             state["n"] += 1
             d_in.copy_(hb, non_blocking=True)
             if args.fused:
-                pkv.paged_attention_decode_append(dv_["q"], dv_["k_new"], dv_["v_new"], dv_["slots"],
-                                                  vals["k_cache"], vals["v_cache"], dv_["tables"], dv_["lens"],
-                                                  wl.scale, out=st["out"], k_scale=ks, v_scale=vs,
-                                                  partition_size=ps, workspace=ws)
+                plan.run()
             else:
                 pkv.paged_kv_append(dv_["k_new"], dv_["v_new"], dv_["slots"], vals["k_cache"], vals["v_cache"], ks,
                                     vs)
@@ -363,7 +366,9 @@ def run_native(args):
         te, _ = reduce_over_ranks(dist, dev, te, {})
         e2e = {"value": round(job["bytes"] / te / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(te * 1e3, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "seq_steps_per_s": round(job["seqs"] / te, 1)}
+               "seq_steps_per_s": round(job["seqs"] / te, 1),
+               "call": "DecodePlan.run (fused append + decode)" if args.fused else
+                       "paged_kv_append + paged_attention_decode"}
         if not torch.equal(out_h, st["out"].cpu()):
             raise RuntimeError("e2e output differs from the device-resident step")
 

@@ -34,7 +34,8 @@ DEV_BAD_BLOCK, DEV_BAD_CONTEXT_LEN, DEV_BAD_SLOT, DEV_BAD_PAIR, DEV_WAIT_TIMEOUT
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR, PATH_TENSOR_2CTA = 0, 1, 2, 3
 SWAP_OUT, SWAP_IN = 0, 1
 
-__all__ = ["paged_kv_append", "paged_attention_decode", "paged_attention_decode_append", "paged_block_copy",
+__all__ = ["paged_kv_append", "paged_attention_decode", "paged_attention_decode_append", "DecodePlan",
+           "paged_block_copy",
            "paged_block_swap", "paged_attention_decode_sparse", "quest_block_minmax", "quest_append_minmax",
            "quest_select", "workspace_size",
            "resolve_partition_size", "device_error", "set_kernel_path", "BlockManager", "OutOfBlocks", "PagedKVError",
@@ -145,6 +146,15 @@ def _workspace(device, stream_ptr: int, nbytes: int) -> torch.Tensor:
 def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, k_scale=None,
                            v_scale=None, partition_size=PARTITION_AUTO, workspace=None, stream=None):
     """Decode attention for q [B, Hq, D] over the paged cache; returns out [B, Hq, D]."""
+    args, out, _ = _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out, k_scale, v_scale,
+                                partition_size, workspace, stream)
+    _native.call("paged_attention_decode", *args)
+    return out
+
+
+def _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out, k_scale, v_scale, partition_size,
+                 workspace, stream):
+    """Validated C arguments of paged_attention_decode, the output and the workspace."""
     B, Hq, D = q.shape
     NB, Hkv, bs, D2 = k_cache.shape
     if D2 != D or v_cache.shape != k_cache.shape:
@@ -167,10 +177,10 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
         if need:
             workspace = _workspace(q.device, s, need)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _native.call("paged_attention_decode", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks,
-                 _ptr(context_lens), B, Hq, Hkv, bs, D, NB, float(scale), _ptr(out), _code(q), _code(k_cache),
-                 _ptr(k_scale), _ptr(v_scale), int(partition_size), _ptr(workspace), ws_bytes, s)
-    return out
+    args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), B, Hq, Hkv,
+            bs, D, NB, float(scale), _ptr(out), _code(q), _code(k_cache), _ptr(k_scale), _ptr(v_scale),
+            int(partition_size), _ptr(workspace), ws_bytes, s)
+    return args, out, workspace
 
 
 def paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, context_lens, scale,
@@ -178,6 +188,15 @@ def paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cach
                                   stream=None):
     """Append each sequence's new K/V row (k_new, v_new [B, Hkv, D] at slot_mapping int64 [B]) and decode, in one
     launch; context_lens count the new token.  Returns out [B, Hq, D]."""
+    args, out, _ = _decode_append_args(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, context_lens,
+                                       scale, out, k_scale, v_scale, partition_size, workspace, stream)
+    _native.call("paged_attention_decode_append", *args)
+    return out
+
+
+def _decode_append_args(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, context_lens, scale, out,
+                        k_scale, v_scale, partition_size, workspace, stream):
+    """Validated C arguments of paged_attention_decode_append, the output and the workspace."""
     B, Hq, D = q.shape
     NB, Hkv, bs, D2 = k_cache.shape
     if D2 != D or v_cache.shape != k_cache.shape or k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape:
@@ -199,11 +218,47 @@ def paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cach
         if need:
             workspace = _workspace(q.device, s, need)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _native.call("paged_attention_decode_append", _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
-                 _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), B, Hq, Hkv, bs, D,
-                 NB, float(scale), _ptr(out), _code(q), _code(k_cache), _ptr(k_scale), _ptr(v_scale),
-                 int(partition_size), _ptr(workspace), ws_bytes, s)
-    return out
+    args = (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            max_blocks, _ptr(context_lens), B, Hq, Hkv, bs, D, NB, float(scale), _ptr(out), _code(q),
+            _code(k_cache), _ptr(k_scale), _ptr(v_scale), int(partition_size), _ptr(workspace), ws_bytes, s)
+    return args, out, workspace
+
+
+class DecodePlan:
+    """One decode step for fixed tensors, validated and marshalled once.
+
+    With k_new, v_new and slot_mapping it is paged_attention_decode_append,
+    else paged_attention_decode; the arguments mean the same.  run() issues
+    the step with a single C call and returns `out`.  Between runs the
+    tensors' contents may change (new queries, tables, lengths), their
+    storage, shapes and types may not.  Every run goes on the stream given
+    here (default: the current stream at construction)."""
+
+    def __init__(self, q, k_cache, v_cache, block_tables, context_lens, scale, out=None, k_scale=None, v_scale=None,
+                 partition_size=PARTITION_AUTO, workspace=None, stream=None, k_new=None, v_new=None,
+                 slot_mapping=None):
+        given = [t is not None for t in (k_new, v_new, slot_mapping)]
+        if any(given) and not all(given):
+            raise ValueError("DecodePlan: k_new, v_new and slot_mapping go together")
+        if all(given):
+            self.func = "paged_attention_decode_append"
+            self._args, self.out, ws = _decode_append_args(q, k_new, v_new, slot_mapping, k_cache, v_cache,
+                                                           block_tables, context_lens, scale, out, k_scale, v_scale,
+                                                           partition_size, workspace, stream)
+        else:
+            self.func = "paged_attention_decode"
+            self._args, self.out, ws = _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                                                    k_scale, v_scale, partition_size, workspace, stream)
+        # the plan holds its tensors so that their storage outlives it
+        self._tensors = (q, k_cache, v_cache, block_tables, context_lens, k_scale, v_scale, ws, k_new, v_new,
+                         slot_mapping)
+        self._fn = _native.function(self.func)
+
+    def run(self):
+        code = self._fn(*self._args)
+        if code != 0:
+            _native.check(self.func, code)
+        return self.out
 
 
 def quest_block_minmax(k_cache, block_tables, context_lens, kmeta=None, stream=None):

@@ -97,6 +97,14 @@ def check(func: str, code: int) -> None:
         raise PagedKVError(func, code, lib().pkv_last_error().decode())
 
 
+def function(func: str):
+    """The library's C function `func` with its declared argument types."""
+    fn = _fns.get(func)
+    if fn is None:
+        fn = _fns[func] = getattr(lib(), func)
+    return fn
+
+
 def call(func: str, *args) -> None:
     fn = _fns.get(func)
     if fn is None:

@@ -93,3 +93,9 @@ def test_append_and_copy_argument_checks(pkv_lib):
     assert lib.paged_block_copy(a, a, a, 1, 16, 100, None) == 1  # not a multiple of 16
     assert lib.paged_block_copy(a, a, a, 0, 16, 4096, None) == 0  # empty
     assert lib.paged_block_copy(None, a, a, 1, 16, 4096, None) == 1
+
+
+def test_decode_plan_wants_all_append_tensors(pkv_lib):
+    """A fused plan needs k_new, v_new and slot_mapping together (checked before any device work)."""
+    with pytest.raises(ValueError):
+        pkv_lib.DecodePlan(None, None, None, None, None, 0.1, k_new=object())

@@ -471,3 +471,36 @@ def test_output_to_pinned_host_memory(kernel_path, path):
     got = pkv.paged_attention_decode(q, kc, vc, t_d, l_d, 0.088, out=host, partition_size=512)
     torch.cuda.synchronize()
     assert got is host and torch.equal(host, want.cpu())
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_plan_matches_the_calls(kernel_path, fused):
+    """DecodePlan.run() gives the same bits as the one-shot call, and sees new
+    contents of its fixed tensors between runs."""
+    pkv = kernel_path
+    g = _gen(94)
+    lens = [40, 300, 1025, 7]
+    q, kc, vc, tables, lens = _random_paged(g, 4, 32, 4, 128, 16, lens, "bf16", "bf16")
+    q, kc, vc = q.cuda(), kc.cuda(), vc.cuda()
+    tab, ln = torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
+    kw = {}
+    if fused:
+        kw = dict(k_new=torch.randn(4, 4, 128, generator=g).bfloat16().cuda(),
+                  v_new=torch.randn(4, 4, 128, generator=g).bfloat16().cuda(),
+                  slot_mapping=torch.tensor([int(tables[b, (L - 1) // 16]) * 16 + (L - 1) % 16
+                                             for b, L in enumerate(lens)], dtype=torch.int64).cuda())
+    out = torch.empty_like(q)
+    pkv.set_kernel_path(pkv.PATH_AUTO)
+    plan = pkv.DecodePlan(q, kc, vc, tab, ln, 0.088, out=out, **kw)
+    for step in range(2):
+        if step == 1:
+            q.copy_(torch.randn(q.shape, generator=g).bfloat16())  # new queries in the same storage
+        kc2, vc2 = kc.clone(), vc.clone()
+        got = plan.run().clone()
+        if fused:
+            want = pkv.paged_attention_decode_append(q, kw["k_new"], kw["v_new"], kw["slot_mapping"], kc2, vc2, tab,
+                                                     ln, 0.088)
+        else:
+            want = pkv.paged_attention_decode(q, kc2, vc2, tab, ln, 0.088)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
