@@ -7,6 +7,8 @@ library's C++ host code.  There is no CPU fallback: a missing library raises.
 
     paged_kv_append(k, v, slot_mapping, k_cache, v_cache, ...)
     paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ...)
+    paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cache, ...)
+    DecodePlan(...).run()   # either of the two above, marshalled once for fixed buffers
     paged_block_copy(k_cache, v_cache, src_dst_pairs, ...)
     BlockManager(num_blocks, block_size, free_list=None)
 
