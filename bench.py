@@ -230,6 +230,11 @@ def run_native(args):
     ks, vs = vals.get("k_scale"), vals.get("v_scale")
     stream = torch.cuda.current_stream(dev)
     npairs = st["pairs"].shape[0]
+    # the fused step through the public plan API: validated and marshalled once
+    # for the step's fixed buffers, one C call per step
+    plan = pkv.DecodePlan(vals["q"], vals["k_cache"], vals["v_cache"], st["tables"], st["lens"], wl.scale,
+                          out=st["out"], k_scale=ks, v_scale=vs, partition_size=ps, workspace=ws, stream=stream,
+                          k_new=vals["k_new"], v_new=vals["v_new"], slot_mapping=st["slots"]) if args.fused else None
 
     def step(ev_mid=None):
         if npairs:
@@ -237,9 +242,7 @@ def run_native(args):
         if args.fused:
             if ev_mid is not None:
                 ev_mid.record(stream)
-            pkv.paged_attention_decode_append(vals["q"], vals["k_new"], vals["v_new"], st["slots"], vals["k_cache"],
-                                              vals["v_cache"], st["tables"], st["lens"], wl.scale, out=st["out"],
-                                              k_scale=ks, v_scale=vs, partition_size=ps, workspace=ws)
+            plan.run()
             return
         pkv.paged_kv_append(vals["k_new"], vals["v_new"], st["slots"], vals["k_cache"], vals["v_cache"], ks, vs)
         if ev_mid is not None:
