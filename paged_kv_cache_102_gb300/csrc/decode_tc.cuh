@@ -76,15 +76,17 @@ template <int NS, int STG = kTcStage>
 struct TcSmem {
     static constexpr int RING = 0;
     static constexpr int Q = NS * STG;
-    // E4M3 cache: 4 KB of Q operands (high + middle parts, low part + 8 zero rows)
-    // and two 8 KB P buffers (4 tiles x 16 rows x 128 one-byte codes)
-    static constexpr int P = Q + (STG == kTcStage8 ? 4096 : kTcQBuf);
+    // E4M3 cache: two 4 KB Q buffers (high + middle parts, low part + 8 zero
+    // rows) and two 8 KB P buffers (4 tiles x 16 rows x 128 one-byte codes)
+    static constexpr int QBUF = STG == kTcStage8 ? 4096 : kTcQBuf;  // one Q buffer
+    static constexpr int QBUFS = STG == kTcStage8 ? 2 : 1;          // Q buffers
+    static constexpr int P = Q + QBUFS * QBUF;
     static constexpr int PBUF = STG == kTcStage8 ? 8192 : kTcPBuf;  // one P buffer
     static constexpr int PBUFS = STG == kTcStage8 ? 2 : 1;           // P buffers
     static constexpr int QUEUE = P + PBUFS * PBUF;  // item numbers [4], q shifts [4], block-table entries [4][32]
     static constexpr int BARS = (QUEUE + 2 * kTcQueue * 4 + kTcQueue * 32 * 4 + 7) / 8 * 8;
     // full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_free[2], final,
-    // item_full[4], item_empty[4] (Q, and P when single, use entry 0 of their pairs)
+    // item_full[4], item_empty[4] (a single Q or P buffer uses entry 0 of its pair)
     static constexpr int NBARS = 2 * NS + 13 + 2 * kTcQueue;
     static constexpr int RED = BARS + NBARS * 8;
     static constexpr int RED_FLOATS = 64 + 32;  // red_max[4][8], red_sum[4][8], stats[2][2][8]
@@ -518,7 +520,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             // rows 8-15 of the low-part operand stay zero (made visible to the
             // MMA by the fence before the first Q is published)
             if (parity == 0)
-                for (int i = lane; i < 64; i += 32) reinterpret_cast<uint4*>(qbuf + 3072)[i] = make_uint4(0u, 0u, 0u, 0u);
+                for (int i = lane; i < 64 * S::QBUFS; i += 32)
+                    reinterpret_cast<uint4*>(qbuf + (i >> 6) * S::QBUF + 3072)[i & 63] = make_uint4(0u, 0u, 0u, 0u);
         }
         auto read_item = [&](TcItem& it, int& phys) {
             const int slot = nread % kTcQueue;
@@ -548,9 +551,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 // a third part: rows 8 + g hold the middle part and the low part
                 // sits in a second operand 2 KB further, over 8 zero rows, so that a
                 // second MMA adds K lo^T into the same accumulator columns.
-                if (lane == 0 && k >= 1) good = tc_wait(&q_empty[0], (k - 1) & 1, abort_flag, p.err);
+                // two Q buffers: item k's Q goes in once the S MMAs of item k-2 have read it
+                const int qb = k & 1;
+                if (lane == 0 && k >= 2) good = tc_wait(&q_empty[qb], ((k >> 1) - 1) & 1, abort_flag, p.err);
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) return false;
+                unsigned char* qbuf_k = qbuf + qb * S::QBUF;
                 const float f = __uint_as_float(static_cast<uint32_t>(127 - it.qshift) << 23);  // 2^-qshift
                 const uint16_t* qg = static_cast<const uint16_t*>(p.q) +
                                      (static_cast<int64_t>(it.seq) * p.num_q_heads + it.kvh * G) * kTcD;
@@ -576,14 +582,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                         if constexpr (Q3) lw[j] = lb[0] | (lb[1] << 16);
                     }
                     const int off = g * 128 + ((c ^ g) * 16);
-                    *reinterpret_cast<uint4*>(qbuf + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(qbuf + 1024 + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+                    *reinterpret_cast<uint4*>(qbuf_k + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(qbuf_k + 1024 + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
                     if constexpr (Q3)
-                        *reinterpret_cast<uint4*>(qbuf + 2048 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        *reinterpret_cast<uint4*>(qbuf_k + 2048 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&q_full[0]);
+                if (lane == 0) mbar_arrive(&q_full[qb]);
                 ++nq;
                 return true;
             }
@@ -624,7 +630,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             phys_c = phys_n;
         }
         drain(use, parity);
-        if (parity == 0 && lane == 0 && nq > 0 && !mbar_wait(&q_full[0], (nq - 1) & 1)) atomicOr(p.err, kErrTimeout);
+        if (parity == 0 && lane == 0 && nq > 0) {
+            const int last = nq - 1;  // the last Q written (16-bit: loaded by TMA) has landed
+            const bool landed = S::QBUFS == 2 ? mbar_wait(&q_full[last & 1], (last >> 1) & 1)
+                                              : mbar_wait(&q_full[0], last & 1);
+            if (!landed) atomicOr(p.err, kErrTimeout);
+        }
     } else if (warp == 1) {
         // --------------------------------------------------------------------- MMA
         uint32_t use = 0;
@@ -652,11 +663,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         auto mma_s = [&](const TcItem& it, int k) {
             const int b = k & 1;
             bool good = true;
-            if (lane == 0) good = tc_wait(&q_full[0], k & 1, abort_flag, p.err);
+            const int qi = S::QBUFS == 2 ? (k & 1) : 0;  // Q buffer of item k
+            if (lane == 0) good = tc_wait(&q_full[qi], S::QBUFS == 2 ? (k >> 1) & 1 : k & 1, abort_flag, p.err);
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) return false;
             tc::fence_after_sync();
-            const uint32_t qb = smem_addr(qbuf);
+            const uint32_t qb = smem_addr(qbuf + qi * S::QBUF);
             for (int t = 0; t < it.n_tiles; ++t) {
                 const int s = use % NS;
                 if (lane == 0) good = tc_wait(&full[s], (use / NS) & 1, abort_flag, p.err);
@@ -690,7 +702,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 ++use;
             }
             if (lane == 0) {
-                tc::commit(&q_empty[0]);
+                tc::commit(&q_empty[qi]);
                 tc::commit(&s_full[b]);
             }
             __syncwarp();
