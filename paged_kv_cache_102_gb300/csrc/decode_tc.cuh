@@ -610,10 +610,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         };
 
         auto issue_k = [&](const TcItem& it, int phys, int k) {
-            if (parity == 0 && !issue_q(it, k)) return false;
+            // 16-bit: Q first (one TMA issue); E4M3: the K copies first, so that
+            // their latency covers the Q conversion
+            if (!FP8 && parity == 0 && !issue_q(it, k)) return false;
             for (int t = 0; t < it.n_tiles; ++t)
                 if (!issue_tile(use, parity, it, phys, t, &kmap)) return false;
-            return true;
+            return !FP8 || parity != 0 || issue_q(it, k);
         };
         TcItem cur, nxt;
         int phys_c = -1, phys_n = -1;
