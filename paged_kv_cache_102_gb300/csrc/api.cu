@@ -450,7 +450,7 @@ int quest_select(const void* q, const void* kmeta, const int32_t* block_tables, 
     if (!err) return fail(PKV_ERR_CUDA, "quest_select: cannot resolve the device error word");
     QuestSelectParams p{q, kmeta, block_tables, context_lens, sel_tables, sel_lens, static_cast<float*>(workspace),
                         err, num_seqs, num_q_heads, num_kv_heads, block_size, head_dim, num_blocks,
-                        max_blocks_per_seq, budget_blocks};
+                        max_blocks_per_seq, budget_blocks, /*group_heads: chosen at launch*/ 0};
     cudaError_t e = launch_quest_select(p, act_dtype, G, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail("quest_select: launch", e);
 }
