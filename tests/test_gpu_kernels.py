@@ -504,3 +504,23 @@ def test_decode_plan_matches_the_calls(kernel_path, fused):
             want = pkv.paged_attention_decode(q, kc2, vc2, tab, ln, 0.088)
         torch.cuda.synchronize()
         assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("cache", ["bf16", "e4m3"])
+def test_decode_tensor_core_many_rows(kernel_path, cache):
+    """720 sequences: the per-row tables leave room for only two 32 KB stages
+    (16-bit cache, more than 292 rows) or four 16 KB stages (E4M3, more than
+    698 rows) at two CTAs per SM, so the smaller rings run."""
+    pkv = kernel_path
+    g = _gen(95)
+    B = 720
+    lens = torch.randint(1, 201, (B,), generator=g).numpy()
+    q, kc, vc, tables, lens = _random_paged(g, B, 32, 4, 128, 16, lens, "bf16", cache)
+    scale = 1.0 / math.sqrt(128)
+    ks, vs = (0.021, 0.013) if cache == "e4m3" else (None, None)
+    code = oracle.E4M3 if cache == "e4m3" else oracle.BF16
+    want = oracle.paged_decode(bits(q), oracle.BF16, bits(kc), bits(vc), code, tables, lens, scale,
+                               **({"k_scale": ks, "v_scale": vs} if ks else {}))
+    pkv.set_kernel_path(pkv.PATH_TENSOR_2CTA)
+    got = _run_decode(pkv, q, kc, vc, tables, lens, scale, 128, ks, vs)
+    assert_attention_close(got, want, TOL[cache], rounding_slack=True)

@@ -161,3 +161,51 @@ def test_quest_select_many_items_per_cta(pkv, group):
         sel, slen = pkv.quest_select(q.to(dev), kmeta, t_d, l_d, bs, budget)
         torch.cuda.synchronize()
         _check_selection(sel.cpu().numpy(), slen.cpu().numpy(), q, bits(kc), "bf16", tables, lens, bs, budget)
+
+
+@pytest.mark.parametrize("path", [1, 3])
+def test_sparse_decode_e4m3_cache(pkv, path):
+    """Per-(sequence, kv head) block lists over an E4M3 cache (chosen here, in
+    random order, with the partly filled last block at the end of some
+    lists), on the CUDA-core and tensor-core kernels."""
+    g = torch.Generator().manual_seed(96)
+    rng = np.random.default_rng(96)
+    B, Hq, Hkv, D, bs = 5, 32, 4, 128, 16
+    lens = [37, 400, 1000, 1537, 2048]
+    nblk = [-(-L // bs) for L in lens]
+    NB = sum(nblk) + 4
+    perm = torch.randperm(NB, generator=g).numpy()
+    owned, o = [], 0
+    for n in nblk:
+        owned.append(perm[o:o + n])
+        o += n
+    maxsel = max(nblk)
+    sel = np.zeros((B, Hkv, maxsel), np.int32)
+    slen = np.zeros((B, Hkv), np.int32)
+    for b, L in enumerate(lens):
+        full, tail = L // bs, L % bs
+        for h in range(Hkv):
+            k = int(rng.integers(1, full + 1)) if full else 0
+            picks = list(rng.permutation(owned[b][:full])[:k])
+            n_tok = k * bs
+            if tail and (rng.random() < 0.5 or k == 0):
+                picks.append(owned[b][full])  # the partly filled block, last
+                n_tok += tail
+            sel[b, h, :len(picks)] = picks
+            slen[b, h] = n_tok
+    kc = torch.randint(0, 256, (NB, Hkv, bs, D), dtype=torch.uint8, generator=g)
+    vc = torch.randint(0, 256, (NB, Hkv, bs, D), dtype=torch.uint8, generator=g)
+    kc[(kc & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    vc[(vc & 0x7F) == 0x7F] = 0x3C
+    q = torch.randn(B, Hq, D, generator=g).bfloat16()
+    ks, vs, scale = 0.021, 0.013, 0.088
+    dev = torch.device("cuda")
+    pkv.set_kernel_path(path)
+    out = pkv.paged_attention_decode_sparse(q.to(dev), kc.to(dev), vc.to(dev), torch.from_numpy(sel).to(dev),
+                                            torch.from_numpy(slen).to(dev), scale,
+                                            k_scale=torch.tensor([ks], device=dev),
+                                            v_scale=torch.tensor([vs], device=dev))
+    torch.cuda.synchronize()
+    want = oracle.sparse_decode(bits(q), oracle.BF16, kc.numpy(), vc.numpy(), oracle.E4M3, sel, slen, scale,
+                                k_scale=ks, v_scale=vs)
+    assert_attention_close(out, want, TOL["e4m3"], rounding_slack=True)
