@@ -19,13 +19,20 @@ dicts, one operation at a time, written from the pages:
 
 * PagedAttention notes, section on automatic prefix caching: a KV block is
   looked up by all tokens up to and including it; equal keys are equal
-  blocks.  Here the key is the exact token prefix itself (a tuple), not a
-  hash of it.
+  blocks, and the stated use is a later round of a dialogue reusing the
+  KV of the earlier rounds (prompt and answer).  Here the key is the exact
+  token prefix itself (a tuple), not a hash of it.  A block is registered
+  when it becomes full: a prompt's full blocks when the prompt is added, and
+  a block filled by decoding when its last token is appended with its id.
 
 Readings where the pages are silent: freed blocks go to the back of the free
 list; writers are processed one at a time in call order, and a writer copies
 only while the block's count is above 1, so the last holder writes in place.
-Prefix cache: only full prompt blocks are registered; a registered block whose
+Prefix cache: a sequence added from its token ids keeps its token list;
+appending a token with its id extends the list, and a block that becomes full
+is registered under its prefix unless that prefix already names a block (the
+first registration stays).  Appending without an id ends the tracking of that
+sequence (its later blocks are not registered).  A registered block whose
 count reaches 0 keeps its contents on a least-recently-freed list and is taken
 (and forgotten) only when the free list is empty.
 """
@@ -47,6 +54,7 @@ class RefBlockManager:
         self.prefix_of_block: dict[int, tuple] = {}  # registered block -> its token prefix
         self.block_of_prefix: dict[tuple, int] = {}
         self.lru: list[int] = []  # registered blocks with count 0, least recently freed first
+        self.tokens: dict[int, list[int]] = {}  # token ids of sequences added from their prompt ids
 
     def available(self) -> int:
         return len(self.free) + len(self.lru)
@@ -73,7 +81,32 @@ class RefBlockManager:
         return list(self.tables[seq])
 
     def append_slot(self, seq: int):
-        """Reserve the slot of the next token; return (slot, cow_pair or None)."""
+        """Reserve the slot of the next token; return (slot, cow_pair or None).
+        The token's id is not known, so the sequence's blocks are no longer
+        registered from here on."""
+        self.tokens.pop(seq, None)
+        return self._reserve(seq)
+
+    def append_token(self, seq: int, token: int):
+        """Reserve the slot of the next token, whose id is `token`; return
+        (slot, cow_pair or None).  If the token fills its block and the
+        sequence's token ids are known, the block is registered under the
+        sequence's whole token prefix (unless that prefix already names a
+        block)."""
+        pos = self.lens[seq]
+        slot, cow = self._reserve(seq)
+        toks = self.tokens.get(seq)
+        if toks is not None:
+            toks.append(int(token))
+            if (pos + 1) % self.block_size == 0:
+                key = tuple(toks[: pos + 1])
+                if key not in self.block_of_prefix:
+                    b = self.tables[seq][pos // self.block_size]
+                    self.block_of_prefix[key] = b
+                    self.prefix_of_block[b] = key
+        return slot, cow
+
+    def _reserve(self, seq: int):
         table = self.tables[seq]
         pos = self.lens[seq]
         bs = self.block_size
@@ -122,6 +155,7 @@ class RefBlockManager:
             table.append(b)
         self.tables[seq] = table
         self.lens[seq] = len(tokens)
+        self.tokens[seq] = tokens
         return len(shared) * bs
 
     def fork(self, parent: int, child: int) -> None:
@@ -129,11 +163,14 @@ class RefBlockManager:
         assert child not in self.tables
         self.tables[child] = list(self.tables[parent])
         self.lens[child] = self.lens[parent]
+        if parent in self.tokens:
+            self.tokens[child] = list(self.tokens[parent])
         for b in self.tables[child]:
             self.ref[b] += 1
 
     def free_sequence(self, seq: int) -> None:
         """Release a finished request: counts - 1, blocks at 0 go back to the pool."""
+        self.tokens.pop(seq, None)
         if seq in getattr(self, "swapped", {}):
             del self.swapped[seq]
             return

@@ -207,3 +207,47 @@ def test_reference_swap_hand_example():
     assert ref2.free == [2, 3] and ref2.ref[:2] == [1, 1]
     ref2.swap_out("p")
     assert ref2.free == [2, 3, 0, 1]
+
+
+def test_reference_prefix_cache_multi_turn_hand_example():
+    """Automatic prefix caching across the rounds of a dialogue, worked by hand
+    (the PagedAttention notes page, section on automatic prefix caching: a
+    block is found by its own and all earlier tokens, so the next round reuses
+    the KV of the previous round's prompt AND answer).  Block size 4, free
+    list [5, 2, 7, 0, 1, 3, 4, 6]:
+
+    round 1  prompt 11..16 (6 tokens): block 5 = 11..14 (full, registered),
+             block 2 = 15, 16 (partial).  Decoding 17 and 18 fills block 2,
+             which is registered under 11..18; 19 starts block 7 (slot 28).
+             Freeing the request parks the registered blocks 5 and 2 on the
+             LRU list; block 7 goes to the back of the free list.
+    round 2  prompt 11..19, 30, 31, 32 (12 tokens): 11..14 and 11..18 hit
+             (blocks 5 and 2), 11..32 misses and takes block 0 -> 8 tokens
+             already in the pool.
+    """
+    from oracle.block_manager_ref import RefBlockManager
+    ref = RefBlockManager(8, 4, free_list=[5, 2, 7, 0, 1, 3, 4, 6])
+    assert ref.add_sequence_cached("r1", [11, 12, 13, 14, 15, 16]) == 0
+    assert ref.tables["r1"] == [5, 2] and ref.block_of_prefix == {(11, 12, 13, 14): 5}
+    assert ref.append_token("r1", 17) == (2 * 4 + 2, None)
+    assert ref.append_token("r1", 18) == (2 * 4 + 3, None)
+    assert ref.block_of_prefix[(11, 12, 13, 14, 15, 16, 17, 18)] == 2
+    assert ref.append_token("r1", 19) == (7 * 4 + 0, None)
+    ref.free_sequence("r1")
+    assert ref.lru == [5, 2] and ref.free == [0, 1, 3, 4, 6, 7]
+    assert ref.add_sequence_cached("r2", [11, 12, 13, 14, 15, 16, 17, 18, 19, 30, 31, 32]) == 8
+    assert ref.tables["r2"] == [5, 2, 0] and ref.lru == [] and ref.free == [1, 3, 4, 6, 7]
+    assert ref.ref[5] == ref.ref[2] == ref.ref[0] == 1
+    # a sequence appended to without token ids stops registering blocks
+    ref.add_sequence_cached("r3", [40, 41, 42])
+    ref.append_slot("r3")
+    ref.append_token("r3", 44)
+    assert all(40 not in key for key in ref.block_of_prefix)
+    # the first registration of a prefix stays: a second request that decodes
+    # the same tokens into its own block does not replace it
+    ref.add_sequence_cached("r4", [50, 51])
+    ref.add_sequence_cached("r5", [50, 51])
+    for t in (52, 53):
+        ref.append_token("r4", t)
+        ref.append_token("r5", t)
+    assert ref.block_of_prefix[(50, 51, 52, 53)] == ref.tables["r4"][0] != ref.tables["r5"][0]
