@@ -106,7 +106,13 @@ class ClockSampler:
             self.proc.wait(timeout=2)
         except Exception:
             self.proc.kill()
-        rows = [r for t, r in self.rows if t0 - 0.25 <= t <= t1 + 0.25] or [r for _, r in self.rows]
+        return self.summary(t0, t1)
+
+    def summary(self, t0, t1):
+        """Median SM clock, max clock and active throttle reasons of the samples in [t0, t1]."""
+        if not self.proc:
+            return None
+        rows = [r for t, r in list(self.rows) if t0 - 0.25 <= t <= t1 + 0.25] or [r for _, r in list(self.rows)]
         if not rows:
             return None
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -382,6 +388,7 @@ def run_native(args):
     if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.ncu):
         cpu = cpu_baseline(st, budget_s=args.cpu_budget)
 
+
     if rank != 0:
         return
     line = {
@@ -416,7 +423,81 @@ def run_native(args):
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
+    # the other target configurations, device-timed on the same box in the same run
+    if world == 1 and not (args.ncu or args.no_workloads) and args.workload == "llama7b" and not args.batch:
+        del plan
+        st.clear()
+        vals = None
+        torch.cuda.empty_cache()
+        line["workloads"] = {}
+        for name in OTHER_WORKLOADS:
+            line["workloads"][name] = time_workload(pkv, W, name, dev, args, peak)
+            torch.cuda.empty_cache()
     print(json.dumps(line), flush=True)
+
+
+# the grouped-query, E4M3 and long-context configurations reported beside the headline line
+OTHER_WORKLOADS = ("gqa_bs16", "gqa_bs32", "long_gqa", "fp8_13b", "gqa_fp8")
+
+
+def time_workload(pkv, W, name, dev, args, peak):
+    """One workload's fused decode step (append + decode through DecodePlan,
+    library-chosen kernel and partition size), warmed up, then `steps` steps
+    each bracketed by CUDA events on the launching stream; the clock sampler
+    runs over the soak and the timed region."""
+    st = setup(pkv, W, name, args.seed, dev)
+    wl, vals = st["wl"], st["vals"]
+    B = len(st["ids"])
+    need = pkv.workspace_size(B, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, st["tables_h"].shape[1],
+                              wl.block_size, -1)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    plan = pkv.DecodePlan(vals["q"], vals["k_cache"], vals["v_cache"], st["tables"], st["lens"], wl.scale,
+                          out=st["out"], k_scale=vals.get("k_scale"), v_scale=vals.get("v_scale"), partition_size=-1,
+                          workspace=ws, stream=stream, k_new=vals["k_new"], v_new=vals["v_new"],
+                          slot_mapping=st["slots"])
+    dec_bytes, app_bytes = algorithmic_bytes(wl, st["lens_h"])
+    sampler = ClockSampler(dev.index if not os.environ.get("CUDA_VISIBLE_DEVICES") else
+                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
+    for _ in range(args.warmup):
+        plan.run()
+    torch.cuda.synchronize(dev)
+    t_soak = time.time()
+    while time.time() - t_soak < 0.6:
+        for _ in range(20):
+            plan.run()
+        torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        plan.run()
+        ends[i].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    clocks = sampler.stop(t_soak, t1)
+    if pkv.device_error(reset=True, device=dev):
+        raise RuntimeError(f"a kernel flagged a device-side error in workload {name}")
+    call_us = statistics.mean(starts[i].elapsed_time(ends[i]) for i in range(args.steps)) * 1e3
+    step_ms = e0.elapsed_time(e1) / args.steps
+    call_gbs = (dec_bytes + app_bytes) / (call_us * 1e-6) / 1e9
+    step_gbs = (dec_bytes + app_bytes) / (step_ms * 1e-3) / 1e9
+    P = pkv.resolve_partition_size(B, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, st["tables_h"].shape[1],
+                                   wl.block_size, -1)
+    # the library's automatic choice: tensor cores for >= 4 query heads per kv head at head_dim 128
+    # with partitions of at most 512 tokens and at most 2048 sequences
+    grouped = wl.num_q_heads // wl.num_kv_heads >= 4 and wl.head_dim == 128 and B <= 2048 and P <= 512
+    path = "tensor-core" if grouped else "CUDA-core"
+    res = {"description": wl.description, "kernel": path, "partition_size": P,
+           "decode_call_gbs": round(call_gbs, 1), "frac": round(call_gbs / peak, 4),
+           "avg_call_us": round(call_us, 2), "step_gbs": round(step_gbs, 1), "step_frac": round(step_gbs / peak, 4),
+           "algorithmic_bytes_per_step": dec_bytes + app_bytes,
+           "seq_steps_per_s": round(B / (step_ms * 1e-3), 1), "clocks": clocks}
+    del plan, ws, st
+    return res
 
 
 def cpu_baseline(st, budget_s=20.0, max_seqs=None):
@@ -660,6 +741,8 @@ def main():
                     help="decode kernel: 0 library choice, 1 CUDA-core, 2/3 tensor-core (1 or 2 CTAs per SM)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other target configurations reported in the line's `workloads` object")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ncu", action="store_true",
                     help="profiling run: only warmup + timed steps (no clock soak, e2e or CPU baseline)")

@@ -234,6 +234,16 @@ int paged_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs,
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it.  Make
  *    that first call before any stream capture.
+ *  - With lazy module loading (the CUDA runtime's default since 12.2, unless
+ *    CUDA_MODULE_LOADING=EAGER), the array's 16 MiB are committed on a device
+ *    when the library's device code holding it is first loaded there, which
+ *    may be that first call.  An engine that reserves all free device memory
+ *    for its pool should make its first call (any valid decode) before that
+ *    reservation; later calls take no device memory.
+ *  - The cached address belongs to the device's primary context, which the
+ *    CUDA runtime uses.  After cudaDeviceReset, or under another context made
+ *    current through the driver API, it is stale: do not call this entry
+ *    point there.
  *  - Every call on a device shares the one array, and it keeps the previous
  *    call's contents.  Each call zeroes the work counter it needs (an
  *    asynchronous 4-byte memset on the stream) and writes all the partials

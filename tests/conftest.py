@@ -44,3 +44,30 @@ def pkv_lib():
     import paged_kv_cache_102_gb300 as pkv
     pkv.load()
     return pkv
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Print every attention parity comparison's largest error as a fraction
+    of the plain tolerance (over the elements held to it) and of each
+    element's bound, and write them as JSON when PKV_PARITY_REPORT names a
+    file."""
+    try:
+        from tests.parity import RESULTS
+    except Exception:
+        return
+    if not RESULTS:
+        return
+    worst = max(RESULTS, key=lambda r: r[3])
+    tr = terminalreporter
+    tr.write_sep("-", f"attention parity: {len(RESULTS)} comparisons; largest max|err|/tol over elements held "
+                      f"to the plain tol = {worst[3]:.3f} ({worst[0]}); largest max|err|/bound = "
+                      f"{max(r[4] for r in RESULTS):.3f}")
+    for name, err, tol, frac_plain, frac_bound, n, n_extra in sorted(RESULTS, key=lambda r: -r[3])[:12]:
+        tr.write_line(f"  plain {frac_plain:6.3f}  bound {frac_bound:6.3f}  max|err| {err:.3e}  tol {tol:.0e}  "
+                      f"elements {n:>8}  half-ulp allowed {n_extra:>5}  {name}")
+    path = os.environ.get("PKV_PARITY_REPORT")
+    if path:
+        with open(path, "w") as f:
+            json.dump([dict(test=r[0], max_err=r[1], tol=r[2], max_err_over_tol_plain_elements=r[3],
+                            max_err_over_bound=r[4], elements=r[5], half_ulp_elements=r[6]) for r in RESULTS],
+                      f, indent=1)

@@ -88,4 +88,4 @@ def test_fused_equals_append_then_decode(pkv, case):
     want = oracle.paged_decode(bits(q), ACT_CODE[DT[act]], bits(kb), bits(vb), code, tables, lens, 0.1,
                                k_scale=float(ks) if ks is not None else 1.0,
                                v_scale=float(vs) if vs is not None else 1.0)
-    assert_attention_close(out_b, want, TOL["e4m3" if cache == "e4m3" else act], rounding_slack=True)
+    assert_attention_close(out_b, want, TOL["e4m3" if cache == "e4m3" else act])

@@ -195,7 +195,7 @@ def test_decode_parity_sweep(pkv, case, partition_size):
                                k_scale=ks, v_scale=vs)
     got = _run_decode(pkv, q, kc, vc, tables, lens, scale, partition_size,
                       *((ks, vs) if cache == "e4m3" else (None, None)))
-    assert_attention_close(got, want, TOL[cache if cache == "e4m3" else act], rounding_slack=True)
+    assert_attention_close(got, want, TOL[cache if cache == "e4m3" else act])
 
 
 def test_decode_closed_forms(pkv):
@@ -257,7 +257,7 @@ def test_decode_empty_batch_and_streams(pkv):
                                          torch.from_numpy(lens).cuda(), 0.125, stream=s)
     s.synchronize()
     want = oracle.paged_decode(bits(q), oracle.F16, bits(kc), bits(vc), oracle.F16, tables, lens, 0.125)
-    assert_attention_close(out, want, TOL["f16"], rounding_slack=True)
+    assert_attention_close(out, want, TOL["f16"])
 
 
 # ------------------------------------------------------ tensor-core GQA path ---
@@ -295,7 +295,7 @@ def test_decode_tensor_core_parity(kernel_path, case, path, partition_size):
     want = oracle.paged_decode(bits(q), ACT_CODE[DT[act]], bits(kc), bits(vc), ACT_CODE[DT[act]], tables, lens, scale)
     pkv.set_kernel_path(path)
     got = _run_decode(pkv, q, kc, vc, tables, lens, scale, partition_size)
-    assert_attention_close(got, want, TOL[act], rounding_slack=True)
+    assert_attention_close(got, want, TOL[act])
 
 
 TC_FP8_CASES = [
@@ -326,7 +326,7 @@ def test_decode_tensor_core_e4m3_parity(kernel_path, case, path, partition_size)
                                k_scale=ks, v_scale=vs)
     pkv.set_kernel_path(path)
     got = _run_decode(pkv, q, kc, vc, tables, lens, scale, partition_size, ks, vs)
-    assert_attention_close(got, want, TOL["e4m3"], rounding_slack=True)
+    assert_attention_close(got, want, TOL["e4m3"])
 
 
 def test_decode_tensor_core_e4m3_large_queries(kernel_path):
@@ -345,7 +345,7 @@ def test_decode_tensor_core_e4m3_large_queries(kernel_path):
     for path in (2, 3):
         pkv.set_kernel_path(path)
         got = _run_decode(pkv, q, kc, vc, tables, lens, scale, -1, ks, vs)
-        assert_attention_close(got, want, TOL["e4m3"], rounding_slack=True)
+        assert_attention_close(got, want, TOL["e4m3"])
 
 
 @pytest.mark.parametrize("act", ["bf16", "f16"])
@@ -362,7 +362,7 @@ def test_decode_tensor_core_e4m3_peaked_softmax(kernel_path, act):
     for path in (2, 3):
         pkv.set_kernel_path(path)
         got = _run_decode(pkv, q, kc, vc, tables, lens, scale, -1, ks, vs)
-        assert_attention_close(got, want, TOL["e4m3"], rounding_slack=True)
+        assert_attention_close(got, want, TOL["e4m3"])
 
 
 @pytest.mark.parametrize("path", [1, 3])
@@ -380,7 +380,7 @@ def test_decode_split_k_merge_many_rows(kernel_path, path):
     want = oracle.paged_decode(bits(q), oracle.BF16, bits(kc), bits(vc), oracle.BF16, tables, lens, scale)
     pkv.set_kernel_path(path)
     got = _run_decode(pkv, q, kc, vc, tables, lens, scale, 64)
-    assert_attention_close(got, want, TOL["bf16"], rounding_slack=True)
+    assert_attention_close(got, want, TOL["bf16"])
 
 
 @pytest.mark.parametrize("path", [1, 2, 3])
@@ -397,7 +397,7 @@ def test_decode_ignores_unwritten_slots(kernel_path, path):
         vc[last, :, L % 16 or 16:] = float("nan")
     pkv.set_kernel_path(path)
     got = _run_decode(pkv, q, kc, vc, tables, lens, 0.09, -1)
-    assert_attention_close(got, want, TOL["bf16"], rounding_slack=True)
+    assert_attention_close(got, want, TOL["bf16"])
 
 
 @pytest.mark.parametrize("path", [1, 2, 3])
@@ -415,7 +415,7 @@ def test_decode_e4m3_ignores_unwritten_slots(kernel_path, path):
         vc[last, :, L % 16 or 16:] = 0xFF
     pkv.set_kernel_path(path)
     got = _run_decode(pkv, q, kc, vc, tables, lens, 0.09, -1, 0.02, 0.01)
-    assert_attention_close(got, want, TOL["e4m3"], rounding_slack=True)
+    assert_attention_close(got, want, TOL["e4m3"])
 
 
 def test_tensor_path_refuses_unsupported_shapes(kernel_path):
@@ -523,4 +523,4 @@ def test_decode_tensor_core_many_rows(kernel_path, cache):
                                **({"k_scale": ks, "v_scale": vs} if ks else {}))
     pkv.set_kernel_path(pkv.PATH_TENSOR_2CTA)
     got = _run_decode(pkv, q, kc, vc, tables, lens, scale, 128, ks, vs)
-    assert_attention_close(got, want, TOL[cache], rounding_slack=True)
+    assert_attention_close(got, want, TOL[cache])

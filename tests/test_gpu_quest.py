@@ -113,7 +113,7 @@ def test_quest_metadata_selection_and_sparse_decode(pkv, case):
         torch.cuda.synchronize()
         want = oracle.sparse_decode(bits(q), ACT_CODE[DT[act]], kbits, bits(dv), ACT_CODE[DT[act]], sel_h, slen_h,
                                     0.09)
-        assert_attention_close(out, want, TOL[act], rounding_slack=True)
+        assert_attention_close(out, want, TOL[act])
 
 
 def test_full_budget_reproduces_full_decode(pkv):
@@ -143,7 +143,7 @@ def test_sparse_decode_paths_agree_with_oracle(pkv, path):
     torch.cuda.synchronize()
     want = oracle.sparse_decode(bits(q), oracle.BF16, bits(dk), bits(dv), oracle.BF16, sel.cpu().numpy(),
                                 slen.cpu().numpy(), 0.088)
-    assert_attention_close(out, want, TOL["bf16"], rounding_slack=True)
+    assert_attention_close(out, want, TOL["bf16"])
 
 
 @pytest.mark.parametrize("group", [4, 8])
@@ -208,4 +208,4 @@ def test_sparse_decode_e4m3_cache(pkv, path):
     torch.cuda.synchronize()
     want = oracle.sparse_decode(bits(q), oracle.BF16, kc.numpy(), vc.numpy(), oracle.E4M3, sel, slen, scale,
                                 k_scale=ks, v_scale=vs)
-    assert_attention_close(out, want, TOL["e4m3"], rounding_slack=True)
+    assert_attention_close(out, want, TOL["e4m3"])
