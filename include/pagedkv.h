@@ -443,7 +443,8 @@ int pkv_bm_get_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n
 
 /* Prefix caching (the PagedAttention notes page, on automatic prefix
  * caching: a block is looked up by a hash of its own tokens and all tokens
- * before it; Ultralytics glossary, section "Sharing blocks between
+ * before it, so a later round of a dialogue reuses the KV of the earlier
+ * rounds; Ultralytics glossary, section "Sharing blocks between
  * sequences": hashing full blocks extends sharing across requests).
  * Register a new sequence from its prompt token ids: every full block is
  * keyed by a chained 64-bit FNV-1a hash of (previous block's key, this
@@ -452,13 +453,27 @@ int pkv_bm_get_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n
  * leading tokens whose K/V are already in the pool (a multiple of
  * block_size); the remaining blocks are taken from the pool and its full
  * blocks registered.  The caller writes K/V for tokens from
- * *num_cached_tokens on.  A registered block whose count drops to 0 keeps
- * its contents on a least-recently-freed list and is reused for new
- * allocations (and unregistered) only when the free list is empty.  Only
- * prompt blocks are registered; a 64-bit key match is trusted.
- * PKV_ERR_NO_SPACE leaves no trace. */
+ * *num_cached_tokens on.  A key that already names a block keeps it (the
+ * first registration stays); a key match counts only if the block's stored
+ * token ids and parent key match too.  A registered block whose count drops
+ * to 0 keeps its contents on a least-recently-freed list and is reused for
+ * new allocations (and unregistered) only when the free list is empty.
+ * The sequence keeps its token ids: pkv_bm_append_tokens registers each
+ * block that decoding fills; pkv_bm_append_slots (no ids) stops that for
+ * the sequence.  Forks inherit the token ids.  PKV_ERR_NO_SPACE leaves no
+ * trace. */
 int pkv_bm_add_sequence_cached(pkv_block_manager* bm, int64_t seq_id, const int32_t* tokens,
                                int num_tokens, int* num_cached_tokens);
+
+/* pkv_bm_append_slots with the id of each appended token (host int32 [n]):
+ * for a sequence added by pkv_bm_add_sequence_cached, a token that fills its
+ * block registers that block in the prefix cache under the chained key of
+ * the sequence's whole token prefix, exactly as a prompt's full blocks are.
+ * Sequences without token ids (pkv_bm_add_sequence) ignore the ids.  Slots,
+ * copy-on-write pairs, errors and the all-or-nothing rule are those of
+ * pkv_bm_append_slots. */
+int pkv_bm_append_tokens(pkv_block_manager* bm, const int64_t* seq_ids, const int32_t* token_ids, int n,
+                         int64_t* slots_out, int32_t* cow_pairs_out, int* num_cow_pairs);
 /* Preemption by swapping (the PagedAttention notes page, section on
  * preemption).  pkv_bm_swap_out writes the sequence's block table (logical
  * order, host int32, capacity cap) to blocks_out and *n, then releases the

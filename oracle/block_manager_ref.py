@@ -148,8 +148,8 @@ class RefBlockManager:
         table = list(shared)
         for i in range(len(shared), n_blocks):
             b = self._take()
-            if i < n_full:
-                key = tuple(tokens[: (i + 1) * bs])
+            key = tuple(tokens[: (i + 1) * bs])
+            if i < n_full and key not in self.block_of_prefix:  # the first registration stays
                 self.block_of_prefix[key] = b
                 self.prefix_of_block[b] = key
             table.append(b)

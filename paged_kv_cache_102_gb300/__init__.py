@@ -442,6 +442,23 @@ class BlockManager:
             pairs.ctypes.data_as(ctypes.c_void_p), ctypes.byref(npairs)))
         return slots, pairs[: npairs.value].copy()
 
+    def append_tokens(self, seq_ids, token_ids):
+        """append_slots with each new token's id: a token that fills its block
+        registers the block in the prefix cache (sequences added by
+        add_sequence_cached).  Returns (slots int64 [n], cow_pairs int32 [k, 2])."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        toks = np.ascontiguousarray(token_ids, dtype=np.int32)
+        n = len(ids)
+        if len(toks) != n:
+            raise ValueError("append_tokens: one token id per sequence id")
+        slots = np.empty(n, np.int64)
+        pairs = np.empty((max(n, 1), 2), np.int32)
+        npairs = ctypes.c_int(0)
+        self._check("pkv_bm_append_tokens", _native.lib().pkv_bm_append_tokens(
+            self._h, ids.ctypes.data_as(ctypes.c_void_p), toks.ctypes.data_as(ctypes.c_void_p), n,
+            slots.ctypes.data_as(ctypes.c_void_p), pairs.ctypes.data_as(ctypes.c_void_p), ctypes.byref(npairs)))
+        return slots, pairs[: npairs.value].copy()
+
     def fork(self, parent_id: int, child_id: int) -> None:
         self._check("pkv_bm_fork", _native.lib().pkv_bm_fork(self._h, int(parent_id), int(child_id)))
 

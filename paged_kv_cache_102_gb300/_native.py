@@ -49,6 +49,7 @@ SIGNATURES = {
     "pkv_bm_destroy": (None, [P]),
     "pkv_bm_add_sequence": (I32, [P, I64, I32]),
     "pkv_bm_append_slots": (I32, [P, P, I32, P, P, P]),
+    "pkv_bm_append_tokens": (I32, [P, P, P, I32, P, P, P]),
     "pkv_bm_fork": (I32, [P, I64, I64]),
     "pkv_bm_free_sequence": (I32, [P, I64]),
     "pkv_bm_get_tables": (I32, [P, P, I32, P, I32, I32, P]),

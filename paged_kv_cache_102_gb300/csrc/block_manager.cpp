@@ -20,9 +20,16 @@
 // sharing across requests).  pkv_bm_add_sequence_cached keys every full
 // block of a prompt by a chained 64-bit FNV-1a hash over (previous block's
 // hash, this block's token ids), reuses the blocks already registered for
-// the longest matching prefix, and registers the new full blocks.  A freed
-// block that is registered keeps its contents and waits on an LRU list; it
-// is taken (and unregistered) only when the free list is empty.
+// the longest matching prefix, and registers the new full blocks.  Such a
+// sequence keeps the chain hash and the token ids of its partial last block;
+// pkv_bm_append_tokens appends with token ids, and a block that becomes full
+// is registered the same way, so a later round of a dialogue finds the
+// blocks of the earlier rounds' answers as well as their prompts.  A key
+// that already names a block keeps it (the first registration stays).  A
+// match is confirmed by the block's own token ids and its parent's hash,
+// stored at registration.  A freed block that is registered keeps its
+// contents and waits on an LRU list; it is taken (and unregistered) only
+// when the free list is empty.
 #include <cstdint>
 #include <cstring>
 #include <deque>
@@ -41,6 +48,11 @@ struct Sequence {
     std::vector<int32_t> blocks;
     int64_t len = 0;
     bool swapped = false;  // contents staged outside the pool; no blocks held
+    // prefix caching: set for sequences added from their token ids, cleared by
+    // an append without token ids
+    bool tracked = false;
+    uint64_t chain = 0;         // hash of the last full block (0: none yet)
+    std::vector<int32_t> tail;  // token ids of the partly filled last block
 };
 
 }  // namespace
@@ -83,6 +95,8 @@ struct pkv_block_manager {
     // prefix cache
     std::unordered_map<uint64_t, int32_t> cached;  // hash -> block
     std::vector<uint64_t> hash_of;                 // per block, valid when registered[b]
+    std::vector<uint64_t> parent_of;               // hash of the previous block (0: first block)
+    std::vector<int32_t> tokens_of;                // [num_blocks][block_size] token ids of registered blocks
     std::vector<char> registered;
     std::list<int32_t> evictable;  // registered blocks with count 0, least recently freed first
     std::vector<std::list<int32_t>::iterator> evict_pos;
@@ -118,6 +132,26 @@ struct pkv_block_manager {
             }
         }
     }
+    // Register full block b under `hash` unless the key already names a block.
+    void register_block(int32_t b, uint64_t hash, uint64_t parent, const int32_t* toks) {
+        if (cached.count(hash)) return;
+        if (tokens_of.empty()) tokens_of.assign(static_cast<size_t>(num_blocks) * block_size, 0);
+        hash_of[b] = hash;
+        parent_of[b] = parent;
+        std::memcpy(&tokens_of[static_cast<size_t>(b) * block_size], toks, sizeof(int32_t) * block_size);
+        registered[b] = 1;
+        cached[hash] = b;
+    }
+    // The registered block for (hash, parent, toks), or -1.
+    int32_t lookup(uint64_t hash, uint64_t parent, const int32_t* toks) const {
+        auto it = cached.find(hash);
+        if (it == cached.end()) return -1;
+        const int32_t b = it->second;
+        if (parent_of[b] != parent ||
+            std::memcmp(&tokens_of[static_cast<size_t>(b) * block_size], toks, sizeof(int32_t) * block_size) != 0)
+            return -1;
+        return b;
+    }
     // A registered block is referenced again.
     void revive(int32_t b) {
         if (ref[b] == 0) evictable.erase(evict_pos[b]);
@@ -138,6 +172,7 @@ pkv_block_manager* pkv_bm_create(int num_blocks, int block_size, const int32_t* 
     bm->block_size = block_size;
     bm->ref.assign(num_blocks, 0);
     bm->hash_of.assign(num_blocks, 0);
+    bm->parent_of.assign(num_blocks, 0);
     bm->registered.assign(num_blocks, 0);
     bm->evict_pos.resize(num_blocks);
     if (free_list == nullptr) {
@@ -173,10 +208,15 @@ int pkv_bm_add_sequence(pkv_block_manager* bm, int64_t seq_id, int num_tokens) {
     return PKV_OK;
 }
 
-int pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n, int64_t* slots_out,
-                        int32_t* cow_pairs_out, int* num_cow_pairs) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of pkv_bm_append_slots (token_ids == nullptr) and pkv_bm_append_tokens.
+int append_batch(pkv_block_manager* bm, const int64_t* seq_ids, const int32_t* token_ids, int n,
+                 int64_t* slots_out, int32_t* cow_pairs_out, int* num_cow_pairs, const char* F) {
     if (!bm || n < 0 || (n > 0 && (!seq_ids || !slots_out || !cow_pairs_out)) || !num_cow_pairs)
-        return pkv::fail(PKV_ERR_INVALID, "pkv_bm_append_slots: bad arguments");
+        return pkv::fail(PKV_ERR_INVALID, std::string(F) + ": bad arguments");
     const int bs = bm->block_size;
     // Pass 1: check ids and count the blocks the whole batch needs, replaying
     // the reference-count decrements that earlier writers in the batch make.
@@ -186,7 +226,7 @@ int pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n, in
     for (int i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seq_ids[i]);
         if (it == bm->seqs.end() || !seen.insert(seq_ids[i]).second || it->second.swapped)
-            return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_append_slots: unknown, repeated or swapped-out sequence id");
+            return pkv::fail(PKV_ERR_NOT_FOUND, std::string(F) + ": unknown, repeated or swapped-out sequence id");
         const Sequence& s = it->second;
         if (s.len % bs == 0) {
             ++need;
@@ -199,7 +239,7 @@ int pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n, in
         }
     }
     if (need > bm->available())
-        return pkv::fail(PKV_ERR_NO_SPACE, "pkv_bm_append_slots: not enough free blocks for the batch");
+        return pkv::fail(PKV_ERR_NO_SPACE, std::string(F) + ": not enough free blocks for the batch");
     // Pass 2: apply.
     int pairs = 0;
     for (int i = 0; i < n; ++i) {
@@ -221,9 +261,36 @@ int pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n, in
         }
         slots_out[i] = static_cast<int64_t>(s.blocks[lb]) * bs + pos % bs;
         s.len = pos + 1;
+        if (!token_ids) {
+            s.tracked = false;  // this token's id is unknown: stop registering
+            s.tail.clear();
+        } else if (s.tracked) {
+            s.tail.push_back(token_ids[i]);
+            if (s.len % bs == 0) {  // the token filled its block
+                const uint64_t h = block_hash(s.chain, s.tail.data(), bs);
+                bm->register_block(s.blocks[lb], h, s.chain, s.tail.data());
+                s.chain = h;
+                s.tail.clear();
+            }
+        }
     }
     *num_cow_pairs = pairs;
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n, int64_t* slots_out,
+                        int32_t* cow_pairs_out, int* num_cow_pairs) {
+    return append_batch(bm, seq_ids, nullptr, n, slots_out, cow_pairs_out, num_cow_pairs, "pkv_bm_append_slots");
+}
+
+int pkv_bm_append_tokens(pkv_block_manager* bm, const int64_t* seq_ids, const int32_t* token_ids, int n,
+                         int64_t* slots_out, int32_t* cow_pairs_out, int* num_cow_pairs) {
+    if (n > 0 && !token_ids) return pkv::fail(PKV_ERR_INVALID, "pkv_bm_append_tokens: token_ids is null");
+    return append_batch(bm, seq_ids, token_ids, n, slots_out, cow_pairs_out, num_cow_pairs, "pkv_bm_append_tokens");
 }
 
 int pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_id) {
@@ -281,33 +348,33 @@ int pkv_bm_add_sequence_cached(pkv_block_manager* bm, int64_t seq_id, const int3
         h = block_hash(h, tokens + static_cast<size_t>(i) * bs, bs);
         hashes[i] = h;
     }
-    int reused = 0;
+    std::vector<int32_t> hit;
     int revived_from_lru = 0;
-    while (reused < n_full) {
-        auto it = bm->cached.find(hashes[reused]);
-        if (it == bm->cached.end()) break;
-        if (bm->ref[it->second] == 0) ++revived_from_lru;
-        ++reused;
+    while (static_cast<int>(hit.size()) < n_full) {
+        const int i = static_cast<int>(hit.size());
+        const int32_t b = bm->lookup(hashes[i], i ? hashes[i - 1] : 0, tokens + static_cast<size_t>(i) * bs);
+        if (b < 0) break;
+        if (bm->ref[b] == 0) ++revived_from_lru;
+        hit.push_back(b);
     }
+    const int reused = static_cast<int>(hit.size());
     const int fresh = n_blocks - reused;
     if (fresh > bm->available() - revived_from_lru)
         return pkv::fail(PKV_ERR_NO_SPACE, "pkv_bm_add_sequence_cached: not enough free blocks");
     Sequence s;
     s.len = num_tokens;
-    for (int i = 0; i < reused; ++i) {
-        const int32_t b = bm->cached[hashes[i]];
+    for (int32_t b : hit) {
         bm->revive(b);
         s.blocks.push_back(b);
     }
     for (int i = reused; i < n_blocks; ++i) {
         const int32_t b = bm->take();
-        if (i < n_full) {
-            bm->hash_of[b] = hashes[i];
-            bm->registered[b] = 1;
-            bm->cached[hashes[i]] = b;
-        }
+        if (i < n_full) bm->register_block(b, hashes[i], i ? hashes[i - 1] : 0, tokens + static_cast<size_t>(i) * bs);
         s.blocks.push_back(b);
     }
+    s.tracked = true;
+    s.chain = n_full ? hashes[n_full - 1] : 0;
+    s.tail.assign(tokens + static_cast<size_t>(n_full) * bs, tokens + num_tokens);
     bm->seqs.emplace(seq_id, std::move(s));
     *num_cached_tokens = reused * bs;
     return PKV_OK;

@@ -77,3 +77,90 @@ def test_prefix_cached_decode_matches_oracle(pkv_lib, cuda_device):
                                                              V[:, None].expand(Hkv, Hq // Hkv, -1, D), scale=0.125)
         assert np.abs(o.reshape(Hq, D).numpy() - want[sid]).max() < 1e-9
     assert pkv.device_error(reset=True) == 0
+
+
+@pytest.mark.parametrize("act,Hq,Hkv,D", [("f16", 8, 8, 64), ("bf16", 32, 8, 128)])
+def test_second_round_reuses_answer_blocks_decode_matches_oracle(pkv_lib, cuda_device, act, Hq, Hkv, D):
+    """A two-round dialogue on the GPU.  Round 1 writes its prompt's K/V, then
+    decodes its answer token by token (the fused append + decode launch, slots
+    from append_tokens, so the blocks the answer fills are registered).  Round
+    2's prompt is round 1's prompt + answer + a new user turn: every full block
+    of round 1 is reused, only the rest is written, and the decode over the
+    shared blocks matches the float64 oracle on the oracle allocator's tables
+    and caches, and attention over the request's own unshared K/V."""
+    pkv = pkv_lib
+    pkv.device_error(reset=True)
+    dt = torch.float16 if act == "f16" else torch.bfloat16
+    code = oracle.F16 if act == "f16" else oracle.BF16
+    bs, NB, scale = 16, 96, 1.0 / np.sqrt(D)
+    rng = np.random.default_rng(11)
+    prompt = list(rng.integers(0, 30000, size=77))
+    answer = list(rng.integers(0, 30000, size=58))  # prompt + answer = 135 tokens: 8 full blocks
+    user = list(rng.integers(0, 30000, size=21))
+    bm = pkv.BlockManager(NB, bs)
+    ref = RefBlockManager(NB, bs)
+    kc = torch.zeros(NB, Hkv, bs, D, dtype=dt, device=cuda_device)
+    vc = torch.zeros_like(kc)
+    rk, rv = bits(kc).copy(), bits(vc).copy()
+    gq = torch.Generator().manual_seed(7)
+
+    def kv_rows(toks, positions):
+        kv = np.stack([_kv_for_prefix(toks, int(p), Hkv, D) for p in positions])
+        return torch.from_numpy(kv[:, 0]).to(dt), torch.from_numpy(kv[:, 1]).to(dt)
+
+    def write_prompt(sid, toks):
+        cached = bm.add_sequence_cached(sid, toks)
+        assert cached == ref.add_sequence_cached(sid, toks)
+        pos = np.arange(cached, len(toks))
+        k_new, v_new = kv_rows(toks, pos)
+        slots = np.array([oracle.slot_of(ref.tables[sid], int(p), bs) for p in pos], np.int64)
+        pkv.paged_kv_append(k_new.to(cuda_device), v_new.to(cuda_device), torch.from_numpy(slots).to(cuda_device),
+                            kc, vc)
+        oracle.append(bits(k_new), bits(v_new), code, slots, rk, rv, code)
+        return cached
+
+    assert write_prompt(0, prompt) == 0
+    # round 1's answer: each step appends the newest token (its id known) and decodes
+    for i, tok in enumerate(answer):
+        toks = prompt + answer[: i + 1]
+        slots, pairs = bm.append_tokens([0], [tok])
+        want_slot, want_pair = ref.append_token(0, tok)
+        assert slots[0] == want_slot and len(pairs) == 0 and want_pair is None
+        k_new, v_new = kv_rows(toks, [len(toks) - 1])
+        tables, lens = bm.tables([0])
+        q = torch.randn(1, Hq, D, generator=gq).to(dt)
+        out = pkv.paged_attention_decode_append(q.to(cuda_device), k_new.to(cuda_device), v_new.to(cuda_device),
+                                                torch.from_numpy(slots).to(cuda_device), kc, vc,
+                                                torch.from_numpy(tables).to(cuda_device),
+                                                torch.from_numpy(lens).to(cuda_device), scale)
+        oracle.append(bits(k_new), bits(v_new), code, slots, rk, rv, code)
+        if i in (0, len(answer) - 1):
+            torch.cuda.synchronize()
+            want = oracle.paged_decode(bits(q), code, rk, rv, code, tables, lens, scale)
+            assert_attention_close(out, want, TOL[act])
+    n1 = len(prompt) + len(answer)
+    assert bm.num_cached_blocks == n1 // bs == len(ref.block_of_prefix)
+    t1, _ = bm.tables([0])
+    bm.free_sequence(0)
+    ref.free_sequence(0)
+    second = prompt + answer + user
+    assert write_prompt(1, second) == (n1 // bs) * bs
+    t2, lens2 = bm.tables([1])
+    assert list(t2[0][: n1 // bs]) == list(t1[0][: n1 // bs])  # prompt and answer blocks reused
+    q = torch.randn(1, Hq, D, generator=gq).to(dt)
+    out = pkv.paged_attention_decode(q.to(cuda_device), kc, vc, torch.from_numpy(t2).to(cuda_device),
+                                     torch.from_numpy(lens2).to(cuda_device), scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(kc), rk) and np.array_equal(bits(vc), rv)
+    want = oracle.paged_decode(bits(q), code, rk, rv, code, np.asarray([ref.tables[1]], np.int32), lens2, scale)
+    assert_attention_close(out, want, TOL[act])
+    # the shared blocks hold exactly the K/V round 2 would have written itself
+    kv = np.stack([_kv_for_prefix(second, p, Hkv, D) for p in range(len(second))])
+    K = torch.from_numpy(kv[:, 0]).to(dt).double().permute(1, 0, 2)
+    V = torch.from_numpy(kv[:, 1]).to(dt).double().permute(1, 0, 2)
+    G = Hq // Hkv
+    o = torch.nn.functional.scaled_dot_product_attention(q[0].double().view(Hkv, G, 1, D),
+                                                         K[:, None].expand(Hkv, G, -1, D),
+                                                         V[:, None].expand(Hkv, G, -1, D), scale=scale)
+    assert np.abs(o.reshape(Hq, D).numpy() - want[0]).max() < 1e-9
+    assert pkv.device_error(reset=True) == 0

@@ -1,5 +1,6 @@
 """Prefix caching in the C++ block manager against the oracle allocator (which
-keys blocks by the exact token prefix instead of a hash)."""
+keys blocks by the exact token prefix instead of a hash): prompt blocks, and
+blocks filled by decoding when each appended token's id is given."""
 import numpy as np
 import pytest
 
@@ -74,7 +75,8 @@ def test_random_requests_match_oracle(pkv_lib, seed):
     systems = [list(rng.integers(0, 50, size=int(rng.integers(0, 4 * bs)))) for _ in range(3)]
     live, nid = [], 0
     for _ in range(300):
-        op = int(rng.integers(0, 5))
+        op = int(rng.integers(0, 6))
+        op = 2 if op == 5 else op  # appends twice as often: decoding fills blocks
         if op <= 1 or not live:
             toks = systems[int(rng.integers(0, 3))] + list(rng.integers(0, 3, size=int(rng.integers(0, 2 * bs))))
             try:
@@ -91,21 +93,28 @@ def test_random_requests_match_oracle(pkv_lib, seed):
             nid += 1
         elif op == 2:
             s = int(rng.choice(live))
+            with_id = rng.random() < 0.9
+            tok = int(rng.integers(0, 3))
             snap = (list(ref.free), list(ref.ref), {k: list(v) for k, v in ref.tables.items()}, dict(ref.lens),
-                    dict(ref.prefix_of_block), dict(ref.block_of_prefix), list(ref.lru))
+                    dict(ref.prefix_of_block), dict(ref.block_of_prefix), list(ref.lru),
+                    {k: list(v) for k, v in ref.tokens.items()})
             try:
-                want = ref.append_slot(s)
+                want = ref.append_token(s, tok) if with_id else ref.append_slot(s)
                 ok = True
             except RefOutOfBlocks:
                 (ref.free, ref.ref, ref.tables, ref.lens, ref.prefix_of_block, ref.block_of_prefix,
-                 ref.lru) = snap
+                 ref.lru, ref.tokens) = snap
                 ok = False
             if ok:
-                slots, pairs = bm.append_slots([s])
+                slots, pairs = bm.append_tokens([s], [tok]) if with_id else bm.append_slots([s])
                 assert slots[0] == want[0]
+                assert [tuple(p) for p in pairs] == ([want[1]] if want[1] is not None else [])
             else:
                 with pytest.raises(pkv_lib.OutOfBlocks):
-                    bm.append_slots([s])
+                    if with_id:
+                        bm.append_tokens([s], [tok])
+                    else:
+                        bm.append_slots([s])
         elif op == 3:
             parent = int(rng.choice(live))
             bm.fork(parent, nid)
@@ -120,3 +129,81 @@ def test_random_requests_match_oracle(pkv_lib, seed):
     for s in live:
         t, lens = bm.tables([s])
         assert list(t[0][: len(ref.tables[s])]) == ref.tables[s] and lens[0] == ref.lens[s]
+
+
+def test_multi_turn_hand_example_matches_oracle(pkv_lib):
+    """The oracle's hand-worked two-round dialogue (block size 4, free list
+    [5, 2, 7, 0, 1, 3, 4, 6]) through the C++ manager: the answer's tokens
+    fill block 2, which the second round finds by its prefix."""
+    fl = [5, 2, 7, 0, 1, 3, 4, 6]
+    bm = pkv_lib.BlockManager(8, 4, free_list=fl)
+    ref = RefBlockManager(8, 4, free_list=fl)
+    assert bm.add_sequence_cached(1, [11, 12, 13, 14, 15, 16]) == 0 == ref.add_sequence_cached(1, [11, 12, 13, 14,
+                                                                                                   15, 16])
+    for t, slot in ((17, 10), (18, 11), (19, 28)):
+        s, p = bm.append_tokens([1], [t])
+        assert s[0] == slot == ref.append_token(1, t)[0] and len(p) == 0
+    assert bm.num_cached_blocks == 2
+    bm.free_sequence(1)
+    ref.free_sequence(1)
+    _state(bm, ref, 8)
+    second = [11, 12, 13, 14, 15, 16, 17, 18, 19, 30, 31, 32]
+    assert bm.add_sequence_cached(2, second) == 8 == ref.add_sequence_cached(2, second)
+    t, _ = bm.tables([2])
+    assert list(t[0]) == [5, 2, 0] == ref.tables[2]
+    _state(bm, ref, 8)
+
+
+@pytest.mark.parametrize("bs", [4, 16])
+def test_next_round_reuses_prompt_and_answer_blocks(pkv_lib, bs):
+    """A dialogue: round 1's prompt, then its answer decoded token by token with
+    ids; round 2's prompt is round 1's prompt + answer + a new user turn.  Every
+    full block of round 1 (prompt blocks and answer blocks alike) is reused,
+    whether round 1 is still running or has finished."""
+    rng = np.random.default_rng(bs)
+    NB = 64
+    for finished in (False, True):
+        bm = pkv_lib.BlockManager(NB, bs)
+        ref = RefBlockManager(NB, bs)
+        prompt = list(rng.integers(0, 32000, size=3 * bs + 5))
+        answer = list(rng.integers(0, 32000, size=2 * bs + 7))
+        assert bm.add_sequence_cached(0, prompt) == 0 == ref.add_sequence_cached(0, prompt)
+        for t in answer:
+            s, _ = bm.append_tokens([0], [t])
+            assert s[0] == ref.append_token(0, t)[0]
+        n1 = len(prompt) + len(answer)
+        t1, _ = bm.tables([0])
+        if finished:
+            bm.free_sequence(0)
+            ref.free_sequence(0)
+        follow = prompt + answer + list(rng.integers(0, 32000, size=bs + 3))
+        cached = bm.add_sequence_cached(1, follow)
+        assert cached == ref.add_sequence_cached(1, follow) == (n1 // bs) * bs
+        t2, _ = bm.tables([1])
+        assert list(t2[0][: n1 // bs]) == list(t1[0][: n1 // bs])  # every full block of round 1
+        _state(bm, ref, NB)
+
+
+def test_append_without_ids_stops_registration_and_forks_inherit(pkv_lib):
+    bs = 4
+    bm = pkv_lib.BlockManager(16, bs)
+    ref = RefBlockManager(16, bs)
+    for m in (bm, ref):
+        m.add_sequence_cached(0, [1, 2, 3])
+        m.add_sequence_cached(1, [1, 2, 3])
+        m.fork(0, 2)
+    # sequence 1 appends without an id: its block is not registered when it fills
+    bm.append_slots([1])
+    ref.append_slot(1)
+    # the fork (2) and its parent (0) append the same token with ids: the parent
+    # copies the shared partial block, the last holder writes in place, and the
+    # first of them to fill registers the prefix 1, 2, 3, 9
+    s, p = bm.append_tokens([0, 2], [9, 9])
+    w0, w2 = ref.append_token(0, 9), ref.append_token(2, 9)
+    assert list(s) == [w0[0], w2[0]] and [tuple(x) for x in p] == [w0[1]]
+    _state(bm, ref, 16)
+    assert bm.num_cached_blocks == 1
+    assert bm.add_sequence_cached(3, [1, 2, 3, 9, 5]) == 4 == ref.add_sequence_cached(3, [1, 2, 3, 9, 5])
+    _state(bm, ref, 16)
+    with pytest.raises(ValueError):
+        bm.append_tokens([0], [1, 2])
