@@ -56,6 +56,8 @@ def _load():
             lib.oracle_append.restype = i32
             lib.oracle_block_copy.argtypes = [P, P, P, i32, i32, sz]
             lib.oracle_block_copy.restype = i32
+            lib.oracle_block_swap.argtypes = [P, P, P, i32, i32, sz, P, i32]
+            lib.oracle_block_swap.restype = i32
             lib.oracle_decode_array.argtypes = [P, i32, sz, P]
             lib.oracle_decode_array.restype = None
             lib.oracle_e4m3_encode_array.argtypes = [P, sz, P]
@@ -159,6 +161,33 @@ def block_copy(k_cache, v_cache, src_dst_pairs):
     rc = _load().oracle_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0], NB, block_bytes)
     if rc != 0:
         raise ValueError("oracle_block_copy: block id outside the pool")
+
+
+def block_swap_out(k_cache, v_cache, block_ids) -> np.ndarray:
+    """Staging bytes [n, 2, block_bytes]: entry i = K block ids[i], then V block ids[i]."""
+    ids = np.ascontiguousarray(block_ids, dtype=np.int32).reshape(-1)
+    assert k_cache.flags["C_CONTIGUOUS"] and v_cache.flags["C_CONTIGUOUS"]
+    NB = k_cache.shape[0]
+    block_bytes = k_cache[0].nbytes
+    staging = np.zeros((len(ids), 2, block_bytes), np.uint8)
+    rc = _load().oracle_block_swap(_ptr(k_cache), _ptr(v_cache), _ptr(ids), len(ids), NB, block_bytes,
+                                   _ptr(staging), 0)
+    if rc != 0:
+        raise ValueError("oracle_block_swap: block id outside the pool")
+    return staging
+
+
+def block_swap_in(k_cache, v_cache, block_ids, staging) -> None:
+    """Write staging entry i back into block ids[i] of both caches, in place."""
+    ids = np.ascontiguousarray(block_ids, dtype=np.int32).reshape(-1)
+    staging = np.ascontiguousarray(staging, dtype=np.uint8)
+    NB = k_cache.shape[0]
+    block_bytes = k_cache[0].nbytes
+    assert staging.shape == (len(ids), 2, block_bytes)
+    rc = _load().oracle_block_swap(_ptr(k_cache), _ptr(v_cache), _ptr(ids), len(ids), NB, block_bytes,
+                                   _ptr(staging), 1)
+    if rc != 0:
+        raise ValueError("oracle_block_swap: block id outside the pool")
 
 
 def quest_select(q, q_dtype, k_cache, cache_dtype, block_tables, context_lens, budget_blocks, k_scale=1.0):

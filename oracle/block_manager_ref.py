@@ -172,7 +172,10 @@ class RefBlockManager:
         """Release a finished request: counts - 1, blocks at 0 go back to the pool."""
         self.tokens.pop(seq, None)
         if seq in getattr(self, "swapped", {}):
-            del self.swapped[seq]
+            gid = self.swapped.pop(seq)["group"]
+            self.swap_groups[gid]["members"].discard(seq)
+            if not self.swap_groups[gid]["members"]:
+                del self.swap_groups[gid]
             return
         for b in self.tables.pop(seq):
             self.ref[b] -= 1
@@ -186,26 +189,72 @@ class RefBlockManager:
     def swap_out(self, seq) -> list:
         """Preemption by swapping (PagedAttention notes, section on preemption):
         release the sequence's blocks, remember its length; returns its table."""
-        table = self.tables.pop(seq)
-        for b in table:
-            self.ref[b] -= 1
-            if self.ref[b] == 0:
-                if b in self.prefix_of_block:
-                    self.lru.append(b)
-                else:
-                    self.free.append(b)
-        self.swapped = getattr(self, "swapped", {})
-        self.swapped[seq] = self.lens.pop(seq)
-        return table
+        return self.swap_out_group([seq])
 
     def swap_in(self, seq) -> list:
         """Give a swapped-out sequence ceil(len / bs) fresh blocks; returns them."""
-        n = -(-self.swapped[seq] // self.block_size)
+        return self.swap_in_group([seq])
+
+    def swap_out_group(self, seqs) -> list:
+        """Swap out several sequences together (the samples of one prompt):
+        their distinct blocks, in first-use order (members in the given order,
+        each table in logical order), are listed once -- each is staged once --
+        and every member remembers its table as positions in that list.  Then
+        each member releases its blocks (members in order, tables in logical
+        order).  Returns the list."""
+        seqs = list(seqs)
+        assert len(set(seqs)) == len(seqs)
+        staged, pos = [], {}
+        for s in seqs:
+            for b in self.tables[s]:
+                if b not in pos:
+                    pos[b] = len(staged)
+                    staged.append(b)
+        self.swapped = getattr(self, "swapped", {})
+        self.swap_groups = getattr(self, "swap_groups", {})
+        gid = object()
+        self.swap_groups[gid] = {"members": set(seqs), "staged": len(staged)}
+        for s in seqs:
+            table = self.tables.pop(s)
+            for b in table:
+                self.ref[b] -= 1
+                if self.ref[b] == 0:
+                    if b in self.prefix_of_block:
+                        self.lru.append(b)
+                    else:
+                        self.free.append(b)
+            self.swapped[s] = {"len": self.lens.pop(s), "idx": [pos[b] for b in table], "group": gid}
+        return staged
+
+    def swap_in_group(self, seqs) -> list:
+        """Bring a group swapped out together back (the same members, in any
+        order; a member freed meanwhile is left out): one fresh block per
+        listed entry, taken in list order; each member's table is rebuilt over
+        them, so blocks the members shared are shared again, with counts equal
+        to the number of members holding them.  An entry no member holds any
+        more is released at once.  Returns the blocks, in list order."""
+        seqs = list(seqs)
+        gid = self.swapped[seqs[0]]["group"]
+        grp = self.swap_groups[gid]
+        assert set(seqs) == grp["members"], "swap in the whole group"
+        n = grp["staged"]
         if n > self.available():
             raise OutOfBlocks("not enough free blocks")
-        self.lens[seq] = self.swapped.pop(seq)
-        self.tables[seq] = [self._take() for _ in range(n)]
-        return list(self.tables[seq])
+        blocks = [self._take() for _ in range(n)]
+        held = [0] * n
+        for s in seqs:
+            for i in self.swapped[s]["idx"]:
+                held[i] += 1
+        for i, b in enumerate(blocks):
+            self.ref[b] = held[i]
+            if held[i] == 0:
+                self.free.append(b)
+        for s in seqs:
+            info = self.swapped.pop(s)
+            self.tables[s] = [blocks[i] for i in info["idx"]]
+            self.lens[s] = info["len"]
+        del self.swap_groups[gid]
+        return blocks
 
     def unused_slots(self, seq: int) -> int:
         """Slots allocated to the request but not yet written."""

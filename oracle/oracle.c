@@ -270,6 +270,30 @@ int oracle_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs
     return 0;
 }
 
+/* Preemption by swapping (the PagedAttention notes page, section on
+ * preemption): the blocks of a preempted sequence are copied out of the pool
+ * and later copied back into the blocks it is given.  Staging entry i holds
+ * block ids[i] of the K cache, then the same block of the V cache.
+ * direction 0: staging[i] = (K[ids[i]], V[ids[i]]); 1: the reverse. */
+int oracle_block_swap(void* k_cache, void* v_cache, const int32_t* ids, int num_ids, int num_blocks,
+                      size_t block_bytes, void* staging, int direction) {
+    for (int i = 0; i < num_ids; ++i) {
+        int b = ids[i];
+        if (b < 0 || b >= num_blocks) return -1;
+        char* st = (char*)staging + (size_t)i * 2 * block_bytes;
+        char* kb = (char*)k_cache + (size_t)b * block_bytes;
+        char* vb = (char*)v_cache + (size_t)b * block_bytes;
+        if (direction == 0) {
+            memcpy(st, kb, block_bytes);
+            memcpy(st + block_bytes, vb, block_bytes);
+        } else {
+            memcpy(kb, st, block_bytes);
+            memcpy(vb, st + block_bytes, block_bytes);
+        }
+    }
+    return 0;
+}
+
 /* Number of OpenMP threads the attention oracle runs with. */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

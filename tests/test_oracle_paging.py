@@ -197,7 +197,7 @@ def test_reference_swap_hand_example():
     ref.add_sequence("c", 20)                       # 5 blocks: b's freed blocks
     with pytest.raises(OutOfBlocks):
         ref.swap_in("b")                            # no room: b stays swapped out
-    assert ref.swapped == {"b": 17}
+    assert set(ref.swapped) == {"b"} and ref.swapped["b"]["len"] == 17
     # a forked sequence shares its parent's blocks: swapping the child out
     # releases nothing, swapping the parent out too releases them
     ref2 = RefBlockManager(4, 4)
@@ -251,3 +251,56 @@ def test_reference_prefix_cache_multi_turn_hand_example():
         ref.append_token("r4", t)
         ref.append_token("r5", t)
     assert ref.block_of_prefix[(50, 51, 52, 53)] == ref.tables["r4"][0] != ref.tables["r5"][0]
+
+
+def test_reference_group_swap_hand_example():
+    """Swapping a forked group together keeps its sharing, worked by hand.
+    Block size 4, free list 0..9.  p holds 6 tokens in blocks [0, 1]; c1 and c2
+    fork p; c1 appends a token, copying the shared partial block 1 to block 2.
+    Tables p = [0, 1], c1 = [0, 2], c2 = [0, 1]; counts 0:3, 1:2, 2:1.
+
+    swap_out_group(p, c1, c2) lists the distinct blocks once, in first-use
+    order: [0, 1, 2] (three stagings, not six).  Releases run member by
+    member, table order: 2 reaches 0 in c1's release, then 0 and 1 in c2's,
+    so the free list becomes 3..9, 2, 0, 1.
+
+    swap_in_group takes three fresh blocks from the front, 3, 4, 5, for list
+    entries 0, 1, 2: p = [3, 4], c1 = [3, 5], c2 = [3, 4], counts 3:3, 4:2,
+    5:1 -- the sharing is back, so c2's next token copies block 4 again."""
+    from oracle.block_manager_ref import RefBlockManager
+    ref = RefBlockManager(10, 4)
+    ref.add_sequence("p", 6)
+    ref.fork("p", "c1")
+    ref.fork("p", "c2")
+    assert ref.append_slot("c1") == (2 * 4 + 2, (1, 2))
+    assert (ref.tables["p"], ref.tables["c1"], ref.tables["c2"]) == ([0, 1], [0, 2], [0, 1])
+    assert ref.swap_out_group(["p", "c1", "c2"]) == [0, 1, 2]
+    assert ref.free == [3, 4, 5, 6, 7, 8, 9, 2, 0, 1] and ref.ref[:3] == [0, 0, 0]
+    assert ref.swap_in_group(["c2", "p", "c1"]) == [3, 4, 5]
+    assert (ref.tables["p"], ref.tables["c1"], ref.tables["c2"]) == ([3, 4], [3, 5], [3, 4])
+    assert ref.ref[3:6] == [3, 2, 1] and ref.lens == {"p": 6, "c1": 7, "c2": 6}
+    assert ref.append_slot("c2") == (6 * 4 + 2, (4, 6))
+    # a member freed while swapped out: its only block is taken and released at once
+    ref2 = RefBlockManager(6, 4)
+    ref2.add_sequence("a", 4)                       # block 0 (full)
+    ref2.fork("a", "b")
+    ref2.append_slot("b")                           # b: [0, 1]
+    assert ref2.swap_out_group(["a", "b"]) == [0, 1]
+    ref2.free_sequence("b")
+    assert ref2.swap_in_group(["a"]) == [2, 3]
+    assert ref2.tables["a"] == [2] and ref2.ref[2:4] == [1, 0] and ref2.free[-1] == 3
+
+
+def test_reference_block_swap_bytes(oracle_mod):
+    """Swap staging by hand: every byte of K block b is b, of V block b is 100 + b;
+    ids [3, 0, 2] stage entries (3, 103), (0, 100), (2, 102); swapping the
+    entries back in to blocks [1, 4, 0] makes those blocks hold them."""
+    NB, nbytes = 5, 32
+    k = np.repeat(np.arange(NB, dtype=np.uint8), nbytes).reshape(NB, 2, 16)
+    v = (k + 100).astype(np.uint8)
+    st = oracle_mod.block_swap_out(k, v, [3, 0, 2])
+    assert st.shape == (3, 2, nbytes)
+    assert [int(x) for x in st[:, 0, 0]] == [3, 0, 2] and [int(x) for x in st[:, 1, 0]] == [103, 100, 102]
+    assert all(np.all(st[i, j] == st[i, j, 0]) for i in range(3) for j in range(2))
+    oracle_mod.block_swap_in(k, v, [1, 4, 0], st)
+    assert [int(x) for x in k[:, 0, 0]] == [2, 3, 2, 3, 0] and [int(x) for x in v[:, 0, 0]] == [102, 103, 102, 103, 100]
