@@ -612,6 +612,25 @@ def run_swap(args):
     pkv.load()
     Hkv, D = 32, 128
     total = 1 << 30  # bytes of K+V moved per direction
+    # the ceiling on this machine: one contiguous 1 GiB cudaMemcpyAsync per direction
+    dbuf = torch.empty(total, dtype=torch.uint8, device=dev).fill_(1)
+    hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    ceiling = {}
+    for name, (dst, src) in (("out", (hbuf, dbuf)), ("in", (dbuf, hbuf))):
+        for _ in range(2):
+            dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        ceiling[name] = total * args.steps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del dbuf, hbuf
+    print(json.dumps({"measure": "ceiling: one contiguous 1 GiB pinned cudaMemcpyAsync per direction",
+                      "memcpy_out_gbs": round(ceiling["out"], 1), "memcpy_in_gbs": round(ceiling["in"], 1)}),
+          flush=True)
     for bs in (1, 4, 16, 32, 64):
         block_bytes = Hkv * bs * D * 2
         n = total // (2 * block_bytes)
@@ -645,6 +664,8 @@ def run_swap(args):
         e1.record()
         torch.cuda.synchronize()
         res["per_block_memcpy_out_gbs"] = round(2 * block_bytes * m / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+        res["kernel_out_frac_of_memcpy"] = round(res["kernel_out_gbs"] / ceiling["out"], 3)
+        res["kernel_in_frac_of_memcpy"] = round(res["kernel_in_gbs"] / ceiling["in"], 3)
         print(json.dumps({"measure": "block swap, pools <-> pinned host memory", "block_size_tokens": bs,
                           "block_bytes_per_cache": block_bytes, "blocks": int(n), "bytes_per_direction": total,
                           **res}), flush=True)

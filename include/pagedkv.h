@@ -475,16 +475,38 @@ int pkv_bm_add_sequence_cached(pkv_block_manager* bm, int64_t seq_id, const int3
 int pkv_bm_append_tokens(pkv_block_manager* bm, const int64_t* seq_ids, const int32_t* token_ids, int n,
                          int64_t* slots_out, int32_t* cow_pairs_out, int* num_cow_pairs);
 /* Preemption by swapping (the PagedAttention notes page, section on
- * preemption).  pkv_bm_swap_out writes the sequence's block table (logical
- * order, host int32, capacity cap) to blocks_out and *n, then releases the
- * blocks (counts - 1) and keeps the sequence as swapped out (its length is
- * remembered; it holds no blocks).  Run paged_block_swap(PKV_SWAP_OUT) on
- * those blocks before any later call reuses them on the same stream.
- * pkv_bm_swap_in gives a swapped-out sequence ceil(len/block_size) fresh
- * private blocks (sharing with forks is not restored), writes them to
- * blocks_out, and makes it resident; run paged_block_swap(PKV_SWAP_IN) into
- * them.  A swapped-out sequence cannot append, fork or appear in tables;
- * pkv_bm_free_sequence accepts it.  PKV_ERR_NO_SPACE leaves no trace. */
+ * preemption: the KV of a preempted sequence group moves to CPU memory and
+ * comes back when there is room; iThome "how to store the KV cache",
+ * section "Physical Block sharing": forked samples share blocks).
+ *
+ * pkv_bm_swap_out_group swaps out n_seqs sequences together (e.g. the
+ * samples of one prompt).  It writes their DISTINCT blocks to blocks_out
+ * (host int32, capacity cap) and their count to *n, in first-use order
+ * (members in the given order, each table in logical order), so a block the
+ * members share is listed -- and staged -- once.  Each member remembers its
+ * table as positions in that list and its length; then the members release
+ * their blocks (counts - 1, in the same order) and hold none.  Run
+ * paged_block_swap(PKV_SWAP_OUT) on the listed blocks before any later call
+ * reuses them on the same stream.
+ *
+ * pkv_bm_swap_in_group brings the group back: seq_ids must be exactly the
+ * members swapped out together (any order; members freed since are left
+ * out).  It takes one fresh block per listed entry, from the front of the
+ * free list in list order, writes them to blocks_out in that order (run
+ * paged_block_swap(PKV_SWAP_IN) into them with the same staging), and
+ * rebuilds every member's table over them: blocks the members shared are
+ * shared again, each with a count equal to the number of members holding
+ * it, so copy-on-write continues as before the swap.  An entry that no
+ * remaining member holds goes straight back to the free list.
+ *
+ * pkv_bm_swap_out / pkv_bm_swap_in are the group of one.  A swapped-out
+ * sequence cannot append, fork or appear in tables; pkv_bm_free_sequence
+ * accepts it.  Unknown, repeated or resident ids give PKV_ERR_NOT_FOUND;
+ * PKV_ERR_NO_SPACE and PKV_ERR_SHAPE (cap too small) leave no trace. */
+int pkv_bm_swap_out_group(pkv_block_manager* bm, const int64_t* seq_ids, int n_seqs, int32_t* blocks_out,
+                          int cap, int* n);
+int pkv_bm_swap_in_group(pkv_block_manager* bm, const int64_t* seq_ids, int n_seqs, int32_t* blocks_out,
+                         int cap, int* n);
 int pkv_bm_swap_out(pkv_block_manager* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n);
 int pkv_bm_swap_in(pkv_block_manager* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n);
 

@@ -426,6 +426,29 @@ class BlockManager:
             self._h, int(seq_id), out.ctypes.data_as(ctypes.c_void_p), len(out), ctypes.byref(cnt)))
         return out[: cnt.value].copy()
 
+    def swap_out_group(self, seq_ids) -> np.ndarray:
+        """Swap out sequences together (e.g. one prompt's samples): returns their
+        distinct blocks, first-use order, each to be staged once."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        cap = max(sum(max(self.num_seq_blocks(s), 0) for s in ids), 1)
+        out = np.empty(cap, np.int32)
+        cnt = ctypes.c_int(0)
+        self._check("pkv_bm_swap_out_group", _native.lib().pkv_bm_swap_out_group(
+            self._h, ids.ctypes.data_as(ctypes.c_void_p), len(ids), out.ctypes.data_as(ctypes.c_void_p), cap,
+            ctypes.byref(cnt)))
+        return out[: cnt.value].copy()
+
+    def swap_in_group(self, seq_ids, max_blocks: int) -> np.ndarray:
+        """Bring a group swapped out together back: one fresh block per staged
+        entry (returned in staging order); shared blocks are shared again."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        out = np.empty(max(max_blocks, 1), np.int32)
+        cnt = ctypes.c_int(0)
+        self._check("pkv_bm_swap_in_group", _native.lib().pkv_bm_swap_in_group(
+            self._h, ids.ctypes.data_as(ctypes.c_void_p), len(ids), out.ctypes.data_as(ctypes.c_void_p), len(out),
+            ctypes.byref(cnt)))
+        return out[: cnt.value].copy()
+
     @property
     def num_cached_blocks(self) -> int:
         return int(_native.lib().pkv_bm_num_cached_blocks(self._h))

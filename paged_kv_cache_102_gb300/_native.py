@@ -55,6 +55,8 @@ SIGNATURES = {
     "pkv_bm_get_tables": (I32, [P, P, I32, P, I32, I32, P]),
     "pkv_bm_add_sequence_cached": (I32, [P, I64, P, I32, P]),
     "pkv_bm_num_cached_blocks": (I32, [P]),
+    "pkv_bm_swap_out_group": (I32, [P, P, I32, P, I32, P]),
+    "pkv_bm_swap_in_group": (I32, [P, P, I32, P, I32, P]),
     "pkv_bm_swap_out": (I32, [P, I64, P, I32, P]),
     "pkv_bm_swap_in": (I32, [P, I64, P, I32, P]),
     "pkv_bm_num_free": (I32, [P]),

@@ -48,6 +48,8 @@ struct Sequence {
     std::vector<int32_t> blocks;
     int64_t len = 0;
     bool swapped = false;  // contents staged outside the pool; no blocks held
+    int64_t swap_group = -1;          // the group it was swapped out with
+    std::vector<int32_t> staged_idx;  // while swapped: its table as positions in the group's staged list
     // prefix caching: set for sequences added from their token ids, cleared by
     // an append without token ids
     bool tracked = false;
@@ -86,12 +88,24 @@ uint64_t block_hash(uint64_t parent, const int32_t* tokens, int n) {
 
 }  // namespace
 
+namespace {
+
+// Sequences swapped out together: their distinct blocks were staged once.
+struct SwapGroup {
+    std::unordered_set<int64_t> members;
+    int n_staged = 0;
+};
+
+}  // namespace
+
 struct pkv_block_manager {
     int num_blocks = 0;
     int block_size = 0;
     std::deque<int32_t> free_list;
     std::vector<int32_t> ref;
     std::unordered_map<int64_t, Sequence> seqs;
+    std::unordered_map<int64_t, SwapGroup> swap_groups;
+    int64_t next_swap_group = 0;
     // prefix cache
     std::unordered_map<uint64_t, int32_t> cached;  // hash -> block
     std::vector<uint64_t> hash_of;                 // per block, valid when registered[b]
@@ -309,6 +323,13 @@ int pkv_bm_free_sequence(pkv_block_manager* bm, int64_t seq_id) {
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_free_sequence: unknown id");
     for (int32_t b : it->second.blocks) bm->release(b);  // a swapped-out sequence holds none
+    if (it->second.swapped) {
+        auto g = bm->swap_groups.find(it->second.swap_group);
+        if (g != bm->swap_groups.end()) {
+            g->second.members.erase(seq_id);
+            if (g->second.members.empty()) bm->swap_groups.erase(g);
+        }
+    }
     bm->seqs.erase(it);
     return PKV_OK;
 }
@@ -380,39 +401,89 @@ int pkv_bm_add_sequence_cached(pkv_block_manager* bm, int64_t seq_id, const int3
     return PKV_OK;
 }
 
-int pkv_bm_swap_out(pkv_block_manager* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n) {
-    if (!bm || !n || cap < 0) return pkv::fail(PKV_ERR_INVALID, "pkv_bm_swap_out: bad arguments");
-    auto it = bm->seqs.find(seq_id);
-    if (it == bm->seqs.end() || it->second.swapped)
-        return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_swap_out: unknown or already swapped-out id");
-    Sequence& s = it->second;
-    const int nb = static_cast<int>(s.blocks.size());
-    if (nb > cap || (nb > 0 && !blocks_out)) return pkv::fail(PKV_ERR_SHAPE, "pkv_bm_swap_out: output too small");
-    for (int i = 0; i < nb; ++i) blocks_out[i] = s.blocks[i];
-    for (int32_t b : s.blocks) bm->release(b);
-    s.blocks.clear();
-    s.swapped = true;
-    *n = nb;
+int pkv_bm_swap_out_group(pkv_block_manager* bm, const int64_t* seq_ids, int n_seqs, int32_t* blocks_out, int cap,
+                          int* n) {
+    if (!bm || !n || cap < 0 || n_seqs < 1 || !seq_ids)
+        return pkv::fail(PKV_ERR_INVALID, "pkv_bm_swap_out_group: bad arguments");
+    // distinct blocks in first-use order: members in call order, tables in logical order
+    std::unordered_set<int64_t> seen;
+    std::unordered_map<int32_t, int32_t> pos;
+    std::vector<int32_t> staged;
+    for (int i = 0; i < n_seqs; ++i) {
+        auto it = bm->seqs.find(seq_ids[i]);
+        if (it == bm->seqs.end() || it->second.swapped || !seen.insert(seq_ids[i]).second)
+            return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_swap_out_group: unknown, repeated or swapped-out id");
+        for (int32_t b : it->second.blocks)
+            if (pos.emplace(b, static_cast<int32_t>(staged.size())).second) staged.push_back(b);
+    }
+    const int ns = static_cast<int>(staged.size());
+    if (ns > cap || (ns > 0 && !blocks_out)) return pkv::fail(PKV_ERR_SHAPE, "pkv_bm_swap_out_group: output too small");
+    const int64_t gid = bm->next_swap_group++;
+    SwapGroup& g = bm->swap_groups[gid];
+    g.n_staged = ns;
+    for (int i = 0; i < ns; ++i) blocks_out[i] = staged[i];
+    for (int i = 0; i < n_seqs; ++i) {
+        Sequence& s = bm->seqs[seq_ids[i]];
+        s.staged_idx.clear();
+        for (int32_t b : s.blocks) {
+            s.staged_idx.push_back(pos[b]);
+            bm->release(b);
+        }
+        s.blocks.clear();
+        s.swapped = true;
+        s.swap_group = gid;
+        g.members.insert(seq_ids[i]);
+    }
+    *n = ns;
     return PKV_OK;
 }
 
-int pkv_bm_swap_in(pkv_block_manager* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n) {
-    if (!bm || !n || cap < 0) return pkv::fail(PKV_ERR_INVALID, "pkv_bm_swap_in: bad arguments");
-    auto it = bm->seqs.find(seq_id);
-    if (it == bm->seqs.end() || !it->second.swapped)
-        return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_swap_in: unknown or resident id");
-    Sequence& s = it->second;
-    const int nb = static_cast<int>((s.len + bm->block_size - 1) / bm->block_size);
-    if (nb > cap || (nb > 0 && !blocks_out)) return pkv::fail(PKV_ERR_SHAPE, "pkv_bm_swap_in: output too small");
-    if (nb > bm->available()) return pkv::fail(PKV_ERR_NO_SPACE, "pkv_bm_swap_in: not enough free blocks");
-    for (int i = 0; i < nb; ++i) {
+int pkv_bm_swap_in_group(pkv_block_manager* bm, const int64_t* seq_ids, int n_seqs, int32_t* blocks_out, int cap,
+                         int* n) {
+    if (!bm || !n || cap < 0 || n_seqs < 1 || !seq_ids)
+        return pkv::fail(PKV_ERR_INVALID, "pkv_bm_swap_in_group: bad arguments");
+    auto first = bm->seqs.find(seq_ids[0]);
+    if (first == bm->seqs.end() || !first->second.swapped)
+        return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_swap_in_group: unknown or resident id");
+    auto git = bm->swap_groups.find(first->second.swap_group);
+    if (git == bm->swap_groups.end()) return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_swap_in_group: unknown group");
+    SwapGroup& g = git->second;
+    std::unordered_set<int64_t> given(seq_ids, seq_ids + n_seqs);
+    if (static_cast<int>(given.size()) != n_seqs || given != g.members)
+        return pkv::fail(PKV_ERR_NOT_FOUND,
+                         "pkv_bm_swap_in_group: the ids must be exactly the sequences swapped out together "
+                         "(minus any freed since)");
+    const int ns = g.n_staged;
+    if (ns > cap || (ns > 0 && !blocks_out)) return pkv::fail(PKV_ERR_SHAPE, "pkv_bm_swap_in_group: output too small");
+    if (ns > bm->available()) return pkv::fail(PKV_ERR_NO_SPACE, "pkv_bm_swap_in_group: not enough free blocks");
+    std::vector<int32_t> held(ns, 0);
+    for (int i = 0; i < n_seqs; ++i)
+        for (int32_t k : bm->seqs[seq_ids[i]].staged_idx) ++held[k];
+    for (int k = 0; k < ns; ++k) {
         const int32_t b = bm->take();
-        s.blocks.push_back(b);
-        blocks_out[i] = b;
+        blocks_out[k] = b;
+        bm->ref[b] = held[k];
+        if (held[k] == 0) bm->free_list.push_back(b);  // no member holds this entry any more
     }
-    s.swapped = false;
-    *n = nb;
+    for (int i = 0; i < n_seqs; ++i) {
+        Sequence& s = bm->seqs[seq_ids[i]];
+        s.blocks.clear();
+        for (int32_t k : s.staged_idx) s.blocks.push_back(blocks_out[k]);
+        s.staged_idx.clear();
+        s.swapped = false;
+        s.swap_group = -1;
+    }
+    bm->swap_groups.erase(git);
+    *n = ns;
     return PKV_OK;
+}
+
+int pkv_bm_swap_out(pkv_block_manager* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n) {
+    return pkv_bm_swap_out_group(bm, &seq_id, 1, blocks_out, cap, n);
+}
+
+int pkv_bm_swap_in(pkv_block_manager* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n) {
+    return pkv_bm_swap_in_group(bm, &seq_id, 1, blocks_out, cap, n);
 }
 
 int pkv_bm_num_cached_blocks(const pkv_block_manager* bm) { return bm ? static_cast<int>(bm->cached.size()) : -1; }

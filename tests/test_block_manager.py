@@ -228,3 +228,115 @@ def test_copy_on_write_without_a_free_block_changes_nothing(pkv_lib):
     bm.free_sequence(3)  # a block comes back; now the copy succeeds
     slots, copies = bm.append_slots([2])
     assert len(copies) == 1 and copies[0][0] == shared and bm.ref_count(shared) == 1
+
+
+def test_group_swap_hand_example_matches_oracle(pkv_lib):
+    """The oracle's hand-worked group swap (block size 4, free list 0..9):
+    three forked samples stage their 3 distinct blocks once and get them back
+    shared (counts 3, 2, 1)."""
+    bm = pkv_lib.BlockManager(10, 4)
+    ref = RefBlockManager(10, 4)
+    ids = {"p": 0, "c1": 1, "c2": 2}
+    for m, key in ((bm, lambda x: ids[x]), (ref, lambda x: x)):
+        m.add_sequence(key("p"), 6)
+        m.fork(key("p"), key("c1"))
+        m.fork(key("p"), key("c2"))
+    s, pairs = bm.append_slots([1])
+    assert (s[0], tuple(pairs[0])) == ref.append_slot("c1")
+    assert list(bm.swap_out_group([0, 1, 2])) == ref.swap_out_group(["p", "c1", "c2"]) == [0, 1, 2]
+    assert list(bm.free_list()) == ref.free
+    assert list(bm.swap_in_group([2, 0, 1], 8)) == ref.swap_in_group(["c2", "p", "c1"]) == [3, 4, 5]
+    t, lens = bm.tables([0, 1, 2])
+    assert [list(r[:2]) for r in t] == [ref.tables["p"], ref.tables["c1"], ref.tables["c2"]]
+    assert [bm.ref_count(b) for b in range(10)] == ref.ref
+    s, pairs = bm.append_slots([2])
+    assert (s[0], tuple(pairs[0])) == ref.append_slot("c2")
+    # the single-sequence calls refuse a member of a group
+    bm.swap_out_group([0, 1])
+    with pytest.raises(pkv_lib.PagedKVError):
+        bm.swap_in(0, 8)
+    with pytest.raises(pkv_lib.PagedKVError):
+        bm.swap_in_group([0], 8)
+    assert len(bm.swap_in_group([1, 0], 8)) == 3
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_group_swap_matches_oracle(pkv_lib, seed):
+    """Random forks, appends (with copy-on-write), group swaps, frees of
+    resident and swapped members: lists, tables, counts and free lists equal
+    the oracle allocator's after every step."""
+    rng = np.random.default_rng(300 + seed)
+    NB, bs = int(rng.integers(16, 48)), int(rng.choice([2, 4, 16]))
+    fl = rng.permutation(NB).astype(np.int32)
+    bm = pkv_lib.BlockManager(NB, bs, free_list=fl)
+    ref = RefBlockManager(NB, bs, free_list=fl)
+    live, groups, nid = [], [], 0
+
+    def check():
+        assert [bm.ref_count(b) for b in range(NB)] == ref.ref
+        assert list(bm.free_list()) == ref.free
+        if live:
+            t, lens = bm.tables(live)
+            for i, s in enumerate(live):
+                assert list(t[i][: len(ref.tables[s])]) == ref.tables[s] and lens[i] == ref.lens[s]
+
+    for _ in range(300):
+        op = int(rng.integers(0, 7))
+        if op == 0 or not (live or groups):
+            n = int(rng.integers(1, 3 * bs))
+            try:
+                ref.add_sequence(nid, n)
+                bm.add_sequence(nid, n)
+                live.append(nid)
+            except RefOutOfBlocks:
+                with pytest.raises(pkv_lib.OutOfBlocks):
+                    bm.add_sequence(nid, n)
+            nid += 1
+        elif op in (1, 2) and live:
+            s = int(rng.choice(live))
+            try:
+                want = ref.append_slot(s)
+            except RefOutOfBlocks:
+                with pytest.raises(pkv_lib.OutOfBlocks):
+                    bm.append_slots([s])
+                continue
+            slots, pairs = bm.append_slots([s])
+            assert slots[0] == want[0] and [tuple(p) for p in pairs] == ([want[1]] if want[1] else [])
+        elif op == 3 and live:
+            parent = int(rng.choice(live))
+            ref.fork(parent, nid)
+            bm.fork(parent, nid)
+            live.append(nid)
+            nid += 1
+        elif op == 4 and live:
+            k = int(rng.integers(1, min(4, len(live)) + 1))
+            members = [int(x) for x in rng.choice(live, size=k, replace=False)]
+            assert list(bm.swap_out_group(members)) == ref.swap_out_group(members)
+            for s in members:
+                live.remove(s)
+            groups.append(members)
+        elif op == 5 and groups:
+            g = groups[int(rng.integers(0, len(groups)))]
+            order = [int(x) for x in rng.permutation(g)]
+            try:
+                want = ref.swap_in_group(order)
+            except RefOutOfBlocks:
+                with pytest.raises(pkv_lib.OutOfBlocks):
+                    bm.swap_in_group(order, 4 * NB)
+                continue
+            assert list(bm.swap_in_group(order, 4 * NB)) == want
+            groups.remove(g)
+            live.extend(g)
+        elif op == 6 and (live or groups):
+            pool = live + [s for g in groups for s in g]
+            s = pool[int(rng.integers(0, len(pool)))]
+            bm.free_sequence(s)
+            ref.free_sequence(s)
+            if s in live:
+                live.remove(s)
+            else:
+                for g in groups:
+                    if s in g:
+                        g.remove(s)
+                groups = [g for g in groups if g]
+        check()
