@@ -110,3 +110,58 @@ def test_minmax_matches_hand_example(oracle_mod):
     mn, mx = oracle_mod.quest_block_minmax(_bits(kc), 0, np.array([g["block_table"]], np.int32),
                                            np.array([g["context_len"]], np.int32))
     assert mn[0, :, 0].tolist() == g["expected_min"] and mx[0, :, 0].tolist() == g["expected_max"]
+
+
+def _e4m3_paged(rng, B, Hkv, L, D, bs):
+    codes = torch.from_numpy(rng.integers(0, 256, size=(B, Hkv, L, D), dtype=np.uint8))
+    codes[(codes & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    kp, _, tables = _paged_from_contiguous(codes, codes, np.full(B, L), bs, rng)
+    return codes, kp, tables
+
+
+def test_e4m3_bound_dominates_every_dequantised_key(oracle_mod):
+    """Over an E4M3 cache the bound covers q . (code x k_scale) for every key
+    of the block, the codes decoded by torch's float8_e4m3fn."""
+    rng = np.random.default_rng(31)
+    B, Hkv, G, D, bs, L, ks = 2, 2, 4, 32, 8, 45, 0.0137
+    codes, kp, tables = _e4m3_paged(rng, B, Hkv, L, D, bs)
+    q = torch.from_numpy(rng.standard_normal((B, Hkv * G, D))).to(torch.bfloat16)
+    lens = np.full(B, L, np.int32)
+    _, _, bounds = oracle_mod.quest_select(_bits(q), 1, kp.numpy(), 2, tables, lens, 2, k_scale=ks)
+    vals = codes.view(torch.float8_e4m3fn).double() * ks
+    for b in range(B):
+        for h in range(Hkv):
+            for j in range(-(-L // bs)):
+                keys = vals[b, h, j * bs: min((j + 1) * bs, L)].numpy()
+                qs = q[b, h * G:(h + 1) * G].double().numpy()
+                assert bounds[b, h, j] >= float((qs @ keys.T).max()) - 1e-9
+
+
+def test_e4m3_selection_does_not_depend_on_the_scale(oracle_mod):
+    """A positive per-tensor scale multiplies every bound by itself, so the
+    selection is the same for any k_scale > 0 (bounds scale exactly in ratio)."""
+    rng = np.random.default_rng(32)
+    B, Hkv, G, D, bs, L = 3, 2, 2, 64, 16, 300
+    codes, kp, tables = _e4m3_paged(rng, B, Hkv, L, D, bs)
+    q = torch.from_numpy(rng.standard_normal((B, Hkv * G, D))).to(torch.float16)
+    lens = np.full(B, L, np.int32)
+    s1, l1, u1 = oracle_mod.quest_select(_bits(q), 0, kp.numpy(), 2, tables, lens, 5, k_scale=1.0)
+    s2, l2, u2 = oracle_mod.quest_select(_bits(q), 0, kp.numpy(), 2, tables, lens, 5, k_scale=0.0219)
+    assert np.array_equal(s1, s2) and np.array_equal(l1, l2)
+    n = -(-L // bs)
+    np.testing.assert_allclose(u2[:, :, :n], 0.0219 * u1[:, :, :n], rtol=1e-12, atol=0)
+
+
+def test_e4m3_minmax_is_the_decoded_codes(oracle_mod):
+    """E4M3 metadata: channel-wise min and max of the decoded codes (no scale),
+    against torch's float8_e4m3fn decoding."""
+    rng = np.random.default_rng(33)
+    B, Hkv, D, bs, L = 2, 3, 16, 8, 21
+    codes, kp, tables = _e4m3_paged(rng, B, Hkv, L, D, bs)
+    mn, mx = oracle_mod.quest_block_minmax(kp.numpy(), 2, tables, np.full(B, L, np.int32))
+    vals = codes.view(torch.float8_e4m3fn).double()
+    for b in range(B):
+        for j in range(-(-L // bs)):
+            blk = vals[b, :, j * bs: min((j + 1) * bs, L)]
+            np.testing.assert_array_equal(mn[b, j], blk.min(dim=1).values.numpy())
+            np.testing.assert_array_equal(mx[b, j], blk.max(dim=1).values.numpy())
