@@ -683,21 +683,22 @@ def run_quest(args):
     bs = wl.block_size
     budget = max(1, args.quest // bs)
     kc, vc = vals["k_cache"], vals["v_cache"]
-    kmeta = pkv.quest_block_minmax(kc, st["tables"], st["lens"])
+    ks, vs = vals.get("k_scale"), vals.get("v_scale")  # E4M3 caches
+    kmeta = pkv.quest_block_minmax(kc, st["tables"], st["lens"], meta_dtype=W.DTYPES[wl.act_dtype])
     B = len(st["ids"])
     sel = torch.empty(B, wl.num_kv_heads, budget, dtype=torch.int32, device=dev)
     slen = torch.empty(B, wl.num_kv_heads, dtype=torch.int32, device=dev)
     out = torch.empty_like(vals["q"])
 
     def quest_step():
-        pkv.paged_kv_append(vals["k_new"], vals["v_new"], st["slots"], kc, vc)
-        pkv.quest_append_minmax(vals["k_new"], st["slots"], kmeta, bs)
+        pkv.paged_kv_append(vals["k_new"], vals["v_new"], st["slots"], kc, vc, ks, vs)
+        pkv.quest_append_minmax(vals["k_new"], st["slots"], kmeta, bs, k_scale=ks)
         pkv.quest_select(vals["q"], kmeta, st["tables"], st["lens"], bs, budget, sel, slen)
-        pkv.paged_attention_decode_sparse(vals["q"], kc, vc, sel, slen, wl.scale, out=out)
+        pkv.paged_attention_decode_sparse(vals["q"], kc, vc, sel, slen, wl.scale, out=out, k_scale=ks, v_scale=vs)
 
     def full_step():
         pkv.paged_attention_decode_append(vals["q"], vals["k_new"], vals["v_new"], st["slots"], kc, vc, st["tables"],
-                                          st["lens"], wl.scale, out=out)
+                                          st["lens"], wl.scale, out=out, k_scale=ks, v_scale=vs)
 
     def graph_us(fn):
         # one CUDA graph per phase: the four small launches of a QUEST step are
@@ -724,11 +725,11 @@ def run_quest(args):
         return round(e0.elapsed_time(e1) * 1e3 / args.steps, 2)
 
     res = {}
-    phases = {"append": lambda: pkv.paged_kv_append(vals["k_new"], vals["v_new"], st["slots"], kc, vc),
-              "metadata": lambda: pkv.quest_append_minmax(vals["k_new"], st["slots"], kmeta, bs),
+    phases = {"append": lambda: pkv.paged_kv_append(vals["k_new"], vals["v_new"], st["slots"], kc, vc, ks, vs),
+              "metadata": lambda: pkv.quest_append_minmax(vals["k_new"], st["slots"], kmeta, bs, k_scale=ks),
               "select": lambda: pkv.quest_select(vals["q"], kmeta, st["tables"], st["lens"], bs, budget, sel, slen),
               "sparse_decode": lambda: pkv.paged_attention_decode_sparse(vals["q"], kc, vc, sel, slen, wl.scale,
-                                                                         out=out)}
+                                                                         out=out, k_scale=ks, v_scale=vs)}
     for name, fn in phases.items():
         res[f"{name}_us"] = graph_us(fn)
     for name, fn in (("full", full_step), ("quest", quest_step)):

@@ -311,24 +311,34 @@ int paged_block_swap(void* k_cache, void* v_cache, const int32_t* block_ids, int
  * channel-wise minimum and maximum key; for a query the upper bound
  * U = sum_c max(q_c * min_c, q_c * max_c) of q.k over the block's keys;
  * attention reads only the K blocks with the largest bounds.
- * kmeta: [num_blocks][num_kv_heads][2][head_dim] of the cache's 16-bit type
- * (min row, then max row, over the block's filled slots).  16-bit caches only.
+ * kmeta: [num_blocks][num_kv_heads][2][head_dim] of the queries' 16-bit
+ * type (min row, then max row, over the block's filled slots).  With a
+ * 16-bit cache that is the cache's type.  With an E4M3 cache (Ultralytics
+ * glossary, section "Related techniques": an 8-bit cache) kmeta holds the
+ * decoded codes without the per-tensor scale -- every E4M3 value is exact in
+ * binary16 and bfloat16 -- so the bounds are the true bounds divided by
+ * k_scale (> 0), which ranks the blocks identically.
  * ---------------------------------------------------------------------- */
 
-/* Recompute kmeta for every block the given sequences use (their filled
- * slots).  Shared blocks get the same values from each sharer. */
+/* Recompute kmeta (of meta_dtype: PKV_F16 or PKV_BF16; cache_dtype is
+ * meta_dtype or PKV_E4M3) for every block the given sequences use (their
+ * filled slots).  Shared blocks get the same values from each sharer. */
 int quest_block_minmax(const void* k_cache, const int32_t* block_tables, int max_blocks_per_seq,
                        const int32_t* context_lens, int num_seqs, int num_kv_heads, int block_size,
-                       int head_dim, int num_blocks, int cache_dtype, void* kmeta, void* stream);
+                       int head_dim, int num_blocks, int cache_dtype, int meta_dtype, void* kmeta,
+                       void* stream);
 
-/* Update kmeta with newly appended keys k_new [num_tokens][num_kv_heads][head_dim]
- * at slot_mapping (as given to paged_kv_append): a token at offset 0 of its
- * block starts the block's metadata, later offsets widen it.  At most one
+/* Update kmeta (of act_dtype) with newly appended keys k_new
+ * [num_tokens][num_kv_heads][head_dim] (act_dtype) at slot_mapping (as given
+ * to paged_kv_append): a token at offset 0 of its block starts the block's
+ * metadata, later offsets widen it.  An E4M3 cache takes each key as the
+ * append stores it, e4m3(x / *k_scale) (k_scale: device float32; ignored
+ * for 16-bit caches), and the metadata takes that code's value.  At most one
  * token per block per call (one decode step); slots < 0 are skipped.
  * Copy-on-write copies do not carry metadata: recompute it for the copies. */
 int quest_append_minmax(const void* k_new, const int64_t* slot_mapping, int num_tokens,
-                        int num_kv_heads, int block_size, int head_dim, int num_blocks,
-                        int cache_dtype, void* kmeta, void* stream);
+                        int num_kv_heads, int block_size, int head_dim, int num_blocks, int act_dtype,
+                        int cache_dtype, const float* k_scale, void* kmeta, void* stream);
 
 /* Select, per (sequence, kv head), the budget_blocks blocks with the largest
  * bounds (the bound of a kv head is the largest over its query heads; equal

@@ -263,24 +263,33 @@ class DecodePlan:
         return self.out
 
 
-def quest_block_minmax(k_cache, block_tables, context_lens, kmeta=None, stream=None):
+def quest_block_minmax(k_cache, block_tables, context_lens, kmeta=None, stream=None, meta_dtype=None):
     """Per-block channel min/max of the keys (QUEST metadata) for every block the sequences use;
-    returns kmeta [num_blocks, Hkv, 2, D] of the cache type."""
+    returns kmeta [num_blocks, Hkv, 2, D] in the queries' 16-bit type (meta_dtype: default the
+    cache's type, bfloat16 for an E4M3 cache, whose metadata holds the unscaled code values)."""
     NB, Hkv, bs, D = k_cache.shape
+    if meta_dtype is None:
+        meta_dtype = kmeta.dtype if kmeta is not None else (
+            torch.bfloat16 if _code(k_cache) == E4M3 else k_cache.dtype)
     if kmeta is None:
-        kmeta = torch.zeros(NB, Hkv, 2, D, dtype=k_cache.dtype, device=k_cache.device)
+        kmeta = torch.zeros(NB, Hkv, 2, D, dtype=meta_dtype, device=k_cache.device)
+    if kmeta.dtype != meta_dtype:
+        raise ValueError("quest_block_minmax: kmeta must be of meta_dtype")
     _require_cuda(k_cache.device, k_cache=k_cache, block_tables=block_tables, context_lens=context_lens, kmeta=kmeta)
     _native.call("quest_block_minmax", _ptr(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
-                 block_tables.shape[0], Hkv, bs, D, NB, _code(k_cache), _ptr(kmeta), _stream(stream, k_cache.device))
+                 block_tables.shape[0], Hkv, bs, D, NB, _code(k_cache), _code(kmeta), _ptr(kmeta),
+                 _stream(stream, k_cache.device))
     return kmeta
 
 
-def quest_append_minmax(k_new, slot_mapping, kmeta, block_size, stream=None):
-    """Widen QUEST metadata with newly appended keys k_new [T, Hkv, D] at slot_mapping (int64 [T])."""
+def quest_append_minmax(k_new, slot_mapping, kmeta, block_size, stream=None, k_scale=None):
+    """Widen QUEST metadata with newly appended keys k_new [T, Hkv, D] at slot_mapping (int64 [T]).
+    For an E4M3 cache pass its k_scale (device float32 [1]): each key enters as the append stores it."""
     T, Hkv, D = k_new.shape
-    _require_cuda(k_new.device, k_new=k_new, slot_mapping=slot_mapping, kmeta=kmeta)
+    _require_cuda(k_new.device, k_new=k_new, slot_mapping=slot_mapping, kmeta=kmeta, k_scale=k_scale)
     _native.call("quest_append_minmax", _ptr(k_new), _ptr(slot_mapping), T, Hkv, block_size, D, kmeta.shape[0],
-                 _code(k_new), _ptr(kmeta), _stream(stream, k_new.device))
+                 _code(k_new), E4M3 if k_scale is not None else _code(k_new), _ptr(k_scale), _ptr(kmeta),
+                 _stream(stream, k_new.device))
 
 
 def quest_select(q, kmeta, block_tables, context_lens, block_size, budget_blocks, sel_tables=None, sel_lens=None,

@@ -32,8 +32,8 @@ SIGNATURES = {
                                              P, P, I32, P]),
     "paged_attention_decode_sparse": (I32, [P, P, P, P, I32, P, I32, I32, I32, I32, I32, I32, F32, P, I32, I32, P,
                                             P, I32, P, SZ, P]),
-    "quest_block_minmax": (I32, [P, P, I32, P, I32, I32, I32, I32, I32, I32, P, P]),
-    "quest_append_minmax": (I32, [P, P, I32, I32, I32, I32, I32, I32, P, P]),
+    "quest_block_minmax": (I32, [P, P, I32, P, I32, I32, I32, I32, I32, I32, I32, P, P]),
+    "quest_append_minmax": (I32, [P, P, I32, I32, I32, I32, I32, I32, I32, P, P, P]),
     "quest_select": (I32, [P, P, P, I32, P, I32, I32, I32, I32, I32, I32, I32, I32, P, P, P, SZ, P]),
     "quest_workspace_size": (SZ, [I32, I32, I32]),
     "pkv_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32, I32]),

@@ -385,12 +385,14 @@ int paged_attention_decode_sparse(const void* q, const void* k_cache, const void
 
 int quest_block_minmax(const void* k_cache, const int32_t* block_tables, int max_blocks_per_seq,
                        const int32_t* context_lens, int num_seqs, int num_kv_heads, int block_size, int head_dim,
-                       int num_blocks, int cache_dtype, void* kmeta, void* stream) {
+                       int num_blocks, int cache_dtype, int meta_dtype, void* kmeta, void* stream) {
     if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0 ||
         head_dim <= 0 || head_dim % 8 != 0)
         return fail(PKV_ERR_INVALID, "quest_block_minmax: sizes must be positive, head_dim a multiple of 8");
-    if (cache_dtype != PKV_F16 && cache_dtype != PKV_BF16)
-        return fail(PKV_ERR_INVALID, "quest_block_minmax: the cache must be PKV_F16 or PKV_BF16");
+    if (meta_dtype != PKV_F16 && meta_dtype != PKV_BF16)
+        return fail(PKV_ERR_INVALID, "quest_block_minmax: meta_dtype must be PKV_F16 or PKV_BF16");
+    if (cache_dtype != meta_dtype && cache_dtype != PKV_E4M3)
+        return fail(PKV_ERR_INVALID, "quest_block_minmax: the cache must be of meta_dtype or PKV_E4M3");
     if (num_seqs == 0) return PKV_OK;
     if (!k_cache || !block_tables || !context_lens || !kmeta) return fail(PKV_ERR_INVALID, "quest_block_minmax: null pointer");
     if (!aligned(k_cache, 16) || !aligned(kmeta, 16)) return fail(PKV_ERR_INVALID, "quest_block_minmax: misaligned");
@@ -398,24 +400,30 @@ int quest_block_minmax(const void* k_cache, const int32_t* block_tables, int max
     if (!err) return fail(PKV_ERR_CUDA, "quest_block_minmax: cannot resolve the device error word");
     QuestMetaParams p{k_cache, block_tables, context_lens, kmeta, err, num_seqs, max_blocks_per_seq, num_kv_heads,
                       block_size, head_dim, num_blocks};
-    cudaError_t e = launch_quest_minmax(p, cache_dtype, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_quest_minmax(p, meta_dtype, cache_dtype, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail("quest_block_minmax: launch", e);
 }
 
 int quest_append_minmax(const void* k_new, const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
-                        int block_size, int head_dim, int num_blocks, int cache_dtype, void* kmeta, void* stream) {
+                        int block_size, int head_dim, int num_blocks, int act_dtype, int cache_dtype,
+                        const float* k_scale, void* kmeta, void* stream) {
     if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0 || head_dim <= 0 || head_dim % 8 != 0)
         return fail(PKV_ERR_INVALID, "quest_append_minmax: sizes must be positive, head_dim a multiple of 8");
-    if (cache_dtype != PKV_F16 && cache_dtype != PKV_BF16)
-        return fail(PKV_ERR_INVALID, "quest_append_minmax: the cache must be PKV_F16 or PKV_BF16");
+    if (act_dtype != PKV_F16 && act_dtype != PKV_BF16)
+        return fail(PKV_ERR_INVALID, "quest_append_minmax: act_dtype must be PKV_F16 or PKV_BF16");
+    if (cache_dtype != act_dtype && cache_dtype != PKV_E4M3)
+        return fail(PKV_ERR_INVALID, "quest_append_minmax: the cache must be of act_dtype or PKV_E4M3");
     if (num_tokens == 0) return PKV_OK;
     if (!k_new || !slot_mapping || !kmeta) return fail(PKV_ERR_INVALID, "quest_append_minmax: null pointer");
+    if (cache_dtype == PKV_E4M3 && !k_scale)
+        return fail(PKV_ERR_INVALID, "quest_append_minmax: an E4M3 cache needs k_scale");
     if (!aligned(k_new, 16) || !aligned(kmeta, 16) || !aligned(slot_mapping, 8))
         return fail(PKV_ERR_INVALID, "quest_append_minmax: misaligned");
     int* err = device_error_word();
     if (!err) return fail(PKV_ERR_CUDA, "quest_append_minmax: cannot resolve the device error word");
-    QuestAppendParams p{k_new, slot_mapping, kmeta, err, num_tokens, num_kv_heads, block_size, head_dim, num_blocks};
-    cudaError_t e = launch_quest_append_minmax(p, cache_dtype, static_cast<cudaStream_t>(stream));
+    QuestAppendParams p{k_new, slot_mapping, cache_dtype == PKV_E4M3 ? k_scale : nullptr, kmeta, err, num_tokens,
+                        num_kv_heads, block_size, head_dim, num_blocks};
+    cudaError_t e = launch_quest_append_minmax(p, act_dtype, cache_dtype, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail("quest_append_minmax: launch", e);
 }
 

@@ -113,6 +113,7 @@ struct QuestMetaParams {
 struct QuestAppendParams {
     const void* k_new;
     const int64_t* slot_mapping;
+    const float* k_scale;  // E4M3 cache only
     void* kmeta;
     int* err;
     int num_tokens;
@@ -142,8 +143,8 @@ struct QuestSelectParams {
     int group_heads;  // kv heads per bound item (set by launch_quest_select)
 };
 
-cudaError_t launch_quest_minmax(const QuestMetaParams& p, int dtype, cudaStream_t s);
-cudaError_t launch_quest_append_minmax(const QuestAppendParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_quest_minmax(const QuestMetaParams& p, int meta, int cache, cudaStream_t s);
+cudaError_t launch_quest_append_minmax(const QuestAppendParams& p, int act, int cache, cudaStream_t s);
 cudaError_t launch_quest_select(const QuestSelectParams& p, int dtype, int G, cudaStream_t s);
 
 cudaError_t launch_append(const AppendParams& p, int act, int cache, cudaStream_t stream);

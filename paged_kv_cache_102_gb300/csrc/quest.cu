@@ -5,9 +5,13 @@
 // of q.k over the block's keys; attention then reads only the K blocks with
 // the largest bounds.
 //
-// Metadata layout: kmeta [num_blocks][Hkv][2][D] in the cache's 16-bit type
-// (row 0 = min, row 1 = max over the block's filled slots; min and max of
-// 16-bit values are themselves exact 16-bit values).
+// Metadata layout: kmeta [num_blocks][Hkv][2][D] in the queries' 16-bit type
+// (row 0 = min, row 1 = max over the block's filled slots).  For a 16-bit
+// cache that is the cache's type, and min and max of 16-bit values are exact
+// 16-bit values.  For an E4M3 cache the metadata holds the decoded codes
+// without the per-tensor scale (every E4M3 value is exact in binary16 and in
+// bfloat16): the bounds are then the true bounds divided by k_scale > 0,
+// which ranks the blocks identically.
 #include <cfloat>
 
 #include "kernels.h"
@@ -23,6 +27,27 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
     Vec16<T>::to_float(u, f);
 }
 
+// 8 consecutive cache elements -> floats (E4M3: the codes' values, unscaled).
+template <int C>
+__device__ __forceinline__ void load8(const void* src, float* f) {
+    if constexpr (C == kE4M3) {
+        const uint2 u = *reinterpret_cast<const uint2*>(src);
+        const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>((w[i] >> (16 * j)) & 0xffffu));
+                const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+                f[4 * i + 2 * j] = t.x;
+                f[4 * i + 2 * j + 1] = t.y;
+            }
+        }
+    } else {
+        unpack8<C>(*reinterpret_cast<const uint4*>(src), f);
+    }
+}
+
 template <int T>
 __device__ __forceinline__ uint4 pack8(const float* f) {
     uint4 u;
@@ -35,9 +60,10 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 }  // namespace
 
 // Full recompute: one thread per (sequence, logical block, kv head, 8-channel
-// chunk) over the block's filled slots.
-template <int T>
+// chunk) over the block's filled slots.  T: metadata type, C: cache type.
+template <int T, int C>
 __global__ void __launch_bounds__(256) quest_minmax_kernel(QuestMetaParams p) {
+    constexpr int EB = C == kE4M3 ? 1 : 2;  // bytes per cache element
     const int chunks = p.head_dim / 8;
     const int64_t per_seq = static_cast<int64_t>(p.max_blocks_per_seq) * p.num_kv_heads * chunks;
     const int64_t total = per_seq * p.num_seqs;
@@ -67,12 +93,12 @@ __global__ void __launch_bounds__(256) quest_minmax_kernel(QuestMetaParams p) {
             mn[e] = FLT_MAX;
             mx[e] = -FLT_MAX;
         }
-        const uint16_t* base = static_cast<const uint16_t*>(p.k_cache) +
-                               ((static_cast<int64_t>(blk) * p.num_kv_heads + kvh) * p.block_size) * p.head_dim +
-                               c * 8;
+        const unsigned char* base =
+            static_cast<const unsigned char*>(p.k_cache) +
+            (((static_cast<int64_t>(blk) * p.num_kv_heads + kvh) * p.block_size) * p.head_dim + c * 8) * EB;
         for (int t = 0; t < filled; ++t) {
             float f[8];
-            unpack8<T>(*reinterpret_cast<const uint4*>(base + static_cast<int64_t>(t) * p.head_dim), f);
+            load8<C>(base + static_cast<int64_t>(t) * p.head_dim * EB, f);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 mn[e] = fminf(mn[e], f[e]);
@@ -87,9 +113,13 @@ __global__ void __launch_bounds__(256) quest_minmax_kernel(QuestMetaParams p) {
 
 // Incremental update with newly appended keys: the first slot of a block
 // starts its metadata, later slots widen it.  At most one new token per block
-// per call (as one decode step gives).
-template <int T>
+// per call (as one decode step gives).  T: query / key / metadata type; an
+// E4M3 cache (C) first stores each key as the append does, e4m3(x / k_scale)
+// (binary32 division, round to nearest even, saturating), and the metadata
+// takes the stored code's value.
+template <int T, int C>
 __global__ void __launch_bounds__(256) quest_append_minmax_kernel(QuestAppendParams p) {
+    const float ks = C == kE4M3 ? *p.k_scale : 1.0f;
     const int chunks = p.head_dim / 8;
     const int64_t total = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * chunks;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -108,6 +138,17 @@ __global__ void __launch_bounds__(256) quest_append_minmax_kernel(QuestAppendPar
         const bool first = slot % p.block_size == 0;
         float k[8];
         unpack8<T>(*reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_new) + th * p.head_dim + c * 8), k);
+        if constexpr (C == kE4M3) {
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const uint16_t lo = __nv_cvt_float_to_fp8(__fdiv_rn(k[e], ks), __NV_SATFINITE, __NV_E4M3);
+                const uint16_t hi = __nv_cvt_float_to_fp8(__fdiv_rn(k[e + 1], ks), __NV_SATFINITE, __NV_E4M3);
+                const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(lo | (hi << 8)));
+                const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+                k[e] = t.x;
+                k[e + 1] = t.y;
+            }
+        }
         uint16_t* meta = static_cast<uint16_t*>(p.kmeta) + ((blk * p.num_kv_heads + kvh) * 2) * p.head_dim + c * 8;
         float mn[8], mx[8];
         if (first) {
@@ -648,25 +689,37 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(QuestSelectPar
     }
 }
 
-cudaError_t launch_quest_minmax(const QuestMetaParams& p, int dtype, cudaStream_t s) {
+cudaError_t launch_quest_minmax(const QuestMetaParams& p, int meta, int cache, cudaStream_t s) {
     const int64_t total = static_cast<int64_t>(p.num_seqs) * p.max_blocks_per_seq * p.num_kv_heads * (p.head_dim / 8);
     if (total == 0) return cudaSuccess;
     const int blocks = static_cast<int>(total / 256 + 1 < 152 * 32 ? total / 256 + 1 : 152 * 32);
-    if (dtype == kBF16)
-        quest_minmax_kernel<kBF16><<<blocks, 256, 0, s>>>(p);
-    else
-        quest_minmax_kernel<kF16><<<blocks, 256, 0, s>>>(p);
+    if (cache == kE4M3) {
+        if (meta == kBF16)
+            quest_minmax_kernel<kBF16, kE4M3><<<blocks, 256, 0, s>>>(p);
+        else
+            quest_minmax_kernel<kF16, kE4M3><<<blocks, 256, 0, s>>>(p);
+    } else if (meta == kBF16) {
+        quest_minmax_kernel<kBF16, kBF16><<<blocks, 256, 0, s>>>(p);
+    } else {
+        quest_minmax_kernel<kF16, kF16><<<blocks, 256, 0, s>>>(p);
+    }
     return cudaGetLastError();
 }
 
-cudaError_t launch_quest_append_minmax(const QuestAppendParams& p, int dtype, cudaStream_t s) {
+cudaError_t launch_quest_append_minmax(const QuestAppendParams& p, int act, int cache, cudaStream_t s) {
     const int64_t total = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * (p.head_dim / 8);
     if (total == 0) return cudaSuccess;
     const int blocks = static_cast<int>(total / 256 + 1 < 152 * 16 ? total / 256 + 1 : 152 * 16);
-    if (dtype == kBF16)
-        quest_append_minmax_kernel<kBF16><<<blocks, 256, 0, s>>>(p);
-    else
-        quest_append_minmax_kernel<kF16><<<blocks, 256, 0, s>>>(p);
+    if (cache == kE4M3) {
+        if (act == kBF16)
+            quest_append_minmax_kernel<kBF16, kE4M3><<<blocks, 256, 0, s>>>(p);
+        else
+            quest_append_minmax_kernel<kF16, kE4M3><<<blocks, 256, 0, s>>>(p);
+    } else if (act == kBF16) {
+        quest_append_minmax_kernel<kBF16, kBF16><<<blocks, 256, 0, s>>>(p);
+    } else {
+        quest_append_minmax_kernel<kF16, kF16><<<blocks, 256, 0, s>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -236,3 +236,81 @@ def test_sparse_decode_e4m3_cache(pkv, path):
     want = oracle.sparse_decode(bits(q), oracle.BF16, kc.numpy(), vc.numpy(), oracle.E4M3, sel, slen, scale,
                                 k_scale=ks, v_scale=vs)
     assert_attention_close(out, want, TOL["e4m3"])
+
+
+@pytest.mark.parametrize("act,Hq,Hkv,D,bs", [("bf16", 32, 4, 128, 16), ("f16", 16, 8, 64, 32)])
+def test_quest_e4m3_cache_metadata_selection_and_step(pkv, act, Hq, Hkv, D, bs):
+    """QUEST over an E4M3 cache: metadata (full, and widened by a step's keys
+    that the append quantises with k_scale) equal to the oracle's decoded
+    codes; selection equal to the oracle's (which scales the bounds by
+    k_scale) where the cut has a margin; the whole step's output within the
+    E4M3 tolerance of the oracle's sparse decode on its own selection."""
+    g = torch.Generator().manual_seed(Hq + D)
+    ctx = [0, 40, 700, 2000, 2900]
+    B = len(ctx)
+    NB = sum(-(-(c + 1) // bs) for c in ctx) + 3
+    ref = RefBlockManager(NB, bs, free_list=torch.randperm(NB, generator=g).numpy())
+    for i, c in enumerate(ctx):
+        ref.add_sequence(i, c)
+    slots = np.array([ref.append_slot(i)[0] for i in range(B)], np.int64)
+    maxb = max(len(t) for t in ref.tables.values())
+    tables = np.zeros((B, maxb), np.int32)
+    for i in range(B):
+        tables[i, : len(ref.tables[i])] = ref.tables[i]
+    lens = np.array([c + 1 for c in ctx], np.int32)
+    kc = torch.randint(0, 256, (NB, Hkv, bs, D), dtype=torch.uint8, generator=g)
+    vc = torch.randint(0, 256, (NB, Hkv, bs, D), dtype=torch.uint8, generator=g)
+    kc[(kc & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    vc[(vc & 0x7F) == 0x7F] = 0x3C
+    q = torch.randn(B, Hq, D, generator=g).to(DT[act])
+    k_new = torch.randn(B, Hkv, D, generator=g).to(DT[act])
+    v_new = torch.randn(B, Hkv, D, generator=g).to(DT[act])
+    ks, vs = 0.0123, 0.0171
+    dev = torch.device("cuda")
+    dk, dv = kc.to(dev), vc.to(dev)
+    ksd, vsd = torch.tensor([ks], device=dev), torch.tensor([vs], device=dev)
+    t_d, l_d = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
+    l0 = torch.from_numpy(np.maximum(lens - 1, 1)).to(dev)
+    kmeta = pkv.quest_block_minmax(dk, t_d, l0, meta_dtype=DT[act])
+    pkv.paged_kv_append(k_new.to(dev), v_new.to(dev), torch.from_numpy(slots).to(dev), dk, dv, ksd, vsd)
+    pkv.quest_append_minmax(k_new.to(dev), torch.from_numpy(slots).to(dev), kmeta, bs, k_scale=ksd)
+    full = pkv.quest_block_minmax(dk, t_d, l_d, meta_dtype=DT[act])
+    torch.cuda.synchronize()
+    kbits = dk.cpu().numpy()
+    # the appended codes are the oracle's
+    rk, rv = kc.numpy().copy(), vc.numpy().copy()
+    oracle.append(bits(k_new), bits(v_new), ACT_CODE[DT[act]], slots, rk, rv, oracle.E4M3, k_scale=ks, v_scale=vs)
+    assert np.array_equal(kbits, rk) and np.array_equal(dv.cpu().numpy(), rv)
+    mn, mx = oracle.quest_block_minmax(kbits, oracle.E4M3, tables, lens)
+    meta = kmeta.float().cpu().numpy().astype(np.float64)
+    meta_full = full.float().cpu().numpy().astype(np.float64)
+    for b in range(B):
+        for j in range(-(-int(lens[b]) // bs)):
+            blk = tables[b, j]
+            np.testing.assert_array_equal(meta_full[blk, :, 0], mn[b, j])
+            np.testing.assert_array_equal(meta_full[blk, :, 1], mx[b, j])
+            if lens[b] > 1 or j > 0:
+                np.testing.assert_array_equal(meta[blk], meta_full[blk])  # incremental == recompute
+    for budget in (2, 16):
+        sel, slen = pkv.quest_select(q.to(dev), full, t_d, l_d, bs, budget)
+        out = pkv.paged_attention_decode_sparse(q.to(dev), dk, dv, sel, slen, 0.08, k_scale=ksd, v_scale=vsd)
+        torch.cuda.synchronize()
+        want_sel, want_len, bounds = oracle.quest_select(bits(q), ACT_CODE[DT[act]], kbits, oracle.E4M3, tables,
+                                                         lens, budget, k_scale=ks)
+        sel_h, slen_h = sel.cpu().numpy(), slen.cpu().numpy()
+        unique = np.zeros((B, Hkv), bool)
+        for b in range(B):
+            n = -(-int(lens[b]) // bs)
+            for h in range(Hkv):
+                if n <= budget:
+                    unique[b, h] = True
+                    assert list(sel_h[b, h, :n]) == list(tables[b, :n]) and slen_h[b, h] == lens[b]
+                    continue
+                order = np.sort(bounds[b, h, :n])[::-1]
+                if order[budget - 1] - order[budget] > MARGIN * max(1.0, abs(order[budget - 1])):
+                    unique[b, h] = True
+                    assert list(sel_h[b, h, :budget]) == list(want_sel[b, h, :budget])
+                    assert slen_h[b, h] == want_len[b, h]
+        want = oracle.sparse_decode(bits(q), ACT_CODE[DT[act]], kbits, dv.cpu().numpy(), oracle.E4M3, want_sel,
+                                    want_len, 0.08, k_scale=ks, v_scale=vs)
+        _assert_rows_close(out, want, unique, Hq // Hkv, TOL["e4m3"])
