@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
                 // test), so probabilities stay below 2^kRescaleLog2 and l and
                 // acc, both relative to m, stay consistent.
                 if (mx > m[g] + kRescaleLog2) {
-                    const float alpha = m[g] == -INFINITY ? 0.f : exp2f(m[g] - mx);
+                    const float alpha = m[g] == -INFINITY ? 0.f : fast_exp2(m[g] - mx);
                     m[g] = mx;
                     l[g] *= alpha;
 #pragma unroll
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
                 }
 #pragma unroll
                 for (int pp = 0; pp < C::PASSES; ++pp) {
-                    pr[pp][g] = sc[pp][g] == -INFINITY ? 0.f : exp2f(sc[pp][g] - m[g]);
+                    pr[pp][g] = sc[pp][g] == -INFINITY ? 0.f : fast_exp2(sc[pp][g] - m[g]);
                     l[g] += pr[pp][g];
                 }
             }
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 2 ? 3 : 2))
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
             const float mw = red_m[w * G + g];
-            const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
+            const float wt = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
             num = fmaf(wt, red_acc[(w * G + g) * D + d], num);
             den = fmaf(wt, red_l[w * G + g], den);
         }

@@ -892,8 +892,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                         uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
                         for (int g = 0; g < G; g += 2) {
-                            const float p0 = sc[t][g] == -INFINITY ? 0.f : exp2f(sc[t][g] - M[g]);
-                            const float p1 = sc[t][g + 1] == -INFINITY ? 0.f : exp2f(sc[t][g + 1] - M[g + 1]);
+                            // M is finite (every item has a token); 2^-inf = 0 for masked rows
+                            const float p0 = fast_exp2(sc[t][g] - M[g]);
+                            const float p1 = fast_exp2(sc[t][g + 1] - M[g + 1]);
                             sum[g] += p0;
                             sum[g + 1] += p1;
                             uint32_t hi, lo;
@@ -906,7 +907,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                         unsigned char* pt = pb + (2 * t + (row >> 6)) * 1024;
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
-                            const float pv = sc[t][g] == -INFINITY ? 0.f : exp2f(sc[t][g] - M[g]);
+                            const float pv = fast_exp2(sc[t][g] - M[g]);  // 2^-inf = 0 for masked rows
                             sum[g] += pv;
                             const int chunk = ((row & 63) >> 3) ^ g;
                             *reinterpret_cast<uint16_t*>(pt + g * 128 + chunk * 16 + (row & 7) * 2) =
@@ -965,7 +966,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             for (int g = 0; g < G; ++g) {
                 const float Mg = stats[b * 16 + g];
                 const float Lg = stats[b * 16 + 8 + g];
-                const float val = o[g] / Lg * vmul;
+                // L >= 1 (the max token's weight is 1): one reciprocal per head
+                const float val = o[g] * (__frcp_rn(Lg) * vmul);
                 const size_t hrow = static_cast<size_t>(it.seq) * p.num_q_heads + it.kvh * G + g;
                 if (single) {
                     static_cast<uint16_t*>(p.out)[hrow * kTcD + d] = float_to_act<ACT>(val);

@@ -166,5 +166,6 @@ cudaError_t launch_decode_bf16_e4m3(const DecodeParams& p, int D, int BS, int G,
 bool decode_tc_supported(int num_seqs, int head_dim, int block_size, int group, int act, int cache,
                          int partition_size);
 cudaError_t launch_decode_tc(const DecodeParams& p, int act, int cache, int BS, int G, int variant, cudaStream_t s);
+cudaError_t launch_decode_tc_e4m3(const DecodeParams& p, int act, int BS, int G, int variant, cudaStream_t s);
 
 }  // namespace pkv

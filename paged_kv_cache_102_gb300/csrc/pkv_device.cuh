@@ -96,6 +96,16 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
+// 2^x with the hardware's base-2 exponential (PTX ex2.approx.ftz.f32: relative
+// error below 2^-22 by the PTX ISA, subnormal results flushed to zero, 2^-inf =
+// +0).  The softmax weights it computes are rounded to 16 (or 8) bits or summed
+// in float32 afterwards, so its error is far below the output's rounding.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- element conversion ---------------------------------------------------
 // 16 bytes of cache elements -> floats (8 for 16-bit types, 16 for E4M3).
 template <int T>
