@@ -865,11 +865,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     }
                 }
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-#pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1)
-                        mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
-                }
+                for (int g = 0; g < G; ++g) mx[g] = warp_max(mx[g]);
                 if (lane == 0) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) red_max[q4 * 8 + g] = mx[g];

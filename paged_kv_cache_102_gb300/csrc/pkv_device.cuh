@@ -106,6 +106,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Maximum of x over the 32 lanes of the warp, in one warp-wide reduction
+// (redux.sync.max.f32; every lane of the warp must call it).
+__device__ __forceinline__ float warp_max(float x) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // ---- element conversion ---------------------------------------------------
 // 16 bytes of cache elements -> floats (8 for 16-bit types, 16 for E4M3).
 template <int T>
