@@ -181,10 +181,11 @@ size_t pkv_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int h
  * pkv_resolve_partition_size -- the partition size in tokens that
  * paged_attention_decode uses for these arguments (a value >= the longest
  * possible context means a single pass), or -1 if partition_size is not
- * accepted.  PKV_PARTITION_AUTO gives 512 when num_q_heads/num_kv_heads >= 4,
- * head_dim is 128 and num_seqs <= 2048 (the shapes the tensor-core kernel
- * serves), or 256 when num_seqs * num_kv_heads * the number of 512-token
- * partitions of the longest possible context is in [256, 1024); else 1024.
+ * accepted.  PKV_PARTITION_AUTO gives 512 when num_q_heads/num_kv_heads >= 4
+ * and head_dim is 128 (the shapes the tensor-core kernel serves; batches of
+ * more than 2048 sequences run as several of its launches), or 256 when
+ * num_seqs * num_kv_heads * the number of 512-token partitions of the longest
+ * possible context is in [256, 1024); else 1024.
  * Host only.
  */
 int pkv_resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -271,9 +272,9 @@ enum pkv_kernel_path {
  * pkv_set_kernel_path -- choose the decode kernel for later calls in this
  * process (all threads, all devices); returns the previous choice, or -1 for
  * an unknown value.  PKV_PATH_AUTO uses the tensor-core kernel (2 CTAs per
- * SM) when
- * num_q_heads/num_kv_heads >= 4, head_dim is 128, the cache is 16-bit and
- * partitions are at most 512 tokens, and the CUDA-core kernel otherwise.
+ * SM) when num_q_heads/num_kv_heads >= 4, head_dim is 128, the cache is
+ * 16-bit or E4M3 and partitions are at most 512 tokens, and the CUDA-core
+ * kernel otherwise.
  * Forcing a tensor-core path on a shape it does not serve makes
  * paged_attention_decode return PKV_ERR_INVALID.  Both kernels compute the
  * same function; this is a tuning and testing switch.
@@ -365,7 +366,8 @@ size_t quest_workspace_size(int num_seqs, int num_kv_heads, int max_blocks_per_s
 /* paged_attention_decode over per-(sequence, kv head) block lists, such as
  * quest_select's: tables [num_seqs][num_kv_heads][max_sel_blocks], lengths
  * [num_seqs][num_kv_heads].  Same kernels as paged_attention_decode (the
- * tensor-core kernel serves num_seqs * num_kv_heads <= 2048); the workspace
+ * tensor-core kernel takes at most 2048 (sequence, kv head) rows per launch
+ * and larger batches in several launches); the workspace
  * is pkv_workspace_size(..., max_sel_blocks, ...). */
 int paged_attention_decode_sparse(const void* q, const void* k_cache, const void* v_cache,
                                   const int32_t* sel_tables, int max_sel_blocks,

@@ -2,6 +2,7 @@
 // choice, workspace carving and kernel dispatch.  Declarations and the
 // contract of each call are in include/pagedkv.h.
 #include <atomic>
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 #include <string>
@@ -112,7 +113,7 @@ int pkv_resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, 
         // the tensor-core grouped-query kernel holds 512 tokens of scores in tensor
         // memory; the CUDA-core kernel amortises its per-partition work over 1024
         const int G = num_q_heads / num_kv_heads;
-        const bool grouped = G >= 4 && head_dim == 128 && num_seqs <= 2048;
+        const bool grouped = G >= 4 && head_dim == 128;
         P = grouped ? kAutoPartitionGrouped : kAutoPartition;
         if (grouped) {
             auto items = [&](long long p) { return static_cast<long long>(num_seqs) * num_kv_heads * ((max_ctx + p - 1) / p); };
@@ -304,16 +305,40 @@ static int decode_impl(const char* fn, const void* q, const void* k_cache, const
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     const int path = g_kernel_path.load();
-    const int table_rows = per_kvh_tables ? num_seqs * num_kv_heads : num_seqs;
-    const bool tc_ok = decode_tc_supported(table_rows, head_dim, block_size, G, act_dtype, cache_dtype, P);
+    // the tensor-core kernel keeps per-row tables in shared memory: larger
+    // batches run as several launches over consecutive sequences
+    const int rows_per_seq = per_kvh_tables ? num_kv_heads : 1;
+    const bool tc_ok = rows_per_seq <= decode_tc_max_rows() &&
+                       decode_tc_supported(head_dim, block_size, G, act_dtype, cache_dtype, P);
     if ((path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA) && !tc_ok)
         return fail(PKV_ERR_INVALID, F + ": " + "the tensor-core path needs head_dim 128, a 16-bit "
                                      "cache, 2/4/8 query heads per kv head and partitions of at most 512 tokens");
     const bool use_tc = path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA ||
                         (path == PKV_PATH_AUTO && tc_ok && G >= 4);
-    if (use_tc)
-        e = launch_decode_tc(p, act_dtype, cache_dtype, block_size, G, path == PKV_PATH_TENSOR ? 0 : 1, s);
-    else if (act_dtype == PKV_F16)
+    if (use_tc) {
+        const int chunk = decode_tc_max_rows() / rows_per_seq;
+        const size_t act_bytes = 2;
+        e = cudaSuccess;
+        for (int s0 = 0; s0 < num_seqs && e == cudaSuccess; s0 += chunk) {
+            DecodeParams c = p;
+            c.num_seqs = std::min(chunk, num_seqs - s0);
+            c.q = static_cast<const char*>(q) + static_cast<size_t>(s0) * num_q_heads * head_dim * act_bytes;
+            c.out = static_cast<char*>(out) + static_cast<size_t>(s0) * num_q_heads * head_dim * act_bytes;
+            c.block_tables = block_tables + s0 * p.table_seq_stride;
+            c.context_lens = context_lens + static_cast<int64_t>(s0) * p.lens_seq_stride;
+            if (new_slots) {
+                c.k_new = static_cast<const char*>(k_new) + static_cast<size_t>(s0) * num_kv_heads * head_dim * act_bytes;
+                c.v_new = static_cast<const char*>(v_new) + static_cast<size_t>(s0) * num_kv_heads * head_dim * act_bytes;
+                c.new_slots = new_slots + s0;
+            }
+            if (max_parts > 1) {
+                const size_t hrow0 = static_cast<size_t>(s0) * num_q_heads * max_parts;
+                c.ws_ml = p.ws_ml + hrow0 * 2;
+                c.ws_o = p.ws_o + hrow0 * head_dim;
+            }
+            e = launch_decode_tc(c, act_dtype, cache_dtype, block_size, G, path == PKV_PATH_TENSOR ? 0 : 1, s);
+        }
+    } else if (act_dtype == PKV_F16)
         e = cache_dtype == PKV_E4M3 ? launch_decode_f16_e4m3(p, head_dim, block_size, G, s)
                                     : launch_decode_f16_f16(p, head_dim, block_size, G, s);
     else

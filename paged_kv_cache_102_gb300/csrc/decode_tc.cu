@@ -4,9 +4,10 @@
 
 namespace pkv {
 
-bool decode_tc_supported(int num_seqs, int head_dim, int block_size, int group, int act, int cache,
-                         int partition_size) {
-    return num_seqs <= kTcMaxSeqs && head_dim == kTcD && (block_size == 16 || block_size == 32) &&
+int decode_tc_max_rows() { return kTcMaxSeqs; }
+
+bool decode_tc_supported(int head_dim, int block_size, int group, int act, int cache, int partition_size) {
+    return head_dim == kTcD && (block_size == 16 || block_size == 32) &&
            (group == 2 || group == 4 || group == 8) && (act == kF16 || act == kBF16) &&
            (cache == act || cache == kE4M3) && partition_size <= kTcMaxTiles * kTcTile && encode_fn() != nullptr;
 }

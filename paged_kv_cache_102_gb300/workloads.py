@@ -87,6 +87,19 @@ WORKLOADS = {
         description="13B-shaped decode with an FP8-E4M3 cache: batch 256, 40 MHA heads, head_dim "
                     "128, per-tensor scales from the N(0,1) data, bf16 q/out, context_lens uniform "
                     "in [256, 4096]"),
+    # shapes at the edges of the tensor-core kernel's envelope
+    "gqa_g2": Workload(
+        "gqa_g2", 128, 16, 8, 128, 16, "bf16", "bf16", ("lognormal", 1024, 1.0, 16, 8192),
+        description="GQA decode with 2 query heads per KV head: batch 128, 16 query heads over 8 KV heads, "
+                    "head_dim 128, bf16, block 16, lengths as gqa_bs16"),
+    "gqa_d64": Workload(
+        "gqa_d64", 128, 64, 8, 64, 16, "bf16", "bf16", ("lognormal", 1024, 1.0, 16, 8192),
+        description="GQA decode at head_dim 64: batch 128, 64 query heads over 8 KV heads, bf16, block 16, "
+                    "lengths as gqa_bs16"),
+    "gqa_wide": Workload(
+        "gqa_wide", 4096, 64, 8, 128, 16, "bf16", "bf16", ("uniform", 64, 512),
+        description="GQA decode over a wide batch: 4096 sequences, 64 query heads over 8 KV heads, head_dim "
+                    "128, bf16, block 16, context_lens uniform in [64, 512]"),
     "long_gqa": Workload(
         "long_gqa", 8, 32, 8, 128, 16, "bf16", "bf16", ("fixed", (32767,) * 8),
         description="8 sequences x 32768 tokens (after the append), 32 query heads over 8 KV heads, "

@@ -524,3 +524,41 @@ def test_decode_tensor_core_many_rows(kernel_path, cache):
     pkv.set_kernel_path(pkv.PATH_TENSOR_2CTA)
     got = _run_decode(pkv, q, kc, vc, tables, lens, scale, 128, ks, vs)
     assert_attention_close(got, want, TOL[cache])
+
+
+def test_decode_tensor_core_more_than_one_launch_of_rows(kernel_path):
+    """More sequences than one tensor-core launch serves (2048 table rows):
+    the library runs consecutive chunks of sequences, each its own persistent
+    launch, then one merge.  2500 sequences with the new token fused in, a
+    few long enough to split into several partitions, every output against
+    the oracle and every appended row bit for bit."""
+    pkv = kernel_path
+    g = _gen(2500)
+    B, Hq, Hkv, D, bs = 2500, 32, 8, 128, 16
+    lens = torch.randint(1, 96, (B,), generator=g).numpy()
+    lens[[0, 1047, 2047, 2048, 2499]] = [1500, 700, 513, 1100, 2000]  # split-K rows on both sides of the cut
+    q, kc, vc, tables, lens = _random_paged(g, B, Hq, Hkv, D, bs, lens, "bf16", "bf16")
+    k_new = torch.randn(B, Hkv, D, generator=g).to(torch.bfloat16)
+    v_new = torch.randn(B, Hkv, D, generator=g).to(torch.bfloat16)
+    slots = np.array([oracle.slot_of(tables[b], int(lens[b]) - 1, bs) for b in range(B)], np.int64)
+    rk, rv = bits(kc).copy(), bits(vc).copy()
+    oracle.append(bits(k_new), bits(v_new), oracle.BF16, slots, rk, rv, oracle.BF16)
+    scale = 1.0 / math.sqrt(D)
+    want = oracle.paged_decode(bits(q), oracle.BF16, rk, rv, oracle.BF16, tables, lens, scale)
+    dk, dv = kc.cuda(), vc.cuda()
+    assert pkv.resolve_partition_size(B, Hq, Hkv, D, tables.shape[1], bs, -1) == 512  # the tensor-core choice
+    got = pkv.paged_attention_decode_append(q.cuda(), k_new.cuda(), v_new.cuda(), torch.from_numpy(slots).cuda(),
+                                            dk, dv, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                                            scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(dk), rk) and np.array_equal(bits(dv), rv)
+    assert_attention_close(got, want, TOL["bf16"])
+    # per-(sequence, kv head) tables: 300 x 8 = 2400 rows, also more than one launch
+    Bs = 300
+    sel = np.repeat(tables[:Bs, None, :], Hkv, axis=1).copy()
+    slen = np.repeat(lens[:Bs, None], Hkv, axis=1).astype(np.int32)
+    out = pkv.paged_attention_decode_sparse(q[:Bs].contiguous().cuda(), dk, dv, torch.from_numpy(sel).cuda(),
+                                            torch.from_numpy(slen).cuda(), scale)
+    torch.cuda.synchronize()
+    want_s = oracle.sparse_decode(bits(q[:Bs]), oracle.BF16, rk, rv, oracle.BF16, sel, slen, scale)
+    assert_attention_close(out, want_s, TOL["bf16"])
