@@ -488,8 +488,8 @@ def time_workload(pkv, W, name, dev, args, peak):
     P = pkv.resolve_partition_size(B, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, st["tables_h"].shape[1],
                                    wl.block_size, -1)
     # the library's automatic choice: tensor cores for >= 4 query heads per kv head at head_dim 128
-    # with partitions of at most 512 tokens and at most 2048 sequences
-    grouped = wl.num_q_heads // wl.num_kv_heads >= 4 and wl.head_dim == 128 and B <= 2048 and P <= 512
+    # with partitions of at most 512 tokens (batches above 2048 sequences in several launches)
+    grouped = wl.num_q_heads // wl.num_kv_heads >= 4 and wl.head_dim == 128 and P <= 512
     path = "tensor-core" if grouped else "CUDA-core"
     res = {"description": wl.description, "kernel": path, "partition_size": P,
            "decode_call_gbs": round(call_gbs, 1), "frac": round(call_gbs / peak, 4),
