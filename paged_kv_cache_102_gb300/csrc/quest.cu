@@ -556,13 +556,13 @@ __device__ __forceinline__ uint32_t bound_key(float f) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Selection, step 2: one CTA of 256 threads per (kv head, sequence) finds the
+// Selection, step 2: one CTA of 1024 threads per (kv head, sequence) finds the
 // budget_blocks largest bounds of its row by radix selection: four passes of
 // 8-bit digit histograms in shared memory give the key of the K-th largest
 // bound.  Blocks above that key are kept, and blocks equal to it are kept in
 // ascending logical order until K are chosen.  One block-wide scan over
 // contiguous per-thread ranges places the chosen blocks in logical order.
-constexpr int kTopkThreads = 256;
+constexpr int kTopkThreads = 1024;
 
 __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(QuestSelectParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -605,7 +605,7 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(QuestSelectPar
     __syncthreads();
     uint32_t mask = 0;
     for (int shift = 24; shift >= 0; shift -= 8) {
-        hist[tid] = 0;  // kTopkThreads == 256 bins
+        if (tid < 256) hist[tid] = 0;
         __syncthreads();
         const uint32_t prefix = s_prefix;
         for (int b0 = 0; b0 < nblk; b0 += kTopkThreads) {  // uniform trip count
