@@ -487,9 +487,11 @@ def time_workload(pkv, W, name, dev, args, peak):
     step_gbs = (dec_bytes + app_bytes) / (step_ms * 1e-3) / 1e9
     P = pkv.resolve_partition_size(B, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, st["tables_h"].shape[1],
                                    wl.block_size, -1)
-    # the library's automatic choice: tensor cores for >= 4 query heads per kv head at head_dim 128
-    # with partitions of at most 512 tokens (batches above 2048 sequences in several launches)
-    grouped = wl.num_q_heads // wl.num_kv_heads >= 4 and wl.head_dim == 128 and P <= 512
+    # the library's automatic choice: tensor cores for >= 4 query heads per kv head at head_dim 128, or
+    # at head_dim 64 with a 16-bit cache and an even kv-head count (two kv heads per item), with
+    # partitions of at most 512 tokens (batches above 2048 sequences in several launches)
+    dims = wl.head_dim == 128 or (wl.head_dim == 64 and wl.cache_dtype != "e4m3" and wl.num_kv_heads % 2 == 0)
+    grouped = wl.num_q_heads // wl.num_kv_heads >= 4 and dims and P <= 512
     path = "tensor-core" if grouped else "CUDA-core"
     res = {"description": wl.description, "kernel": path, "partition_size": P,
            "decode_call_gbs": round(call_gbs, 1), "frac": round(call_gbs / peak, 4),

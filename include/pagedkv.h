@@ -182,10 +182,11 @@ size_t pkv_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int h
  * paged_attention_decode uses for these arguments (a value >= the longest
  * possible context means a single pass), or -1 if partition_size is not
  * accepted.  PKV_PARTITION_AUTO gives 512 when num_q_heads/num_kv_heads >= 4
- * and head_dim is 128 (the shapes the tensor-core kernel serves; batches of
- * more than 2048 sequences run as several of its launches), or 256 when
- * num_seqs * num_kv_heads * the number of 512-token partitions of the longest
- * possible context is in [256, 1024); else 1024.
+ * and head_dim is 128, or 64 with an even num_kv_heads (the shapes the
+ * tensor-core kernel serves; batches of more than 2048 sequences run as
+ * several of its launches), or 256 when the number of its work items
+ * (num_seqs * num_kv_heads, halved at head_dim 64, * the number of 512-token
+ * partitions of the longest possible context) is in [256, 1024); else 1024.
  * Host only.
  */
 int pkv_resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -272,9 +273,11 @@ enum pkv_kernel_path {
  * pkv_set_kernel_path -- choose the decode kernel for later calls in this
  * process (all threads, all devices); returns the previous choice, or -1 for
  * an unknown value.  PKV_PATH_AUTO uses the tensor-core kernel (2 CTAs per
- * SM) when num_q_heads/num_kv_heads >= 4, head_dim is 128, the cache is
- * 16-bit or E4M3 and partitions are at most 512 tokens, and the CUDA-core
- * kernel otherwise.
+ * SM) when num_q_heads/num_kv_heads >= 4, partitions are at most 512 tokens
+ * and either head_dim is 128 with a 16-bit or E4M3 cache, or head_dim is 64
+ * with a 16-bit cache, an even num_kv_heads and tables shared by a
+ * sequence's kv heads (one item then covers kv heads 2v and 2v+1); the
+ * CUDA-core kernel otherwise.
  * Forcing a tensor-core path on a shape it does not serve makes
  * paged_attention_decode return PKV_ERR_INVALID.  Both kernels compute the
  * same function; this is a tuning and testing switch.

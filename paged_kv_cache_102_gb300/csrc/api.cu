@@ -113,10 +113,12 @@ int pkv_resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, 
         // the tensor-core grouped-query kernel holds 512 tokens of scores in tensor
         // memory; the CUDA-core kernel amortises its per-partition work over 1024
         const int G = num_q_heads / num_kv_heads;
-        const bool grouped = G >= 4 && head_dim == 128;
+        const bool grouped = G >= 4 && (head_dim == 128 || (head_dim == 64 && num_kv_heads % 2 == 0));
         P = grouped ? kAutoPartitionGrouped : kAutoPartition;
         if (grouped) {
-            auto items = [&](long long p) { return static_cast<long long>(num_seqs) * num_kv_heads * ((max_ctx + p - 1) / p); };
+            // items: (sequence, kv head, partition), or (sequence, pair of kv heads, partition) at head_dim 64
+            const int item_heads = head_dim == 64 ? num_kv_heads / 2 : num_kv_heads;
+            auto items = [&](long long p) { return static_cast<long long>(num_seqs) * item_heads * ((max_ctx + p - 1) / p); };
             if (items(P) >= kAutoGroupedItemsLow && items(P) < kAutoGroupedItemsHigh && (P / 2) % block_size == 0)
                 P /= 2;
         }
@@ -309,10 +311,12 @@ static int decode_impl(const char* fn, const void* q, const void* k_cache, const
     // batches run as several launches over consecutive sequences
     const int rows_per_seq = per_kvh_tables ? num_kv_heads : 1;
     const bool tc_ok = rows_per_seq <= decode_tc_max_rows() &&
-                       decode_tc_supported(head_dim, block_size, G, act_dtype, cache_dtype, P);
+                       decode_tc_supported(head_dim, block_size, G, act_dtype, cache_dtype, P, num_kv_heads,
+                                           per_kvh_tables);
     if ((path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA) && !tc_ok)
-        return fail(PKV_ERR_INVALID, F + ": " + "the tensor-core path needs head_dim 128, a 16-bit "
-                                     "cache, 2/4/8 query heads per kv head and partitions of at most 512 tokens");
+        return fail(PKV_ERR_INVALID, F + ": " + "the tensor-core path needs head_dim 128 (16-bit or E4M3 "
+                                     "cache) or 64 (16-bit cache, even kv heads, shared tables), 2/4/8 query "
+                                     "heads per kv head and partitions of at most 512 tokens");
     const bool use_tc = path == PKV_PATH_TENSOR || path == PKV_PATH_TENSOR_2CTA ||
                         (path == PKV_PATH_AUTO && tc_ok && G >= 4);
     if (use_tc) {
@@ -336,7 +340,8 @@ static int decode_impl(const char* fn, const void* q, const void* k_cache, const
                 c.ws_ml = p.ws_ml + hrow0 * 2;
                 c.ws_o = p.ws_o + hrow0 * head_dim;
             }
-            e = launch_decode_tc(c, act_dtype, cache_dtype, block_size, G, path == PKV_PATH_TENSOR ? 0 : 1, s);
+            e = launch_decode_tc(c, act_dtype, cache_dtype, head_dim, block_size, G, path == PKV_PATH_TENSOR ? 0 : 1,
+                                 s);
         }
     } else if (act_dtype == PKV_F16)
         e = cache_dtype == PKV_E4M3 ? launch_decode_f16_e4m3(p, head_dim, block_size, G, s)

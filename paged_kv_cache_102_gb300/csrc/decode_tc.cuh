@@ -45,6 +45,14 @@
 // (16-bit) or double (E4M3).  With 16-bit operands N = 16 columns are
 // computed for at most 8 heads: rows 8-15 of the Q and P operands alias the
 // next 1 KB of shared memory, and the matching output columns are never read.
+// head_dim 64 (PAIR): an item covers kv heads 2v and 2v+1 of a sequence (the
+// two share its block table), laid side by side as one 128-wide head: tile
+// half h holds kv head 2v+h, and the Q operand is block-diagonal (rows 0-7:
+// the queries of 2v on dimensions 0-63, rows 8-15: those of 2v+1 on 64-127,
+// zeros elsewhere), so S columns 0-7 and 8-15 are the two heads' scores.  P
+// fills all 16 rows; O = V^T P is right on dimensions 0-63 in columns 0-7 and
+// on 64-127 in columns 8-15, the only ones read.  The K/V bytes per item and
+// the MMA shapes are those of head_dim 128.
 // Every barrier wait is bounded (kWaitLimitNs); on a timeout the CTA stops
 // issuing work, drains its in-flight copies and MMAs, frees tensor memory and
 // reports kErrTimeout.
@@ -72,16 +80,18 @@ constexpr int kTcSmemPerSm = 228 * 1024;      // shared memory of one SM, includ
 constexpr int kTcQueue = 4;                   // claimed items in flight between the roles
 constexpr int kTcLenBuckets = 8;              // length buckets of the partly filled partitions
 
-template <int NS, int STG = kTcStage>
+template <int NS, int STG = kTcStage, bool PAIR = false>
 struct TcSmem {
     static constexpr int RING = 0;
     static constexpr int Q = NS * STG;
     // E4M3 cache: two 4 KB Q buffers (high + middle parts, low part + 8 zero
-    // rows) and two 8 KB P buffers (4 tiles x 16 rows x 128 one-byte codes)
-    static constexpr int QBUF = STG == kTcStage8 ? 4096 : kTcQBuf;  // one Q buffer
-    static constexpr int QBUFS = STG == kTcStage8 ? 2 : 1;          // Q buffers
+    // rows) and two 8 KB P buffers (4 tiles x 16 rows x 128 one-byte codes).
+    // Pairs of head_dim-64 kv heads: a 4 KB Q buffer (two 8-row regions of
+    // queries around 2 KB of zeros) and a 16 KB P buffer (16 rows per region).
+    static constexpr int QBUF = STG == kTcStage8 || PAIR ? 4096 : kTcQBuf;  // one Q buffer
+    static constexpr int QBUFS = STG == kTcStage8 ? 2 : 1;                  // Q buffers
     static constexpr int P = Q + QBUFS * QBUF;
-    static constexpr int PBUF = STG == kTcStage8 ? 8192 : kTcPBuf;  // one P buffer
+    static constexpr int PBUF = STG == kTcStage8 ? 8192 : PAIR ? 2 * kTcMaxTiles * 2048 : kTcPBuf;  // one P buffer
     static constexpr int PBUFS = STG == kTcStage8 ? 2 : 1;           // P buffers
     static constexpr int QUEUE = P + PBUFS * PBUF;  // item numbers [4], q shifts [4], block-table entries [4][32]
     static constexpr int BARS = (QUEUE + 2 * kTcQueue * 4 + kTcQueue * 32 * 4 + 7) / 8 * 8;
@@ -89,7 +99,7 @@ struct TcSmem {
     // item_full[4], item_empty[4] (a single Q or P buffer uses entry 0 of its pair)
     static constexpr int NBARS = 2 * NS + 13 + 2 * kTcQueue;
     static constexpr int RED = BARS + NBARS * 8;
-    static constexpr int RED_FLOATS = 64 + 32;  // red_max[4][8], red_sum[4][8], stats[2][2][8]
+    static constexpr int RED_FLOATS = 64 + 64;  // red_max[4][8], red_sum[4][8], stats[2][2][2][8]
     static constexpr int MISC = RED + RED_FLOATS * 4;
     // per row: length (int), item prefix (int, rows + 2 entries), length order (uint16)
     static constexpr int ROWS = (MISC + 16 + 15) / 16 * 16;
@@ -115,12 +125,12 @@ __device__ __forceinline__ int tc_rows(const DecodeParams& p) {
 // before r, a row of L tokens has floor(L / partition_size) of them per kv
 // head it covers, kv head major.  Items [F, F + H * prefix[rows + 1]) are the
 // partly filled last partitions of the rows listed in `order`, H per row
-// (H = the kv heads a row covers).
+// (H = the item heads a row covers: its kv heads, or at head_dim 64 the pairs
+// of kv heads, when it.kvh is the pair's index).
 __device__ __forceinline__ void tc_decode_item(int ci, const DecodeParams& p, const int* lens, const int* prefix,
-                                               const uint16_t* order, TcItem& it) {
+                                               const uint16_t* order, int H, TcItem& it) {
     const int rows = tc_rows(p);
     const int F = prefix[rows];
-    const int H = tc_per_kvh(p) ? 1 : p.num_kv_heads;
     int row, part, h;
     if (ci < F) {
         int lo = 0, hi = rows;  // the last r with prefix[r] <= ci
@@ -207,13 +217,17 @@ __device__ __forceinline__ void split3_e4m3x2(float x0, float x1, uint32_t& hi, 
     split_e4m3x2(x0 - hv.x, x1 - hv.y, mid, lo);
 }
 
-template <int ACT, int CACHE, int BS, int G, int NS>
+template <int ACT, int CACHE, int BS, int G, int NS, bool PAIR = false>
 __global__ void __launch_bounds__(kTcThreads, 2)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const __grid_constant__ CUtensorMap qmap, const DecodeParams p) {
     constexpr bool FP8 = CACHE == kE4M3;
     constexpr int STG = FP8 ? kTcStage8 : kTcStage;  // bytes of one ring stage
-    using S = TcSmem<NS, STG>;
+    // PAIR: head_dim 64, kv heads 2v and 2v+1 of a sequence in one item, as
+    // dimensions 0-63 and 64-127 of a 128-wide head (tile halves, Q regions)
+    constexpr int HD = PAIR ? 64 : kTcD;  // head_dim of the caches, queries and output
+    static_assert(!PAIR || !FP8, "pairs of head_dim-64 kv heads: 16-bit caches");
+    using S = TcSmem<NS, STG, PAIR>;
     constexpr int THREADS = kTcThreads;
     constexpr int BPT = kTcTile / BS;  // blocks per tile
     // E4M3 x E4M3 (kind::f8f6f4) has the same descriptor bits as binary16 x binary16
@@ -251,7 +265,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     uint64_t* item_empty = item_full + kTcQueue;
     float* red_max = reinterpret_cast<float*>(sm + S::RED);
     float* red_sum = red_max + 32;
-    float* stats = red_max + 64;  // [buffer][max, sum][8]
+    float* stats = red_max + 64;  // [buffer][kv head of a pair][max, sum][8]
     uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(sm + S::MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::MISC + 4);
 
@@ -261,7 +275,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     int* s_lens = reinterpret_cast<int*>(sm + S::ROWS);
     int* s_prefix = s_lens + B;
     uint16_t* s_order = reinterpret_cast<uint16_t*>(s_prefix + B + 2);
-    const int heads_per_row = tc_per_kvh(p) ? 1 : p.num_kv_heads;
+    // item heads per row (per-(sequence, kv head) tables: one; pairs need shared tables)
+    const int heads_per_row = tc_per_kvh(p) ? 1 : PAIR ? p.num_kv_heads / 2 : p.num_kv_heads;
 
     // Lengths, the exclusive prefix of full-partition items per row and the
     // rows with a partly filled partition sorted by its length, longest first
@@ -343,6 +358,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             s_prefix[B + 1] = partial;
         }
     }
+    if constexpr (PAIR) {
+        // rows 8-15 of the dimension 0-63 Q operand and rows 0-7 of the 64-127
+        // one: zero for the whole launch (the sync below orders them before any MMA)
+        for (int i = threadIdx.x; i < 2048 / 16; i += THREADS)
+            reinterpret_cast<uint4*>(qbuf + 1024)[i] = make_uint4(0u, 0u, 0u, 0u);
+        tc::fence_proxy_async_smem();
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&full[i], 1);
@@ -377,8 +399,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // Arm one ring stage with tile t of an item; `map` is the K or V tensor map.
     // Lane 0 waits for the stage and sets its byte count; lane 2j+h then loads
     // half h of block j of the tile, so one warp instruction issues the tile's
-    // 2*BPT copies.  E4M3: a token's 128 codes are one 128-byte row, so lane j
-    // loads block j whole.
+    // 2*BPT copies (PAIR: half h is block j of kv head 2v+h).  E4M3: a token's
+    // 128 codes are one 128-byte row, so lane j loads block j whole.
     auto issue_tile = [&](uint32_t& use, uint32_t parity, const TcItem& it, int phys, int t,
                           const CUtensorMap* map) {
         if ((use & 1u) != parity) {
@@ -401,8 +423,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) return false;
         if (mine) {
-            const int y = (pbj * p.num_kv_heads + it.kvh) * BS;
-            tc::tma_load_2d(ring + s * STG + half * kTcHalf + j * BS * 128, map, half * 64, y, &full[s], policy);
+            const int y = (pbj * p.num_kv_heads + (PAIR ? 2 * it.kvh + half : it.kvh)) * BS;
+            tc::tma_load_2d(ring + s * STG + half * kTcHalf + j * BS * 128, map, PAIR ? 0 : half * 64, y, &full[s],
+                            policy);
         }
         ++use;
         return true;
@@ -456,7 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             ci = __shfl_sync(0xffffffffu, ci, 0);
             it.qshift = 0;
             if (ci >= 0) {
-                tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
+                tc_decode_item(ci, p, s_lens, s_prefix, s_order, heads_per_row, it);
                 if constexpr (FP8) {
                     // q enters the MMA as E4M3 high and low parts of q x 2^-qshift:
                     // the exact power-of-2 scale puts its largest magnitude in
@@ -479,9 +502,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 if (p.new_slots != nullptr && it.tok_begin + it.n_tok == s_lens[it.row]) {
                     // fused append: this item holds the new (last) token; write it
                     // before the item is published, so before any copy of its block
-                    append_row_warp<ACT, CACHE>(p.k_new, p.v_new, p.new_slots[it.seq], it.seq, it.kvh,
-                                                p.num_kv_heads, BS, kTcD, p.num_blocks, const_cast<void*>(p.k_cache),
-                                                const_cast<void*>(p.v_cache), p.k_scale, p.v_scale, p.err, lane);
+#pragma unroll
+                    for (int h = 0; h < (PAIR ? 2 : 1); ++h)
+                        append_row_warp<ACT, CACHE>(p.k_new, p.v_new, p.new_slots[it.seq], it.seq,
+                                                    PAIR ? 2 * it.kvh + h : it.kvh, p.num_kv_heads, BS, HD,
+                                                    p.num_blocks, const_cast<void*>(p.k_cache),
+                                                    const_cast<void*>(p.v_cache), p.k_scale, p.v_scale, p.err, lane);
                 }
             }
             const int slot = nclaim % kTcQueue;
@@ -537,7 +563,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             if (ci < 0) return 0;
             // (an appended row of this item was written, and fenced for the copy
             // engine, by the scheduler before it published the item)
-            tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
+            tc_decode_item(ci, p, s_lens, s_prefix, s_order, heads_per_row, it);
             return 1;
         };
         auto issue_q = [&](const TcItem& it, int k) {
@@ -598,9 +624,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 if (k >= 1) good = tc_wait(&q_empty[0], (k - 1) & 1, abort_flag, p.err);
                 if (good) {
                     mbar_arrive_expect_tx(&q_full[0], 2 * G * 128);
-                    const int row = it.seq * p.num_q_heads + it.kvh * G;
-                    tc::tma_load_2d(qbuf, &qmap, 0, row, &q_full[0], policy);
-                    tc::tma_load_2d(qbuf + 1024, &qmap, 64, row, &q_full[0], policy);
+                    if constexpr (PAIR) {
+                        // the queries of kv head 2v (rows 0-7 of the first operand) and
+                        // of 2v+1 (rows 8-15 of the second, 3 KB in)
+                        const int row = it.seq * p.num_q_heads + 2 * it.kvh * G;
+                        tc::tma_load_2d(qbuf, &qmap, 0, row, &q_full[0], policy);
+                        tc::tma_load_2d(qbuf + 3072, &qmap, 0, row + G, &q_full[0], policy);
+                    } else {
+                        const int row = it.seq * p.num_q_heads + it.kvh * G;
+                        tc::tma_load_2d(qbuf, &qmap, 0, row, &q_full[0], policy);
+                        tc::tma_load_2d(qbuf + 1024, &qmap, 64, row, &q_full[0], policy);
+                    }
                 }
             }
             good = __shfl_sync(0xffffffffu, good, 0);
@@ -659,7 +693,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             ++nread;
             if (!good) return -1;
             if (ci < 0) return 0;
-            tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
+            tc_decode_item(ci, p, s_lens, s_prefix, s_order, heads_per_row, it);
             return 1;
         };
         auto mma_s = [&](const TcItem& it, int k) {
@@ -693,7 +727,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 #pragma unroll
                         for (int kk = 0; kk < kTcD / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kTcHalf + (kk & 3) * 32;
-                            const uint32_t qoff = (kk >> 2) * 1024 + (kk & 3) * 32;
+                            // PAIR: dimensions 64-127 read the operand 2 KB in (rows 0-7 zero)
+                            const uint32_t qoff = (kk >> 2) * (PAIR ? 2048 : 1024) + (kk & 3) * 32;
                             tc::mma_f16(tmem + b * kTcSlotCols + t * kTcN, tc::desc_sw128(kb + off, 16, 1024),
                                         tc::desc_sw128(qb + qoff, 16, 1024), IDESC_S, kk > 0);
                         }
@@ -757,7 +792,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                                        tc::desc_noswizzle(pbase + t * 2048 + j * 512, 128, 2048), IDESC_O,
                                        (t > 0 || j > 0) ? 1u : 0u);
                         } else {
-                            const uint32_t poff = (2 * t + (j >> 2)) * 1024 + (j & 3) * 32;
+                            const uint32_t poff = (2 * t + (j >> 2)) * (PAIR ? 2048 : 1024) + (j & 3) * 32;
                             tc::mma_f16(tmem + b * kTcSlotCols + kTcMaxTiles * kTcN,
                                         tc::desc_sw128(vaddr + j * 2048, kTcHalf, 1024),
                                         tc::desc_sw128(pbase + poff, 16, 1024), IDESC_O, (t > 0 || j > 0) ? 1u : 0u);
@@ -812,7 +847,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             if (named_bar_or(3, 128, !good)) return -1;
             if (tid == 0) mbar_arrive(&item_empty[slot]);
             if (ci < 0) return 0;
-            tc_decode_item(ci, p, s_lens, s_prefix, s_order, it);
+            tc_decode_item(ci, p, s_lens, s_prefix, s_order, heads_per_row, it);
             it.qshift = qshift;
             return 1;
         };
@@ -825,111 +860,121 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 0xffffffffu, tc_wait(&s_full[b], (k >> 1) & 1, abort_flag, p.err) &&
                                  (k == 0 || S::PBUFS == 2 ||
                                   tc_wait(&o_full[(k - 1) & 1], ((k - 1) >> 1) & 1, abort_flag, p.err)));
-            float sc[kTcMaxTiles][G] = {};
             // E4M3: S was computed on the stored codes and on q x 2^-qshift
             const float sl = FP8 ? p.scale_log2 * *p.k_scale * __uint_as_float(static_cast<uint32_t>(127 + it.qshift) << 23)
                                  : p.scale_log2;
-            if (good) {
-                tc::fence_after_sync();
-                if constexpr (FP8) {
-                    // column g: the high part of q, column 8 + g: the low part
-                    float lo[kTcMaxTiles][G] = {};
-#pragma unroll
-                    for (int t = 0; t < kTcMaxTiles; ++t)
-                        if (t < it.n_tiles) {
-                            tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN, sc[t]);
-                            tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN + 8, lo[t]);
-                        }
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int t = 0; t < kTcMaxTiles; ++t)
-#pragma unroll
-                        for (int g = 0; g < G; ++g) sc[t][g] += lo[t][g];
-                } else {
-#pragma unroll
-                    for (int t = 0; t < kTcMaxTiles; ++t)
-                        if (t < it.n_tiles) tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN, sc[t]);
-                    tc::tmem_wait_ld();
-                }
-                tc::fence_before_sync();  // these reads precede the next MMA into this S buffer
-                float mx[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) mx[g] = -INFINITY;
-#pragma unroll
-                for (int t = 0; t < kTcMaxTiles; ++t) {
-                    const bool valid = t < it.n_tiles && t * kTcTile + row < it.n_tok;
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        sc[t][g] = valid ? sc[t][g] * sl : -INFINITY;
-                        mx[g] = fmaxf(mx[g], sc[t][g]);
-                    }
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) mx[g] = warp_max(mx[g]);
-                if (lane == 0) {
-#pragma unroll
-                    for (int g = 0; g < G; ++g) red_max[q4 * 8 + g] = mx[g];
-                }
-            }
-            if (named_bar_or(1, 128, !good)) return false;
-            float M[G], sum[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                M[g] = fmaxf(fmaxf(red_max[g], red_max[8 + g]), fmaxf(red_max[16 + g], red_max[24 + g]));
-                sum[g] = 0.f;
-            }
             unsigned char* pb = pbuf + (S::PBUFS == 2 ? b * S::PBUF : 0);
-#pragma unroll
-            for (int t = 0; t < kTcMaxTiles; ++t) {
-                if (t < it.n_tiles) {
+            // PAIR: columns 0-7 (kv head 2v) and 8-15 (kv head 2v+1) in two
+            // passes over the same scores, each as the single-head case
+            constexpr int NH = PAIR ? 2 : 1;
+#pragma unroll 1
+            for (int hh = 0; hh < NH; ++hh) {
+                float sc[kTcMaxTiles][G] = {};
+                if (good) {
+                    tc::fence_after_sync();
                     if constexpr (FP8) {
-                        // P x 2^8 (at most 256) = hi + lo in E4M3; token `row` of
-                        // tile t holds 16 bytes: hi of heads 0-7, then lo of heads 0-7
-                        uint32_t w[4] = {0u, 0u, 0u, 0u};
+                        // column g: the high part of q, column 8 + g: the low part
+                        float lo[kTcMaxTiles][G] = {};
 #pragma unroll
-                        for (int g = 0; g < G; g += 2) {
-                            // M is finite (every item has a token); 2^-inf = 0 for masked rows
-                            const float p0 = fast_exp2(sc[t][g] - M[g]);
-                            const float p1 = fast_exp2(sc[t][g + 1] - M[g + 1]);
-                            sum[g] += p0;
-                            sum[g + 1] += p1;
-                            uint32_t hi, lo;
-                            split_e4m3x2(p0 * 256.f, p1 * 256.f, hi, lo);
-                            w[g >> 2] |= hi << (8 * (g & 3));
-                            w[2 + (g >> 2)] |= lo << (8 * (g & 3));
-                        }
-                        *reinterpret_cast<uint4*>(pb + t * 2048 + row * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int t = 0; t < kTcMaxTiles; ++t)
+                            if (t < it.n_tiles) {
+                                tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN, sc[t]);
+                                tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN + 8, lo[t]);
+                            }
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int t = 0; t < kTcMaxTiles; ++t)
+#pragma unroll
+                            for (int g = 0; g < G; ++g) sc[t][g] += lo[t][g];
                     } else {
-                        unsigned char* pt = pb + (2 * t + (row >> 6)) * 1024;
+#pragma unroll
+                        for (int t = 0; t < kTcMaxTiles; ++t)
+                            if (t < it.n_tiles)
+                                tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + t * kTcN + hh * 8, sc[t]);
+                        tc::tmem_wait_ld();
+                    }
+                    tc::fence_before_sync();  // these reads precede the next MMA into this S buffer
+                    float mx[G];
+#pragma unroll
+                    for (int g = 0; g < G; ++g) mx[g] = -INFINITY;
+#pragma unroll
+                    for (int t = 0; t < kTcMaxTiles; ++t) {
+                        const bool valid = t < it.n_tiles && t * kTcTile + row < it.n_tok;
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
-                            const float pv = fast_exp2(sc[t][g] - M[g]);  // 2^-inf = 0 for masked rows
-                            sum[g] += pv;
-                            const int chunk = ((row & 63) >> 3) ^ g;
-                            *reinterpret_cast<uint16_t*>(pt + g * 128 + chunk * 16 + (row & 7) * 2) =
-                                float_to_act<ACT>(pv);
+                            sc[t][g] = valid ? sc[t][g] * sl : -INFINITY;
+                            mx[g] = fmaxf(mx[g], sc[t][g]);
+                        }
+                    }
+#pragma unroll
+                    for (int g = 0; g < G; ++g) mx[g] = warp_max(mx[g]);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int g = 0; g < G; ++g) red_max[q4 * 8 + g] = mx[g];
+                    }
+                }
+                if (named_bar_or(1, 128, !good)) return false;
+                float M[G], sum[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    M[g] = fmaxf(fmaxf(red_max[g], red_max[8 + g]), fmaxf(red_max[16 + g], red_max[24 + g]));
+                    sum[g] = 0.f;
+                }
+#pragma unroll
+                for (int t = 0; t < kTcMaxTiles; ++t) {
+                    if (t < it.n_tiles) {
+                        if constexpr (FP8) {
+                            // P x 2^8 (at most 256) = hi + lo in E4M3; token `row` of
+                            // tile t holds 16 bytes: hi of heads 0-7, then lo of heads 0-7
+                            uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                            for (int g = 0; g < G; g += 2) {
+                                // M is finite (every item has a token); 2^-inf = 0 for masked rows
+                                const float p0 = fast_exp2(sc[t][g] - M[g]);
+                                const float p1 = fast_exp2(sc[t][g + 1] - M[g + 1]);
+                                sum[g] += p0;
+                                sum[g + 1] += p1;
+                                uint32_t hi, lo;
+                                split_e4m3x2(p0 * 256.f, p1 * 256.f, hi, lo);
+                                w[g >> 2] |= hi << (8 * (g & 3));
+                                w[2 + (g >> 2)] |= lo << (8 * (g & 3));
+                            }
+                            *reinterpret_cast<uint4*>(pb + t * 2048 + row * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                        } else {
+                            // 8-row regions of (tile, 64-token half), 1 KB apart; PAIR:
+                            // 16-row regions, 2 KB apart, rows 8-15 for kv head 2v+1
+                            unsigned char* pt = pb + (2 * t + (row >> 6)) * (PAIR ? 2048 : 1024) + hh * 1024;
+#pragma unroll
+                            for (int g = 0; g < G; ++g) {
+                                const float pv = fast_exp2(sc[t][g] - M[g]);  // 2^-inf = 0 for masked rows
+                                sum[g] += pv;
+                                const int chunk = ((row & 63) >> 3) ^ g;
+                                *reinterpret_cast<uint16_t*>(pt + g * 128 + chunk * 16 + (row & 7) * 2) =
+                                    float_to_act<ACT>(pv);
+                            }
                         }
                     }
                 }
-            }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) sum[g] += __shfl_xor_sync(0xffffffffu, sum[g], off);
-            }
-            if (lane == 0) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) red_sum[q4 * 8 + g] = sum[g];
-            }
-            tc::fence_proxy_async_smem();
-            asm volatile("bar.sync 2, 128;" ::: "memory");
-            if (tid == 0) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    stats[b * 16 + g] = M[g];
-                    stats[b * 16 + 8 + g] = red_sum[g] + red_sum[8 + g] + red_sum[16 + g] + red_sum[24 + g];
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) sum[g] += __shfl_xor_sync(0xffffffffu, sum[g], off);
                 }
-                mbar_arrive(&p_full[S::PBUFS == 2 ? b : 0]);
+                if (lane == 0) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) red_sum[q4 * 8 + g] = sum[g];
+                }
+                if (hh == NH - 1) tc::fence_proxy_async_smem();
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+                if (tid == 0) {
+                    float* st = stats + (b * 2 + hh) * 16;
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        st[g] = M[g];
+                        st[8 + g] = red_sum[g] + red_sum[8 + g] + red_sum[16 + g] + red_sum[24 + g];
+                    }
+                    if (hh == NH - 1) mbar_arrive(&p_full[S::PBUFS == 2 ? b : 0]);
+                }
             }
             return true;
         };
@@ -937,9 +982,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const int b = k & 1;
             const bool good = __all_sync(0xffffffffu, tc_wait(&o_full[b], (k >> 1) & 1, abort_flag, p.err));
             float o[G] = {};
+            // PAIR: dimensions 64-127 (warps of lane quarters 2 and 3) are kv head
+            // 2v+1, whose heads are columns 8-15
+            const int hh = PAIR ? (q4 >> 1) : 0;
             if (good) {
                 tc::fence_after_sync();
-                tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + kTcMaxTiles * kTcN, o);
+                tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + kTcMaxTiles * kTcN + hh * 8, o);
                 if constexpr (FP8) {
                     float lo[G];  // O of the low parts of P
                     tc::TmemLd<G>::load(lane_addr + b * kTcSlotCols + kTcMaxTiles * kTcN + 8, lo);
@@ -954,22 +1002,23 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             // also orders the stats written by the softmax of this item before the reads below
             if (named_bar_or(1, 128, !good)) return false;
             if (tid == 0) mbar_arrive(&o_free[b]);
-            const int d = row;
+            const int d = PAIR ? (row & 63) : row;
             const bool single = p.max_parts == 1 || s_lens[it.row] <= p.partition_size;
             // E4M3: O was computed on the stored codes and on P x 2^8
             const float vmul = FP8 ? *p.v_scale * (1.0f / 256.f) : 1.0f;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float Mg = stats[b * 16 + g];
-                const float Lg = stats[b * 16 + 8 + g];
+                const float Mg = stats[(b * 2 + hh) * 16 + g];
+                const float Lg = stats[(b * 2 + hh) * 16 + 8 + g];
                 // L >= 1 (the max token's weight is 1): one reciprocal per head
                 const float val = o[g] * (__frcp_rn(Lg) * vmul);
-                const size_t hrow = static_cast<size_t>(it.seq) * p.num_q_heads + it.kvh * G + g;
+                const int kvh = PAIR ? 2 * it.kvh + hh : it.kvh;
+                const size_t hrow = static_cast<size_t>(it.seq) * p.num_q_heads + kvh * G + g;
                 if (single) {
-                    static_cast<uint16_t*>(p.out)[hrow * kTcD + d] = float_to_act<ACT>(val);
+                    static_cast<uint16_t*>(p.out)[hrow * HD + d] = float_to_act<ACT>(val);
                 } else {
                     const size_t slot = hrow * p.max_parts + it.part;
-                    p.ws_o[slot * kTcD + d] = val;
+                    p.ws_o[slot * HD + d] = val;
                     if (d == 0) {
                         p.ws_ml[slot * 2] = Mg;
                         p.ws_ml[slot * 2 + 1] = Lg;

@@ -160,12 +160,16 @@ cudaError_t launch_decode_bf16_bf16(const DecodeParams& p, int D, int BS, int G,
 cudaError_t launch_decode_f16_e4m3(const DecodeParams& p, int D, int BS, int G, cudaStream_t s);
 cudaError_t launch_decode_bf16_e4m3(const DecodeParams& p, int D, int BS, int G, cudaStream_t s);
 
-// Tensor-core grouped-query path (head_dim 128, 16-bit cache, group 2/4/8,
-// partitions of at most 512 tokens).  variant 0: 5 stages, 1 CTA/SM;
-// variant 1: 2 stages, 2 CTAs/SM.
-bool decode_tc_supported(int head_dim, int block_size, int group, int act, int cache, int partition_size);
+// Tensor-core grouped-query path (head_dim 128 with a 16-bit or E4M3 cache,
+// or head_dim 64 with a 16-bit cache, an even kv-head count and shared
+// tables; group 2/4/8; partitions of at most 512 tokens).  variant 0: one CTA
+// per SM; variant 1: two CTAs per SM.
+bool decode_tc_supported(int head_dim, int block_size, int group, int act, int cache, int partition_size,
+                         int num_kv_heads, bool per_kvh_tables);
 int decode_tc_max_rows();  // table rows (sequences, or (sequence, kv head) pairs) of one launch
-cudaError_t launch_decode_tc(const DecodeParams& p, int act, int cache, int BS, int G, int variant, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeParams& p, int act, int cache, int head_dim, int BS, int G, int variant,
+                             cudaStream_t s);
 cudaError_t launch_decode_tc_e4m3(const DecodeParams& p, int act, int BS, int G, int variant, cudaStream_t s);
+cudaError_t launch_decode_tc_d64(const DecodeParams& p, int act, int BS, int G, int variant, cudaStream_t s);
 
 }  // namespace pkv

@@ -71,7 +71,10 @@ def test_partition_and_workspace_sizes(pkv_lib):
     assert lib.pkv_resolve_partition_size(4, 64, 8, 128, 129, 16, -1) == 512   # 4 * 8 * 5 = 160 items
     assert lib.pkv_resolve_partition_size(16, 64, 8, 128, 129, 16, -1) == 256  # 16 * 8 * 5 = 640 items
     assert lib.pkv_resolve_partition_size(32, 64, 8, 128, 129, 16, -1) == 512  # 32 * 8 * 5 = 1280 items
-    assert lib.pkv_resolve_partition_size(4, 64, 8, 64, 129, 16, -1) == 1024
+    # head_dim 64: items cover pairs of kv heads; an odd kv-head count has no pairs (CUDA-core shapes)
+    assert lib.pkv_resolve_partition_size(4, 64, 8, 64, 129, 16, -1) == 512    # 4 * 4 * 5 = 80 items
+    assert lib.pkv_resolve_partition_size(16, 64, 8, 64, 129, 16, -1) == 256   # 16 * 4 * 5 = 320 items
+    assert lib.pkv_resolve_partition_size(16, 24, 3, 64, 129, 16, -1) == 1024
     assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 8, 16, 512) == 128    # whole context fits one
     assert lib.pkv_resolve_partition_size(4, 8, 8, 128, 129, 32, 48) == -1
     assert lib.pkv_workspace_size(4, 8, 8, 128, 8, 16, 512) == 256  # the work-counter header only

@@ -35,6 +35,8 @@ CASES = [
     ("bf16", "bf16", 16, 8, 128, 16, 64),   # group 2: CUDA-core path
     ("bf16", "e4m3", 32, 4, 128, 16, -1),   # tensor-core path, E4M3 cache
     ("f16", "e4m3", 32, 4, 128, 32, 128),   # tensor-core path, E4M3 cache
+    ("bf16", "bf16", 32, 4, 64, 16, -1),    # tensor-core path, head_dim 64 (two kv heads per item)
+    ("f16", "f16", 16, 2, 64, 32, 128),     # tensor-core path, head_dim 64, one pair
 ]
 
 

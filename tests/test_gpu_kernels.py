@@ -262,12 +262,16 @@ def test_decode_empty_batch_and_streams(pkv):
 
 # ------------------------------------------------------ tensor-core GQA path ---
 TC_CASES = [
-    # act, Hq, Hkv, bs
-    ("bf16", 16, 2, 16),
-    ("bf16", 32, 8, 32),
-    ("f16", 16, 4, 16),
-    ("bf16", 8, 4, 32),
-    ("f16", 8, 2, 16),
+    # act, Hq, Hkv, bs, head_dim (64: pairs of kv heads per item)
+    ("bf16", 16, 2, 16, 128),
+    ("bf16", 32, 8, 32, 128),
+    ("f16", 16, 4, 16, 128),
+    ("bf16", 8, 4, 32, 128),
+    ("f16", 8, 2, 16, 128),
+    ("bf16", 64, 8, 16, 64),
+    ("f16", 8, 2, 32, 64),
+    ("bf16", 16, 4, 32, 64),
+    ("f16", 8, 4, 16, 64),
 ]
 
 
@@ -283,15 +287,15 @@ def kernel_path(pkv):
 @pytest.mark.parametrize("partition_size", [-1, 128, 256, 64])
 def test_decode_tensor_core_parity(kernel_path, case, path, partition_size):
     pkv = kernel_path
-    act, Hq, Hkv, bs = case
+    act, Hq, Hkv, bs, D = case
     if partition_size > 0 and partition_size % bs:
         pytest.skip("partition must be a multiple of the block size")
     if partition_size == -1 and Hq // Hkv < 4:
         partition_size = 512  # the library's own choice for group 2 is 1024, beyond the tensor-core kernel
     g = _gen(zlib.crc32(repr((case, path, partition_size)).encode()))
     lens = [1, 2, 15, 16, 17, 100, 127, 128, 129, 255, 256, 257, 511, 512, 513, 1000, 1531]
-    q, kc, vc, tables, lens = _random_paged(g, len(lens), Hq, Hkv, 128, bs, lens, act, act)
-    scale = 1.0 / math.sqrt(128)
+    q, kc, vc, tables, lens = _random_paged(g, len(lens), Hq, Hkv, D, bs, lens, act, act)
+    scale = 1.0 / math.sqrt(D)
     want = oracle.paged_decode(bits(q), ACT_CODE[DT[act]], bits(kc), bits(vc), ACT_CODE[DT[act]], tables, lens, scale)
     pkv.set_kernel_path(path)
     got = _run_decode(pkv, q, kc, vc, tables, lens, scale, partition_size)
@@ -383,13 +387,14 @@ def test_decode_split_k_merge_many_rows(kernel_path, path):
     assert_attention_close(got, want, TOL["bf16"])
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("path", [1, 2, 3])
-def test_decode_ignores_unwritten_slots(kernel_path, path):
+def test_decode_ignores_unwritten_slots(kernel_path, path, D):
     """NaN in the never-written slots of each sequence's last block does not reach the output."""
     pkv = kernel_path
-    g = _gen(77)
+    g = _gen(77 + D)
     lens = [5, 37, 130, 300]
-    q, kc, vc, tables, lens = _random_paged(g, 4, 16, 4, 128, 16, lens, "bf16", "bf16")
+    q, kc, vc, tables, lens = _random_paged(g, 4, 16, 4, D, 16, lens, "bf16", "bf16")
     want = oracle.paged_decode(bits(q), oracle.BF16, bits(kc), bits(vc), oracle.BF16, tables, lens, 0.09)
     for b, L in enumerate(lens):
         last = int(tables[b, (L - 1) // 16])
@@ -425,6 +430,13 @@ def test_tensor_path_refuses_unsupported_shapes(kernel_path):
     pkv.set_kernel_path(pkv.PATH_TENSOR)
     with pytest.raises(pkv.PagedKVError):
         _run_decode(pkv, q, kc, vc, tables, lens, 0.1, -1)
+    # head_dim 64: an odd number of kv heads has no pairs; an E4M3 cache is not served
+    q, kc, vc, tables, lens = _random_paged(g, 2, 12, 3, 64, 16, [20, 40], "bf16", "bf16")
+    with pytest.raises(pkv.PagedKVError):
+        _run_decode(pkv, q, kc, vc, tables, lens, 0.1, -1)
+    q, kc, vc, tables, lens = _random_paged(g, 2, 16, 4, 64, 16, [20, 40], "bf16", "e4m3")
+    with pytest.raises(pkv.PagedKVError):
+        _run_decode(pkv, q, kc, vc, tables, lens, 0.1, -1, 0.02, 0.02)
     with pytest.raises(ValueError):
         pkv.set_kernel_path(9)
 

@@ -29,7 +29,7 @@ def _cache_code(wl):
 
 
 
-WORKLOADS = ["tiny", "llama7b", "gqa_bs16", "gqa_bs32", "fp8_13b", "long_gqa", "gqa_fp8"]
+WORKLOADS = ["tiny", "llama7b", "gqa_bs16", "gqa_bs32", "fp8_13b", "long_gqa", "gqa_fp8", "gqa_g2", "gqa_d64"]
 
 
 @pytest.mark.parametrize("name", WORKLOADS)
