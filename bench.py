@@ -437,7 +437,7 @@ def run_native(args):
 
 
 # the grouped-query, E4M3 and long-context configurations reported beside the headline line
-OTHER_WORKLOADS = ("gqa_bs16", "gqa_bs32", "long_gqa", "fp8_13b", "gqa_fp8")
+OTHER_WORKLOADS = ("gqa_bs16", "gqa_bs32", "long_gqa", "fp8_13b", "gqa_fp8", "gqa_g2", "gqa_d64")
 
 
 def time_workload(pkv, W, name, dev, args, peak):
