@@ -5,30 +5,14 @@
 // launch template.
 #pragma once
 
-#include <cudaTypedefs.h>
-
 #include <cstring>
-#include <mutex>
 
 #include "decode_tc.cuh"
+#include "tensor_map.cuh"
 
 namespace pkv {
 
-namespace {  // each translation unit keeps its own copies (caches of the driver entry point and SM count)
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
+namespace {  // each translation unit keeps its own copy of the SM count cache
 
 // A [rows][cols] 16-bit matrix (cols 128, or 64 for head_dim-64 pairs) read
 // in boxes of 64 columns x box_rows rows, 128-byte swizzled in shared memory

@@ -17,6 +17,7 @@
 #include "kernels.h"
 #include "pkv_device.cuh"
 #include "pkv_tc.cuh"
+#include "tensor_map.cuh"
 
 namespace pkv {
 
@@ -549,6 +550,299 @@ __global__ void __launch_bounds__(kQThreads, 1) quest_bounds_kernel(QuestSelectP
     }
 }
 
+// ---- selection, step 1, kv heads in groups of 8: A straight from TMA ---------
+// When Hkv is a multiple of 8 the metadata of 8 consecutive kv heads of a
+// block is 8 consecutive 4D-byte rows.  Viewed as a 3-D tensor (64 elements
+// of a 128-byte atom; rows, 4D bytes apart; the 2D/64 atoms of a row, 128
+// bytes apart), one TMA box of 64 x 8 x 2D/64 with 128-byte swizzle lands a
+// block's 8 rows as 2D/64 consecutive 1 KB swizzle atoms of a K-major MMA
+// operand, so the A operand needs no transcription: an item (sequence, group
+// of 8 kv heads, chunk of 16 blocks) is 16 boxes, and A row 8*jl + h is the
+// metadata row of (block jl of the chunk, kv head h of the group); 8-row
+// groups (blocks) are 2D/64 KB apart.  B = [q- | q+] of the group's 8G query
+// heads (zero-padded to N) as in the kernel above, D = A B^T in tensor memory.
+// Roles (224 threads):
+//  warps 0, 6 producers of the even and the odd items: block ids and lengths
+//             fetched three items ahead, TMA boxes into a ring of stages
+//  warp 1     tensor memory; lane 0 issues the 2D/16 MMAs of an item and frees
+//             its stage when they complete
+//  warps 2-5  write B for each new (sequence, group), 8 or 16 chunks a thread
+//             with every load issued first (the epilogue of the previous item
+//             has seen its MMAs, the last to read the old B, complete); thread
+//             i reads D row i, keeps the max over its kv head's G columns and
+//             stores the bound (-inf past the context or for a bad block id)
+// Every wait is bounded; a timeout stops the CTA's roles, which drain their
+// copies and MMAs before the tensor memory is freed.
+constexpr int kQ8Blocks = 16;  // blocks per item: 16 x 8 rows = M
+constexpr int kQ8Threads = 32 * 7;
+
+template <int D, int G>
+struct QBounds8Cfg {
+    static constexpr int NATOM = 2 * D / 64;             // 128-byte atoms of a metadata row
+    static constexpr int BLK = NATOM * 1024;             // staging bytes of one block's 8 rows
+    static constexpr int STG = kQ8Blocks * BLK;          // one stage (64 KB at D = 128)
+    static constexpr int N = 8 * G < 16 ? 16 : 8 * G;    // MMA N: the group's query heads, padded
+    static constexpr int KCH = 2 * D / 8;                // 16-byte chunks of a B row
+    static constexpr int BSBO = KCH * 128;               // bytes between 8-row groups of B
+    static constexpr int B_BYTES = N * 4 * D;
+    static constexpr int NSTG_FIT = (227 * 1024 - B_BYTES - 1024 - 256) / STG;
+    static constexpr int NSTG = NSTG_FIT > 6 ? 6 : NSTG_FIT;
+    static constexpr int SMEM = NSTG * STG + B_BYTES + 1024;  // + room to align the base to 1 KB
+    static constexpr int TMEM_COLS = 2 * N <= 32 ? 32 : (2 * N <= 64 ? 64 : 128);  // two D buffers
+    static_assert(NSTG >= 2, "at least two staging stages");
+    static_assert(N * KCH % 128 == 0, "the 128 epilogue threads share B's chunks evenly");
+};
+
+template <int T, int D, int G>
+__global__ void __launch_bounds__(kQ8Threads, 1)
+    quest_bounds8_kernel(const __grid_constant__ CUtensorMap mmap, QuestSelectParams p, int64_t num_items) {
+    using Cfg = QBounds8Cfg<D, G>;
+    constexpr int NSTG = Cfg::NSTG;
+    constexpr int N = Cfg::N;
+    constexpr int KS = 2 * D / 16;  // MMA k-steps of 16 elements
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ uint64_t full[NSTG], empty[NSTG], d_full[2], d_free[2], b_full, final_bar;
+    __shared__ int armed[NSTG];  // the last item whose copies were armed on each stage
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_flag_s;
+    volatile int* abort_flag = &abort_flag_s;
+    unsigned char* sm =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
+    unsigned char* staging = sm;
+    unsigned char* Btile = sm + NSTG * Cfg::STG;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int groups = p.num_kv_heads / 8;
+    const int chunks = (p.max_blocks_per_seq + kQ8Blocks - 1) / kQ8Blocks;
+    const int64_t begin = num_items * blockIdx.x / gridDim.x;
+    const int count = static_cast<int>(num_items * (blockIdx.x + 1) / gridDim.x - begin);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTG; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+            armed[i] = -1;
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_free[i], 4);
+        }
+        mbar_init(&b_full, 4);  // the four epilogue warps
+        mbar_init(&final_bar, 1);
+        abort_flag_s = 0;
+        mbar_init_fence();
+        tc::prefetch_tensormap(&mmap);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&tmem_base_s, Cfg::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base_s;
+    // item -> (sequence, kv-head group, first block)
+    auto coords = [&](int i, int& seq, int& kvg, int& j0) {
+        const int64_t it = begin + i;
+        j0 = static_cast<int>(it % chunks) * kQ8Blocks;
+        const int64_t r = it / chunks;
+        kvg = static_cast<int>(r % groups);
+        seq = static_cast<int>(r / groups);
+    };
+    // items i and i-1 read different B (a new (sequence, group)); true for i = 0
+    auto new_b = [&](int i) {
+        if (i == 0) return true;
+        int s0, g0, j0, s1, g1, j1;
+        coords(i - 1, s0, g0, j0);
+        coords(i, s1, g1, j1);
+        return s0 != s1 || g0 != g1;
+    };
+    auto nblocks_of = [&](int L) {
+        return L >= 1 && L <= p.max_blocks_per_seq * p.block_size ? (L + p.block_size - 1) / p.block_size : 0;
+    };
+
+    if (warp == 0 || warp == 6) {
+        // ------------------------------------------------------------ producers
+        // warp 0 the even items, warp 6 the odd ones (the lanes of one copy
+        // instruction issue one after another, so two warps issue twice as
+        // fast); lane jl holds block jl of the item and loads its box
+        const int pw = warp == 0 ? 0 : 1;
+        const uint64_t policy = l2_policy_evict_first();
+        int pf_len[kQFetchAhead], pf_blk[kQFetchAhead];
+        auto fetch = [&](int i, int& len, int& blk) {
+            len = 0;
+            blk = -1;
+            if (i >= count) return;
+            int seq, kvg, j0;
+            coords(i, seq, kvg, j0);
+            len = p.context_lens[seq];
+            if (lane < kQ8Blocks && j0 + lane < p.max_blocks_per_seq)
+                blk = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks_per_seq + j0 + lane];
+        };
+#pragma unroll
+        for (int k = 0; k < kQFetchAhead; ++k) fetch(pw + 2 * k, pf_len[k], pf_blk[k]);
+        auto produce = [&](int i, int& len, int& pblk) {
+            const int s = i % NSTG;
+            if (i >= NSTG &&
+                !__all_sync(0xffffffffu, q_wait(&empty[s], ((i / NSTG) - 1) & 1, abort_flag, p.err)))
+                return false;
+            int seq, kvg, j0;
+            coords(i, seq, kvg, j0);
+            int blk = -1;
+            if (lane < kQ8Blocks && j0 + lane < nblocks_of(len)) {
+                blk = pblk;
+                if (blk < 0 || blk >= p.num_blocks) {
+                    atomicOr(p.err, kErrBadBlock);
+                    blk = -1;
+                }
+            }
+            const unsigned valid = __ballot_sync(0xffffffffu, blk >= 0);
+            fetch(i + 2 * kQFetchAhead, len, pblk);
+            if (lane == 0) {
+                armed[s] = i;  // stage s is re-armed only after item i's copies landed
+                mbar_arrive_expect_tx(&full[s], __popc(valid) * Cfg::BLK);
+            }
+            __syncwarp();
+            if (blk >= 0)
+                tc::tma_load_3d(staging + s * Cfg::STG + lane * Cfg::BLK, &mmap, 0, blk * p.num_kv_heads + kvg * 8, 0,
+                                &full[s], policy);
+            return true;
+        };
+        bool ok = true;
+        for (int base = pw; base < count && ok; base += 2 * kQFetchAhead) {
+#pragma unroll
+            for (int k = 0; k < kQFetchAhead; ++k) {  // fetch slot k holds item base + 2k
+                const int i = base + 2 * k;
+                if (i >= count || !(ok = produce(i, pf_len[k], pf_blk[k]))) break;
+            }
+        }
+        // (the copies still in flight are drained after the final barrier)
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_f16(kQRows, N, T == kBF16, false, false);
+            const uint32_t b0 = smem_addr(Btile);
+            int v = -1;  // B versions seen
+            for (int i = 0; i < count; ++i) {
+                const int s = i % NSTG, b = i & 1;
+                if (new_b(i)) {
+                    ++v;
+                    if (!q_wait(&b_full, v & 1, abort_flag, p.err)) break;
+                }
+                if (!q_wait(&full[s], (i / NSTG) & 1, abort_flag, p.err)) break;
+                if (i >= 2 && !q_wait(&d_free[b], ((i >> 1) - 1) & 1, abort_flag, p.err)) break;
+                tc::fence_after_sync();
+                const uint32_t a0 = smem_addr(staging + s * Cfg::STG);
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks)
+                    tc::mma_f16(tmem + b * N, tc::desc_sw128(a0 + (ks >> 2) * 1024 + (ks & 3) * 32, 16, Cfg::BLK),
+                                tc::desc_noswizzle(b0 + ks * 256, 128, Cfg::BSBO), idesc, ks > 0 ? 1u : 0u);
+                tc::commit(&empty[s]);
+                tc::commit(&d_full[b]);
+            }
+            // every MMA this thread issued completes before the tensor memory is freed
+            tc::commit(&final_bar);
+            if (!mbar_wait(&final_bar, 0)) atomicOr(p.err, kErrTimeout);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------- epilogue
+        const int quad = warp & 3;  // tensor-memory lanes 32*quad .. 32*quad+31
+        const int R = quad * 32 + lane;
+        const int jl = R >> 3, h = R & 7;  // block of the item, kv head of the group
+        int pf_len[kQFetchAhead], pf_blk[kQFetchAhead];
+        auto fetch = [&](int i, int& len, int& blk) {
+            len = 0;
+            blk = -1;
+            if (i >= count) return;
+            int seq, kvg, j0;
+            coords(i, seq, kvg, j0);
+            len = p.context_lens[seq];
+            if (j0 + jl < p.max_blocks_per_seq)
+                blk = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks_per_seq + j0 + jl];
+        };
+#pragma unroll
+        for (int k = 0; k < kQFetchAhead; ++k) fetch(k, pf_len[k], pf_blk[k]);
+        auto finish = [&](int i, int& len, int& pblk) {
+            const int b = i & 1;
+            int seq, kvg, j0;
+            coords(i, seq, kvg, j0);
+            const int j = j0 + jl;
+            const bool valid = j < nblocks_of(len) && pblk >= 0 && pblk < p.num_blocks;
+            fetch(i + kQFetchAhead, len, pblk);
+            if (!__all_sync(0xffffffffu, q_wait(&d_full[b], (i >> 1) & 1, abort_flag, p.err))) return false;
+            tc::fence_after_sync();
+            float best = -INFINITY;
+#pragma unroll
+            for (int c0 = 0; c0 < N; c0 += 16) {  // columns h*G .. h*G+G-1 are this row's heads
+                float v[16];
+                tc::TmemLd<16>::load(tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * N + c0, v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    if (c0 + k >= h * G && c0 + k < h * G + G) best = fmaxf(best, v[k]);
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&d_free[b]);
+            if (j < p.max_blocks_per_seq)
+                p.bounds[(static_cast<int64_t>(seq) * p.num_kv_heads + kvg * 8 + h) * p.max_blocks_per_seq + j] =
+                    valid ? best : -INFINITY;
+            return true;
+        };
+        // B = [q- | q+] of the (sequence, group) of item i, rows 8G..N-1 zero
+        const int t = threadIdx.x - 64;  // 0..127
+        auto write_b = [&](int i) {
+            int seq, kvg, j0;
+            coords(i, seq, kvg, j0);
+            const uint16_t* qrow =
+                static_cast<const uint16_t*>(p.q) + (static_cast<int64_t>(seq) * p.num_q_heads + kvg * 8 * G) * D;
+            constexpr int PER = N * Cfg::KCH / 128;  // chunks per thread
+            uint4 raw[PER];
+#pragma unroll
+            for (int r = 0; r < PER; ++r) {
+                const int idx = r * 128 + t;
+                const int n = idx / Cfg::KCH, c = idx % Cfg::KCH;
+                const int cc = c >= Cfg::KCH / 2 ? c - Cfg::KCH / 2 : c;
+                raw[r] = n < 8 * G ? *reinterpret_cast<const uint4*>(qrow + n * D + cc * 8) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int r = 0; r < PER; ++r) {
+                const int idx = r * 128 + t;
+                const int n = idx / Cfg::KCH, c = idx % Cfg::KCH;
+                uint4 pos, neg;
+                split_signs(raw[r], pos, neg);
+                *reinterpret_cast<uint4*>(Btile + (n / 8) * Cfg::BSBO + c * 128 + (n % 8) * 16) =
+                    c >= Cfg::KCH / 2 ? pos : neg;
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&b_full);
+        };
+        bool ok = true;
+        for (int base = 0; base < count && ok; base += kQFetchAhead) {
+#pragma unroll
+            for (int k = 0; k < kQFetchAhead; ++k) {  // fetch slot k holds item base + k
+                const int i = base + k;
+                if (i >= count) break;
+                // a new B: the previous item's epilogue saw the last MMAs on the old one complete
+                if (new_b(i)) write_b(i);
+                if (!(ok = finish(i, pf_len[k], pf_blk[k]))) break;
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // every copy armed on a stage has landed before the CTA exits: a stage's
+        // last arming is its latest phase (no role arms anything past the barrier)
+        for (int st = 0; st < NSTG; ++st)
+            if (armed[st] >= 0 && !mbar_wait(&full[st], (armed[st] / NSTG) & 1)) atomicOr(p.err, kErrTimeout);
+    }
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    }
+}
+
 // Order-preserving map of a float bound to an unsigned key (larger bound,
 // larger key).
 __device__ __forceinline__ uint32_t bound_key(float f) {
@@ -746,6 +1040,55 @@ cudaError_t bounds_one(const QuestSelectParams& p, cudaStream_t s) {
     quest_bounds_kernel<T, D, G><<<grid, kQThreads, smem, s>>>(p, items);
     return cudaGetLastError();
 }
+// Hkv a multiple of 8: the metadata as a 3-D tensor (64 elements; rows,
+// 4D bytes apart; 2D/64 atoms, 128 bytes apart) read in 64 x 8 x 2D/64
+// boxes, 128-byte swizzled.  False if the driver does not encode it.
+template <int D>
+bool make_meta_map(CUtensorMap* m, const QuestSelectParams& p, int T) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    constexpr int NATOM = 2 * D / 64;
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(p.num_blocks) * p.num_kv_heads, NATOM};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(4 * D), 128};
+    cuuint32_t box[3] = {64, 8, NATOM};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    return fn(m, T == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+              const_cast<void*>(p.kmeta), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+template <int T, int D, int G>
+cudaError_t bounds8_one(const QuestSelectParams& p, const CUtensorMap& m, cudaStream_t s) {
+    using Cfg = QBounds8Cfg<D, G>;
+    const int64_t items = static_cast<int64_t>(p.num_seqs) * (p.num_kv_heads / 8) *
+                          ((p.max_blocks_per_seq + kQ8Blocks - 1) / kQ8Blocks);
+    static bool configured[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
+        e = cudaFuncSetAttribute(quest_bounds8_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
+    }
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int grid = static_cast<int>(items < sms ? items : sms);
+    quest_bounds8_kernel<T, D, G><<<grid, kQ8Threads, Cfg::SMEM, s>>>(m, p, items);
+    return cudaGetLastError();
+}
+template <int T, int D>
+cudaError_t bounds8_g(const QuestSelectParams& p, const CUtensorMap& m, int G, cudaStream_t s) {
+    switch (G) {
+        case 1: return bounds8_one<T, D, 1>(p, m, s);
+        case 2: return bounds8_one<T, D, 2>(p, m, s);
+        case 4: return bounds8_one<T, D, 4>(p, m, s);
+        case 8: return bounds8_one<T, D, 8>(p, m, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
 template <int T, int D>
 cudaError_t bounds_g(const QuestSelectParams& p, int G, cudaStream_t s) {
     switch (G) {
@@ -763,14 +1106,26 @@ cudaError_t launch_quest_select(const QuestSelectParams& p_in, int dtype, int G,
     // kv heads per bound item: the largest power of two dividing Hkv with at
     // most 32 query heads (the MMA's N) and at most 128 rows
     QuestSelectParams p = p_in;
-    int hg = 1;
-    while (p.num_kv_heads % (2 * hg) == 0 && 2 * hg * G <= kQMaxN && 2 * hg <= kQRows) hg *= 2;
-    p.group_heads = hg;
     cudaError_t e;
-    if (dtype == kBF16)
-        e = p.head_dim == 128 ? bounds_g<kBF16, 128>(p, G, s) : bounds_g<kBF16, 64>(p, G, s);
-    else
-        e = p.head_dim == 128 ? bounds_g<kF16, 128>(p, G, s) : bounds_g<kF16, 64>(p, G, s);
+    CUtensorMap m;
+    const bool box8 = p.num_kv_heads % 8 == 0 && G <= 8 &&
+                      (p.head_dim == 128 ? make_meta_map<128>(&m, p, dtype) : make_meta_map<64>(&m, p, dtype));
+    if (box8) {
+        // groups of 8 kv heads: A straight from TMA boxes
+        p.group_heads = 8;
+        if (dtype == kBF16)
+            e = p.head_dim == 128 ? bounds8_g<kBF16, 128>(p, m, G, s) : bounds8_g<kBF16, 64>(p, m, G, s);
+        else
+            e = p.head_dim == 128 ? bounds8_g<kF16, 128>(p, m, G, s) : bounds8_g<kF16, 64>(p, m, G, s);
+    } else {
+        int hg = 1;
+        while (p.num_kv_heads % (2 * hg) == 0 && 2 * hg * G <= kQMaxN && 2 * hg <= kQRows) hg *= 2;
+        p.group_heads = hg;
+        if (dtype == kBF16)
+            e = p.head_dim == 128 ? bounds_g<kBF16, 128>(p, G, s) : bounds_g<kBF16, 64>(p, G, s);
+        else
+            e = p.head_dim == 128 ? bounds_g<kF16, 128>(p, G, s) : bounds_g<kF16, 64>(p, G, s);
+    }
     if (e != cudaSuccess) return e;
     const size_t smem = static_cast<size_t>(p.max_blocks_per_seq) * 8;  // key + block id per logical block
     if (smem > 48 * 1024) {

@@ -173,13 +173,15 @@ def test_sparse_decode_paths_agree_with_oracle(pkv, path):
     _assert_rows_close(out, want, unique, 32 // 4, TOL["bf16"])
 
 
-@pytest.mark.parametrize("group", [4, 8])
-def test_quest_select_many_items_per_cta(pkv, group):
-    """Enough (sequence, kv head, 32-block chunk) items that every persistent
-    CTA of the bounds kernel cycles its shared-memory ring several times."""
-    Hkv, D, bs = 2, 64, 16
-    ctx = [9000 + 37 * i for i in range(96)]  # 96 x 2 x 23 items over at most 3 CTAs per SM
-    q, kc, _, _, _, tables, _, lens = _setup("bf16", Hkv * group, Hkv, D, bs, ctx, 77 + group)
+@pytest.mark.parametrize("Hkv,group,D", [(2, 4, 64), (2, 8, 64), (8, 4, 128), (16, 8, 128), (8, 1, 64)])
+def test_quest_select_many_items_per_cta(pkv, Hkv, group, D):
+    """Enough (sequence, kv-head group, chunk) items that every persistent CTA
+    of the bounds kernel cycles its shared-memory ring several times and, with
+    8 or more kv heads (groups of 8 loaded by TMA boxes), rewrites its query
+    operand for several (sequence, group) pairs."""
+    bs = 16
+    ctx = [18000 // Hkv + 37 * i for i in range(96)]  # 96 sequences x (9 to 23 chunks) per group
+    q, kc, _, _, _, tables, _, lens = _setup("bf16", Hkv * group, Hkv, D, bs, ctx, 77 + group + Hkv)
     dev = torch.device("cuda")
     dk = kc.to(dev)
     t_d, l_d = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
