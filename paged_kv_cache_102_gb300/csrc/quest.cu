@@ -277,7 +277,8 @@ __global__ void __launch_bounds__(kQThreads, 1) quest_bounds_kernel(QuestSelectP
     const int N = (HGG + 15) / 16 * 16;           // MMA N
     const int groups = p.num_kv_heads / HG;
     const int chunks = (p.max_blocks_per_seq + BPI - 1) / BPI;
-    const int64_t begin = num_items * blockIdx.x / gridDim.x;
+    // items number fewer than 2^31 (checked on the host): 32-bit item arithmetic
+    const int begin = static_cast<int>(num_items * blockIdx.x / gridDim.x);
     const int count = static_cast<int>(num_items * (blockIdx.x + 1) / gridDim.x - begin);
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTG; ++i) {
@@ -304,11 +305,11 @@ __global__ void __launch_bounds__(kQThreads, 1) quest_bounds_kernel(QuestSelectP
     const uint32_t tmem = tmem_base_s;
     // item -> (sequence, kv-head group, first block)
     auto coords = [&](int i, int& seq, int& kvg, int& j0) {
-        const int64_t it = begin + i;
-        j0 = static_cast<int>(it % chunks) * BPI;
-        const int64_t r = it / chunks;
-        kvg = static_cast<int>(r % groups);
-        seq = static_cast<int>(r / groups);
+        const unsigned it = static_cast<unsigned>(begin + i);
+        const unsigned r = it / static_cast<unsigned>(chunks);
+        j0 = static_cast<int>(it - r * chunks) * BPI;
+        seq = static_cast<int>(r / static_cast<unsigned>(groups));
+        kvg = static_cast<int>(r) - seq * groups;
     };
     auto nblocks_of = [&](int L) {
         return L >= 1 && L <= p.max_blocks_per_seq * p.block_size ? (L + p.block_size - 1) / p.block_size : 0;
@@ -600,20 +601,21 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     constexpr int NSTG = Cfg::NSTG;
     constexpr int N = Cfg::N;
     constexpr int KS = 2 * D / 16;  // MMA k-steps of 16 elements
-    extern __shared__ __align__(1024) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem8[];  // aligned to 1 KB below
     __shared__ uint64_t full[NSTG], empty[NSTG], d_full[2], d_free[2], b_full, final_bar;
     __shared__ int armed[NSTG];  // the last item whose copies were armed on each stage
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_flag_s;
     volatile int* abort_flag = &abort_flag_s;
     unsigned char* sm =
-        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem8) + 1023) & ~uintptr_t(1023));
     unsigned char* staging = sm;
     unsigned char* Btile = sm + NSTG * Cfg::STG;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int groups = p.num_kv_heads / 8;
     const int chunks = (p.max_blocks_per_seq + kQ8Blocks - 1) / kQ8Blocks;
-    const int64_t begin = num_items * blockIdx.x / gridDim.x;
+    // items number fewer than 2^31 (checked on the host): 32-bit item arithmetic
+    const int begin = static_cast<int>(num_items * blockIdx.x / gridDim.x);
     const int count = static_cast<int>(num_items * (blockIdx.x + 1) / gridDim.x - begin);
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTG; ++i) {
@@ -641,11 +643,11 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     const uint32_t tmem = tmem_base_s;
     // item -> (sequence, kv-head group, first block)
     auto coords = [&](int i, int& seq, int& kvg, int& j0) {
-        const int64_t it = begin + i;
-        j0 = static_cast<int>(it % chunks) * kQ8Blocks;
-        const int64_t r = it / chunks;
-        kvg = static_cast<int>(r % groups);
-        seq = static_cast<int>(r / groups);
+        const unsigned it = static_cast<unsigned>(begin + i);
+        const unsigned r = it / static_cast<unsigned>(chunks);
+        j0 = static_cast<int>(it - r * chunks) * kQ8Blocks;
+        seq = static_cast<int>(r / static_cast<unsigned>(groups));
+        kvg = static_cast<int>(r) - seq * groups;
     };
     // items i and i-1 read different B (a new (sequence, group)); true for i = 0
     auto new_b = [&](int i) {
@@ -1023,6 +1025,7 @@ cudaError_t bounds_one(const QuestSelectParams& p, cudaStream_t s) {
     const int bpi = kQRows / p.group_heads;
     const int64_t items = static_cast<int64_t>(p.num_seqs) * (p.num_kv_heads / p.group_heads) *
                           ((p.max_blocks_per_seq + bpi - 1) / bpi);
+    if (items > 0x7fffffff) return cudaErrorInvalidValue;
     constexpr int smem = QBoundsCfg<D>::SMEM;
     static bool configured[kMaxDevices] = {};
     int dev = 0;
@@ -1062,6 +1065,7 @@ cudaError_t bounds8_one(const QuestSelectParams& p, const CUtensorMap& m, cudaSt
     using Cfg = QBounds8Cfg<D, G>;
     const int64_t items = static_cast<int64_t>(p.num_seqs) * (p.num_kv_heads / 8) *
                           ((p.max_blocks_per_seq + kQ8Blocks - 1) / kQ8Blocks);
+    if (items > 0x7fffffff) return cudaErrorInvalidValue;
     static bool configured[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
