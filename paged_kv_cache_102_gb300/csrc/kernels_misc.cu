@@ -24,18 +24,17 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(AppendParams p) {
     }
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int c = static_cast<int>(i % chunks_per_row);
-        const int64_t th = i / chunks_per_row;  // token * Hkv + head
-        const int h = static_cast<int>(th % p.num_kv_heads);
-        const int64_t t = th / p.num_kv_heads;
+        int64_t th, t, blk;  // th = token * Hkv + head
+        int c, h, off;
+        divmod_u(i, chunks_per_row, th, c);
+        divmod_u(th, p.num_kv_heads, t, h);
         const int64_t slot = p.slot_mapping[t];
         if (slot < 0) continue;
         if (slot >= num_slots) {
             atomicOr(p.err, kErrBadSlot);
             continue;
         }
-        const int64_t blk = slot / p.block_size;
-        const int64_t off = slot % p.block_size;
+        divmod_u(slot, p.block_size, blk, off);
         const int64_t dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * p.head_dim + c * 8;
         const int64_t src = th * p.head_dim + c * 8;
         const uint4 kin = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k) + src);
@@ -189,7 +188,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) paged_decode_merge_kernel(Me
     bool active = row < static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
     int n_parts = 0;
     if (active) {
-        const int seq = static_cast<int>(row / p.num_q_heads), h = static_cast<int>(row % p.num_q_heads);
+        int64_t seq64;
+        int h;
+        divmod_u(row, p.num_q_heads, seq64, h);
+        const int seq = static_cast<int>(seq64);
         const int L =
             p.context_lens[static_cast<int64_t>(seq) * p.lens_seq_stride + (h / p.group) * p.lens_kvh_stride];
         // a bad length was flagged by the partition kernel; one partition was written directly

@@ -100,6 +100,20 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 // error below 2^-22 by the PTX ISA, subnormal results flushed to zero, 2^-inf =
 // +0).  The softmax weights it computes are rounded to 16 (or 8) bits or summed
 // in float32 afterwards, so its error is far below the output's rounding.
+// q = x / d, r = x % d for x >= 0, d > 0: one 32-bit unsigned division when x
+// fits 32 bits (every index of the workloads this library serves), the
+// 64-bit routine otherwise.
+__device__ __forceinline__ void divmod_u(int64_t x, int d, int64_t& q, int& r) {
+    if ((static_cast<uint64_t>(x) >> 32) == 0) {
+        const uint32_t x32 = static_cast<uint32_t>(x), q32 = x32 / static_cast<uint32_t>(d);
+        q = q32;
+        r = static_cast<int>(x32 - q32 * static_cast<uint32_t>(d));
+    } else {
+        q = x / d;
+        r = static_cast<int>(x - q * d);
+    }
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -235,7 +249,9 @@ __device__ __forceinline__ void append_row_warp(const void* k_new, const void* v
         if (lane == 0) atomicOr(err, kErrBadSlot);
         return;
     }
-    const int64_t blk = slot / block_size, off = slot % block_size;
+    int64_t blk;
+    int off;
+    divmod_u(slot, block_size, blk, off);
     const int64_t dst = ((blk * num_kv_heads + kvh) * block_size + off) * head_dim;
     const int64_t src = (static_cast<int64_t>(seq) * num_kv_heads + kvh) * head_dim;
     for (int c = lane; c < head_dim / 8; c += 32) {

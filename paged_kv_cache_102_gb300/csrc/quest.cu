@@ -70,12 +70,13 @@ __global__ void __launch_bounds__(256) quest_minmax_kernel(QuestMetaParams p) {
     const int64_t total = per_seq * p.num_seqs;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int seq = static_cast<int>(i / per_seq);
-        int64_t r = i % per_seq;
-        const int j = static_cast<int>(r / (p.num_kv_heads * chunks));
-        r %= p.num_kv_heads * chunks;
-        const int kvh = static_cast<int>(r / chunks);
-        const int c = static_cast<int>(r % chunks);
+        // i = ((seq * max_blocks + j) * Hkv + kvh) * chunks + c
+        int64_t q1, q2, q3;
+        int c, kvh, j;
+        divmod_u(i, chunks, q1, c);
+        divmod_u(q1, p.num_kv_heads, q2, kvh);
+        divmod_u(q2, p.max_blocks_per_seq, q3, j);
+        const int seq = static_cast<int>(q3);
         const int L = p.context_lens[seq];
         if (L < 1 || L > p.max_blocks_per_seq * p.block_size) {
             if (j == 0 && kvh == 0 && c == 0) atomicOr(p.err, kErrBadLen);
@@ -125,18 +126,18 @@ __global__ void __launch_bounds__(256) quest_append_minmax_kernel(QuestAppendPar
     const int64_t total = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * chunks;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int c = static_cast<int>(i % chunks);
-        const int64_t th = i / chunks;
-        const int kvh = static_cast<int>(th % p.num_kv_heads);
-        const int64_t t = th / p.num_kv_heads;
+        int64_t th, t, blk;  // th = token * Hkv + kv head
+        int c, kvh, off;
+        divmod_u(i, chunks, th, c);
+        divmod_u(th, p.num_kv_heads, t, kvh);
         const int64_t slot = p.slot_mapping[t];
         if (slot < 0) continue;
         if (slot >= static_cast<int64_t>(p.num_blocks) * p.block_size) {
             atomicOr(p.err, kErrBadSlot);
             continue;
         }
-        const int64_t blk = slot / p.block_size;
-        const bool first = slot % p.block_size == 0;
+        divmod_u(slot, p.block_size, blk, off);
+        const bool first = off == 0;
         float k[8];
         unpack8<T>(*reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_new) + th * p.head_dim + c * 8), k);
         if constexpr (C == kE4M3) {
