@@ -18,7 +18,8 @@
 // The kernel is persistent and balances ragged lengths dynamically: the
 // scheduler warp of each CTA claims the next item number from a counter in the
 // workspace (zeroed before the launch) and passes it, with the item's block-
-// table entries, to the other roles through a 4-entry queue in shared memory.
+// table entries, to the other roles through a 2-entry queue in shared memory
+// (a deeper queue leaves more claimed work per CTA when the counter runs dry).
 // Roles (256 threads):
 //  warp 0    scheduler: claims, block-table entries, the fused append (fenced
 //            for the copy engine before the item is published), and for an
@@ -77,7 +78,7 @@ constexpr int kTcSlotCols = kTcMaxTiles * kTcN + kTcN;  // S (4 x 16) + O (16) p
 constexpr int kTcTmemCols = 256;              // two buffers of 80 columns, rounded to a power of 2
 constexpr int kTcMaxSeqs = 2048;              // sequences served (lengths and item prefix in shared memory)
 constexpr int kTcSmemPerSm = 228 * 1024;      // shared memory of one SM, including the 1 KB each CTA reserves
-constexpr int kTcQueue = 4;                   // claimed items in flight between the roles
+constexpr int kTcQueue = 2;                   // claimed items in flight between the roles
 constexpr int kTcLenBuckets = 8;              // length buckets of the partly filled partitions
 
 template <int NS, int STG = kTcStage, bool PAIR = false>
@@ -93,10 +94,10 @@ struct TcSmem {
     static constexpr int P = Q + QBUFS * QBUF;
     static constexpr int PBUF = STG == kTcStage8 ? 8192 : PAIR ? 2 * kTcMaxTiles * 2048 : kTcPBuf;  // one P buffer
     static constexpr int PBUFS = STG == kTcStage8 ? 2 : 1;           // P buffers
-    static constexpr int QUEUE = P + PBUFS * PBUF;  // item numbers [4], q shifts [4], block-table entries [4][32]
+    static constexpr int QUEUE = P + PBUFS * PBUF;  // item numbers, q shifts, block-table entries [32] per entry
     static constexpr int BARS = (QUEUE + 2 * kTcQueue * 4 + kTcQueue * 32 * 4 + 7) / 8 * 8;
     // full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_free[2], final,
-    // item_full[4], item_empty[4] (a single Q or P buffer uses entry 0 of its pair)
+    // item_full[kTcQueue], item_empty[kTcQueue] (a single Q or P buffer uses entry 0 of its pair)
     static constexpr int NBARS = 2 * NS + 13 + 2 * kTcQueue;
     static constexpr int RED = BARS + NBARS * 8;
     static constexpr int RED_FLOATS = 64 + 64;  // red_max[4][8], red_sum[4][8], stats[2][2][2][8]
@@ -443,8 +444,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (warp == 0) {
         // ------------------------------------------------------------ scheduler
         // Claims items, reads their block-table entries, performs the fused
-        // append and publishes each item through the queue, up to four ahead of
-        // the slowest reader.
+        // append and publishes each item through the queue, up to kTcQueue
+        // ahead of the slowest reader.
         int nclaim = 0;  // queue entries written so far
         bool ok = true;
         if (lane == 0) {
