@@ -132,15 +132,27 @@ def _dist():
     return None, 0, 1, 0
 
 
-def _traffic(workload: str):
-    """dram bytes per decode launch from a committed ncu summary, if it still matches the kernel source."""
+# every source the partition kernel (with its fused append) is compiled from
+TRAFFIC_SOURCES = ("decode_bf16_bf16.cu", "decode_inst.cuh", "decode.cuh", "pkv_device.cuh", "kernels.h")
+
+
+def traffic_sources_sha256() -> str:
+    """sha256 over the partition kernel's sources, in TRAFFIC_SOURCES order."""
     import hashlib
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_102_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic(workload: str):
+    """dram bytes per decode launch from a committed ncu summary, if it still matches the kernel sources."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-        src = open(os.path.join(ROOT, "paged_kv_cache_102_gb300", "csrc", "decode.cuh"), "rb").read()
-        if t.get("decode_cuh_sha256") != hashlib.sha256(src).hexdigest() or t.get("workload") != workload:
+        if t.get("sources_sha256") != traffic_sources_sha256() or t.get("workload") != workload:
             return None
         return float(t["dram_bytes_per_launch"])
     except Exception:
