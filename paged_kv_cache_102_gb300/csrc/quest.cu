@@ -910,8 +910,14 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(QuestSelectPar
             const uint32_t k = j < nblk ? keys[j] : 0u;
             const bool in = j < nblk && (k & mask) == prefix;
             const int digit = in ? static_cast<int>((k >> shift) & 255u) : 256;
-            const unsigned same = __match_any_sync(0xffffffffu, digit);
-            if (in && lane == __ffs(same) - 1) atomicAdd(&hist[digit], __popc(same));
+            if (shift == 24) {
+                // the top byte: a row's bounds share sign and most of the exponent,
+                // so equal digits are aggregated per warp
+                const unsigned same = __match_any_sync(0xffffffffu, digit);
+                if (in && lane == __ffs(same) - 1) atomicAdd(&hist[digit], __popc(same));
+            } else if (in) {
+                atomicAdd(&hist[digit], 1);  // spread digits, or few keys in the prefix
+            }
         }
         __syncthreads();
         if (warp == 0) {
