@@ -865,7 +865,6 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(QuestSelectPar
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int hist[256];
     __shared__ uint32_t warp_scan[kTopkThreads / 32];
-    __shared__ int warp_tokens[kTopkThreads / 32];
     __shared__ uint32_t s_prefix;
     __shared__ int s_remaining;
     const int kvh = blockIdx.x;
@@ -971,24 +970,16 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(QuestSelectPar
     uint32_t before = incl - packed;
     for (int w = 0; w < warp; ++w) before += warp_scan[w];
     int gt = static_cast<int>(before & 0xffffu), eq = static_cast<int>(before >> 16);
-    int tokens = 0;
     for (int j = lo; j < hi; ++j) {
         const uint32_t k = keys[j];
-        if (k > kth || (k == kth && eq < ties)) {
-            out_row[gt + min(eq, ties)] = blocks[j];
-            tokens += j == nblk - 1 ? L - j * p.block_size : p.block_size;
-        }
+        const bool kept = k > kth || (k == kth && eq < ties);
+        if (kept) out_row[gt + min(eq, ties)] = blocks[j];
+        // exactly budget_blocks blocks are kept, all full but the row's last
+        // block: its owner writes the selected token count
+        if (j == nblk - 1)
+            *out_len = p.budget_blocks * p.block_size - (kept ? p.block_size - (L - j * p.block_size) : 0);
         if (k > kth) ++gt;
         else if (k == kth) ++eq;
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) tokens += __shfl_xor_sync(0xffffffffu, tokens, off);
-    if (lane == 0) warp_tokens[warp] = tokens;
-    __syncthreads();
-    if (tid == 0) {
-        int total = 0;
-        for (int w = 0; w < kTopkThreads / 32; ++w) total += warp_tokens[w];
-        *out_len = total;
     }
 }
 
