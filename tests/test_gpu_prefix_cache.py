@@ -80,12 +80,12 @@ def test_prefix_cached_decode_matches_oracle(pkv_lib, cuda_device):
 
 
 @pytest.mark.parametrize("act,Hq,Hkv,D", [("f16", 8, 8, 64), ("bf16", 32, 8, 128)])
-def test_second_round_reuses_answer_blocks_decode_matches_oracle(pkv_lib, cuda_device, act, Hq, Hkv, D):
-    """A two-round dialogue on the GPU.  Round 1 writes its prompt's K/V, then
+def test_second_turn_reuses_answer_blocks_decode_matches_oracle(pkv_lib, cuda_device, act, Hq, Hkv, D):
+    """A two-turn dialogue on the GPU.  Turn 1 writes its prompt's K/V, then
     decodes its answer token by token (the fused append + decode launch, slots
-    from append_tokens, so the blocks the answer fills are registered).  Round
-    2's prompt is round 1's prompt + answer + a new user turn: every full block
-    of round 1 is reused, only the rest is written, and the decode over the
+    from append_tokens, so the blocks the answer fills are registered).  Turn
+    2's prompt is turn 1's prompt + answer + a new user turn: every full block
+    of turn 1 is reused, only the rest is written, and the decode over the
     shared blocks matches the float64 oracle on the oracle allocator's tables
     and caches, and attention over the request's own unshared K/V."""
     pkv = pkv_lib
@@ -120,7 +120,7 @@ def test_second_round_reuses_answer_blocks_decode_matches_oracle(pkv_lib, cuda_d
         return cached
 
     assert write_prompt(0, prompt) == 0
-    # round 1's answer: each step appends the newest token (its id known) and decodes
+    # turn 1's answer: each step appends the newest token (its id known) and decodes
     for i, tok in enumerate(answer):
         toks = prompt + answer[: i + 1]
         slots, pairs = bm.append_tokens([0], [tok])
@@ -154,7 +154,7 @@ def test_second_round_reuses_answer_blocks_decode_matches_oracle(pkv_lib, cuda_d
     assert np.array_equal(bits(kc), rk) and np.array_equal(bits(vc), rv)
     want = oracle.paged_decode(bits(q), code, rk, rv, code, np.asarray([ref.tables[1]], np.int32), lens2, scale)
     assert_attention_close(out, want, TOL[act])
-    # the shared blocks hold exactly the K/V round 2 would have written itself
+    # the shared blocks hold exactly the K/V turn 2 would have written itself
     kv = np.stack([_kv_for_prefix(second, p, Hkv, D) for p in range(len(second))])
     K = torch.from_numpy(kv[:, 0]).to(dt).double().permute(1, 0, 2)
     V = torch.from_numpy(kv[:, 1]).to(dt).double().permute(1, 0, 2)

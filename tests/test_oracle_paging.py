@@ -212,16 +212,16 @@ def test_reference_swap_hand_example():
 def test_reference_prefix_cache_multi_turn_hand_example():
     """Automatic prefix caching across the rounds of a dialogue, worked by hand
     (the PagedAttention notes page, section on automatic prefix caching: a
-    block is found by its own and all earlier tokens, so the next round reuses
-    the KV of the previous round's prompt AND answer).  Block size 4, free
+    block is found by its own and all earlier tokens, so the next turn reuses
+    the KV of the previous turn's prompt AND answer).  Block size 4, free
     list [5, 2, 7, 0, 1, 3, 4, 6]:
 
-    round 1  prompt 11..16 (6 tokens): block 5 = 11..14 (full, registered),
+    turn 1  prompt 11..16 (6 tokens): block 5 = 11..14 (full, registered),
              block 2 = 15, 16 (partial).  Decoding 17 and 18 fills block 2,
              which is registered under 11..18; 19 starts block 7 (slot 28).
              Freeing the request parks the registered blocks 5 and 2 on the
              LRU list; block 7 goes to the back of the free list.
-    round 2  prompt 11..19, 30, 31, 32 (12 tokens): 11..14 and 11..18 hit
+    turn 2  prompt 11..19, 30, 31, 32 (12 tokens): 11..14 and 11..18 hit
              (blocks 5 and 2), 11..32 misses and takes block 0 -> 8 tokens
              already in the pool.
     """

@@ -132,9 +132,9 @@ def test_random_requests_match_oracle(pkv_lib, seed):
 
 
 def test_multi_turn_hand_example_matches_oracle(pkv_lib):
-    """The oracle's hand-worked two-round dialogue (block size 4, free list
+    """The oracle's hand-worked two-turn dialogue (block size 4, free list
     [5, 2, 7, 0, 1, 3, 4, 6]) through the C++ manager: the answer's tokens
-    fill block 2, which the second round finds by its prefix."""
+    fill block 2, which the second turn finds by its prefix."""
     fl = [5, 2, 7, 0, 1, 3, 4, 6]
     bm = pkv_lib.BlockManager(8, 4, free_list=fl)
     ref = RefBlockManager(8, 4, free_list=fl)
@@ -155,11 +155,11 @@ def test_multi_turn_hand_example_matches_oracle(pkv_lib):
 
 
 @pytest.mark.parametrize("bs", [4, 16])
-def test_next_round_reuses_prompt_and_answer_blocks(pkv_lib, bs):
-    """A dialogue: round 1's prompt, then its answer decoded token by token with
-    ids; round 2's prompt is round 1's prompt + answer + a new user turn.  Every
-    full block of round 1 (prompt blocks and answer blocks alike) is reused,
-    whether round 1 is still running or has finished."""
+def test_next_turn_reuses_prompt_and_answer_blocks(pkv_lib, bs):
+    """A dialogue: turn 1's prompt, then its answer decoded token by token with
+    ids; turn 2's prompt is turn 1's prompt + answer + a new user turn.  Every
+    full block of turn 1 (prompt blocks and answer blocks alike) is reused,
+    whether turn 1 is still running or has finished."""
     rng = np.random.default_rng(bs)
     NB = 64
     for finished in (False, True):
@@ -180,7 +180,7 @@ def test_next_round_reuses_prompt_and_answer_blocks(pkv_lib, bs):
         cached = bm.add_sequence_cached(1, follow)
         assert cached == ref.add_sequence_cached(1, follow) == (n1 // bs) * bs
         t2, _ = bm.tables([1])
-        assert list(t2[0][: n1 // bs]) == list(t1[0][: n1 // bs])  # every full block of round 1
+        assert list(t2[0][: n1 // bs]) == list(t1[0][: n1 // bs])  # every full block of turn 1
         _state(bm, ref, NB)
 
 
