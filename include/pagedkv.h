@@ -458,8 +458,8 @@ int pkv_bm_get_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n
 
 /* Prefix caching (the PagedAttention notes page, on automatic prefix
  * caching: a block is looked up by a hash of its own tokens and all tokens
- * before it, so a later round of a dialogue reuses the KV of the earlier
- * rounds; Ultralytics glossary, section "Sharing blocks between
+ * before it, so a later turn of a dialogue reuses the KV of the earlier
+ * turns; Ultralytics glossary, section "Sharing blocks between
  * sequences": hashing full blocks extends sharing across requests).
  * Register a new sequence from its prompt token ids: every full block is
  * keyed by a chained 64-bit FNV-1a hash of (previous block's key, this

@@ -19,8 +19,8 @@ dicts, one operation at a time, written from the pages:
 
 * PagedAttention notes, section on automatic prefix caching: a KV block is
   looked up by all tokens up to and including it; equal keys are equal
-  blocks, and the stated use is a later round of a dialogue reusing the
-  KV of the earlier rounds (prompt and answer).  Here the key is the exact
+  blocks, and the stated use is a later turn of a dialogue reusing the
+  KV of the earlier turns (prompt and answer).  Here the key is the exact
   token prefix itself (a tuple), not a hash of it.  A block is registered
   when it becomes full: a prompt's full blocks when the prompt is added, and
   a block filled by decoding when its last token is appended with its id.

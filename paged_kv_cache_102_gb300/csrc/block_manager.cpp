@@ -23,8 +23,8 @@
 // the longest matching prefix, and registers the new full blocks.  Such a
 // sequence keeps the chain hash and the token ids of its partial last block;
 // pkv_bm_append_tokens appends with token ids, and a block that becomes full
-// is registered the same way, so a later round of a dialogue finds the
-// blocks of the earlier rounds' answers as well as their prompts.  A key
+// is registered the same way, so a later turn of a dialogue finds the
+// blocks of the earlier turns' answers as well as their prompts.  A key
 // that already names a block keeps it (the first registration stays).  A
 // match is confirmed by the block's own token ids and its parent's hash,
 // stored at registration.  A freed block that is registered keeps its
