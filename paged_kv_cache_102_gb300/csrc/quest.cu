@@ -568,13 +568,15 @@ __global__ void __launch_bounds__(kQThreads, 1) quest_bounds_kernel(QuestSelectP
 //             fetched three items ahead, TMA boxes into a ring of stages
 //  warp 1     tensor memory; lane 0 issues the 2D/16 MMAs of an item and frees
 //             its stage when they complete
-//  warps 2-5  write B for each new (sequence, group), 8 or 16 chunks a thread
-//             with every load issued first (the epilogue of the previous item
-//             has seen its MMAs, the last to read the old B, complete); thread
-//             i reads D row i, keeps the max over its kv head's G columns and
-//             stores the bound (-inf past the context or for a bad block id)
-// Every wait is bounded; a timeout stops the CTA's roles, which drain their
-// copies and MMAs before the tensor memory is freed.
+//  warps 2-5  write B for each new (sequence, group), N * 2D / 1024 16-byte
+//             chunks a thread (2 to 16) with every load issued first (the
+//             epilogue of the previous item has seen its MMAs, the last to
+//             read the old B, complete); thread i reads D row i, keeps the max
+//             over its kv head's G columns and stores the bound (-inf past the
+//             context or for a bad block id)
+// Every wait is bounded; a timeout stops the CTA's roles.  After the final
+// barrier one thread waits for the copies last armed on each stage, and the
+// MMA warp has waited for its MMAs, before the tensor memory is freed.
 constexpr int kQ8Blocks = 16;  // blocks per item: 16 x 8 rows = M
 constexpr int kQ8Threads = 32 * 7;
 
